@@ -1,0 +1,472 @@
+"""Benchmark of the MSA block-sparse prefill path on GB300.
+
+One step = one pass of the whole per-layer path on one batch: msa_plan
+(build_k2q_csr + work list), the attention kernel and the log-sum-exp
+combine -- the unit the MSA prefill page times per layer (vLLM PR 60684,
+Performance: build_k2q_csr + attention + combine).
+
+Workload (default): long_prefill_1m -- one request, 2048 query tokens at the
+tail of a 1,048,576-token context (8192 pages of 128 tokens), Hkv = 2,
+Hq = 16, head dim 128, E4M3 Q/K/V with per-tensor scales, top-16 pages per
+(token, KV head) drawn by the pages' rule (random earlier pages, own page
+forced, later pages masked), block_table a random permutation.
+
+Metric: selected-token attention TFLOP/s = 4 * 128 * N_pairs / time, with
+N_pairs the (query head, key) pairs the causal page mask leaves, and the
+per-layer time in microseconds; plus the roofline fraction of the dominant
+kernel.  L2 is flushed (256 MiB written) before every timed step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With N > 1 (torchrun, one process per GPU) every rank runs its own
+independent batch of the same shape (different seed): the path has no
+exchange between batches, so scaling is weak and no collective touches the
+data path; ranks meet only in a barrier and a max-reduction of the timings.
+
+--impl reference times the FP64 CPU oracle (the test-side checker) on the
+host cores on bounded samples of the same workload, as a reported baseline.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+WORKLOAD = "long_prefill_1m"
+L2_FLUSH_BYTES = 256 << 20
+KERNELS_PER_STEP = 7  # plan: prep, mark, count, scan, fill; attention; combine
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attention_kernel_traffic.json")
+ATTN_SOURCES = ["attention.cu", "ptx.cuh", "common.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]),
+                "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained",
+                                                     p["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+            "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- work counts
+
+def pair_and_page_counts(w):
+    """(query-head, key) pairs after the causal page mask, and the unique
+    (KV head, physical page) set the batch selects -- measurement
+    bookkeeping for the metric and the roofline."""
+    tk = w.topk.cpu().numpy()
+    bt = w.block_table.cpu().numpy()
+    pairs = 0
+    pages = set()
+    off = 0
+    for b in range(w.B):
+        ql, sl = w.q_lens[b], w.seq_lens[b]
+        npg = (sl + 127) // 128
+        t0 = int(w.cu_q[b])
+        ids = tk[t0:t0 + ql].astype(np.int64)          # [ql, Hkv, 16]
+        pos = np.arange(sl - ql, sl)[:, None, None]
+        own = pos // 128
+        valid = (ids >= 0) & (ids < npg) & (ids <= own)
+        # repeats count once
+        srt = np.sort(np.where(valid, ids, -1), axis=-1)
+        first = np.ones_like(srt, dtype=bool)
+        first[..., 1:] = srt[..., 1:] != srt[..., :-1]
+        keep = first & (srt >= 0)
+        keys = np.where(srt < own, 128, (pos % 128) + 1)
+        pairs += int((keys * keep).sum()) * w.G
+        for h in range(w.Hkv):
+            sel = np.unique(srt[:, h][keep[:, h]])
+            for p in sel.tolist():
+                pages.add((h, int(bt[b, p])))
+        off += npg
+    return pairs, len(pages)
+
+
+def algorithmic_bytes(w, unique_pages):
+    q = w.T * w.Hq * 128
+    kv = unique_pages * 128 * 256
+    out = w.T * w.Hq * 128 * 2
+    topk = w.T * w.Hkv * 16 * 4
+    return {"attention": q + kv, "step": q + kv + out + topk}
+
+
+def source_hash(names):
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "block_sparse_attention_prefill_gb300", "csrc")
+    for n in names:
+        with open(os.path.join(d, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic():
+    """dram bytes per attention launch from the committed ncu summary, or
+    None when the kernel source changed since it was captured."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("source_hash") != source_hash(ATTN_SOURCES):
+        return None
+    return t.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(device_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world):
+    import block_sparse_attention_prefill_gb300 as msa
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    msa.load()
+    w = workloads.make_config(args.workload, seed=args.seed + rank,
+                              device="cpu", kv_device=dev)
+    pairs, upages = pair_and_page_counts(w)
+    wd = w.to(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    ws_plan = torch.empty(msa.plan_workspace_bytes(
+        w.B, w.T, w.Hq, w.Hkv, w.total_rows, w.max_seqlen_q), dtype=torch.uint8,
+        device=dev)
+    ws_pre = torch.empty(msa.prefill_workspace_bytes(w.T, w.Hq),
+                         dtype=torch.uint8, device=dev)
+    out = torch.empty((w.T, w.Hq, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.T, w.Hq), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        plan = msa.msa_plan(wd.topk, wd.cu_q, wd.cu_k, wd.block_table,
+                            w.num_pages, w.Hq, w.total_rows, w.max_seqlen_q,
+                            w.max_seqlen_k, workspace=ws_plan, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        msa.msa_prefill_attention(wd.q, wd.kv, w.q_scale, w.k_scale,
+                                  w.v_scale, w.softmax_scale, wd.block_table,
+                                  plan, ws_pre, stream=stream)
+        if ev:
+            ev[2].record(stream)
+        msa.msa_prefill_combine(plan, ws_pre, out, lse, stream=stream)
+        if ev:
+            ev[3].record(stream)
+        return plan
+
+    clocks = ClockSampler(local)
+    for _ in range(args.warmup):
+        flush.zero_()
+        plan = step()
+    torch.cuda.synchronize()
+    status = plan.status()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+           for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        torch.distributed.barrier()
+    per = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]),
+                     e[2].elapsed_time(e[3]), e[0].elapsed_time(e[3])]
+                    for e in evs])                       # ms
+    plan_ms, attn_ms, comb_ms, step_ms = per.mean(axis=0)
+    total_ms = float(per[:, 3].sum())
+
+    # ---- end to end through host buffers (pinned), copies inside the region
+    e2e = None
+    if not args.no_e2e:
+        host = {k: getattr(w, k).cpu().pin_memory() if getattr(w, k).device.type == "cpu"
+                else getattr(w, k).cpu().pin_memory()
+                for k in ("q", "kv", "topk", "block_table", "cu_q", "cu_k")}
+        dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        out_h = torch.empty((w.T, w.Hq, 128), dtype=torch.bfloat16).pin_memory()
+        lse_h = torch.empty((w.T, w.Hq), dtype=torch.float32).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = out_h.numel() * 2 + lse_h.numel() * 4
+        e2e_steps = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            for k in host:
+                dev_in[k].copy_(host[k], non_blocking=True)
+            p = msa.msa_plan(dev_in["topk"], dev_in["cu_q"], dev_in["cu_k"],
+                             dev_in["block_table"], w.num_pages, w.Hq,
+                             w.total_rows, w.max_seqlen_q, w.max_seqlen_k,
+                             workspace=ws_plan, stream=stream)
+            msa.msa_prefill(dev_in["q"], dev_in["kv"], w.q_scale, w.k_scale,
+                            w.v_scale, w.softmax_scale, dev_in["block_table"],
+                            p, workspace=ws_pre, out=out, lse=lse,
+                            stream=stream)
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / e2e_steps
+        e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h}
+    clk = clocks.stop()
+
+    t = torch.tensor([total_ms, attn_ms, comb_ms, plan_ms, step_ms,
+                      e2e["ms"] if e2e else 0.0], dtype=torch.float64,
+                     device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    total_ms, attn_ms, comb_ms, plan_ms, step_ms, e2e_ms = t.tolist()
+    return dict(w=w, pairs=pairs, upages=upages, total_ms=total_ms,
+                attn_ms=attn_ms, comb_ms=comb_ms, plan_ms=plan_ms,
+                step_ms=step_ms, e2e=e2e, e2e_ms=e2e_ms, clocks=clk,
+                status=status, t_wall=t_wall)
+
+
+# ---------------------------------------------------------------- oracle
+
+def oracle_sample_rate(w, budget_s, nthreads):
+    """Time the FP64 oracle on a bounded sample of tokens of ``w``; returns
+    (TFLOP/s, seconds, tokens, description)."""
+    import oracle
+
+    n = 8
+    rng = np.random.default_rng(0)
+    while True:
+        toks = np.sort(rng.choice(w.T, size=min(n, w.T), replace=False))
+        t0 = time.perf_counter()
+        _, _, nk = oracle.attention(w, tokens=toks, nthreads=nthreads)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or n >= w.T:
+            break
+        n = int(min(w.T, max(n * 2, n * budget_s / max(dt, 1e-3) * 1.1)))
+    flops = 4.0 * 128 * float(nk.sum()) * w.G
+    desc = "%d of %d query tokens (all %d heads, all their selected pages)" % (
+        len(toks), w.T, w.Hq)
+    return flops / dt / 1e12, dt, len(toks), desc
+
+
+def run_reference(args, rank, world):
+    import oracle
+
+    if rank != 0:
+        return None
+    w = workloads.make_config(args.workload, seed=args.seed)
+    nthreads = os.cpu_count() or 1
+    pairs, upages = pair_and_page_counts(w)
+    per_step = max(0.05, 120.0 / max(1, args.steps + args.warmup))
+    rng = np.random.default_rng(1)
+    # size one step's token sample to the per-step budget
+    probe = np.sort(rng.choice(w.T, size=min(4, w.T), replace=False))
+    t0 = time.perf_counter()
+    oracle.attention(w, tokens=probe, nthreads=nthreads)
+    t_tok = (time.perf_counter() - t0) / len(probe)
+    ntok = int(max(1, min(w.T, per_step / max(t_tok, 1e-6))))
+    done_flops, done_t = 0.0, 0.0
+    for i in range(args.warmup + args.steps):
+        toks = np.sort(rng.choice(w.T, size=ntok, replace=False))
+        t0 = time.perf_counter()
+        _, _, nk = oracle.attention(w, tokens=toks, nthreads=nthreads)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            done_flops += 4.0 * 128 * float(nk.sum()) * w.G
+            done_t += dt
+    value = done_flops / done_t / 1e12
+    full_ms = 4.0 * 128 * pairs / (value * 1e12) * 1e3
+    sample = "%d of %d query tokens per step, all heads and selected pages" % (
+        ntok, w.T)
+    line = {
+        "impl": "reference", "metric": "selected-token attention TFLOP/s",
+        "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": full_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, args),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "note": "FP64 CPU oracle (the parity checker), not a GPU kernel; "
+                "ms_per_step is the whole workload extrapolated from the "
+                "sampled rate",
+    }
+    print(json.dumps(line))
+    return line
+
+
+def config_of(w, args):
+    return {"workload": "%s: %s" % (w.name, w.meta.get("description", "")),
+            "T": w.T, "seq_lens": w.seq_lens if w.B <= 8 else "%d requests" % w.B,
+            "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": 128, "page": 128, "topk": 16,
+            "l2": "flushed before every timed step (256 MiB write)",
+            "parallelism": "independent batch per GPU" if args.gpus > 1
+            else "single GPU"}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        torch.distributed.init_process_group(
+            backend="nccl" if args.impl == "ours" else "gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+            return
+        r = run_ours(args, rank, world)
+        if rank != 0:
+            return
+        w = r["w"]
+        peaks = load_peaks()
+        flops = 4.0 * 128 * r["pairs"]
+        step_s = r["step_ms"] / 1e3
+        value = world * flops / step_s / 1e12
+        alg = algorithmic_bytes(w, r["upages"])
+        attn_s = r["attn_ms"] / 1e3
+        achieved = alg["attention"] / attn_s / 1e9
+        fp8_peak = 2.0 * peaks["bf16_tflops"]
+        t_hbm = alg["step"] / (peaks["hbm_gbs"] * 1e9)
+        t_fp8 = flops / (fp8_peak * 1e12)
+        traffic = measured_traffic()
+        line = {
+            "metric": "selected-token attention TFLOP/s (and us per layer)",
+            "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": r["step_ms"], "us_per_layer": r["step_ms"] * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
+            "config": config_of(w, args),
+            "breakdown_us": {"plan": r["plan_ms"] * 1e3,
+                             "attention": r["attn_ms"] * 1e3,
+                             "combine": r["comb_ms"] * 1e3},
+            "roofline": {"bound": "hbm", "achieved": achieved,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": traffic,
+                         "kernel": "attention_kernel",
+                         "algorithmic_bytes": alg["attention"],
+                         "peak_source": peaks["source"] + " (burst hbm_gbs)"},
+            "roofline_step": {
+                "bound": "hbm" if t_hbm >= t_fp8 else "tensor",
+                "roofline_us": max(t_hbm, t_fp8) * 1e6,
+                "frac": max(t_hbm, t_fp8) / step_s,
+                "algorithmic_bytes": alg["step"], "flops": flops,
+                "fp8_peak_tflops": fp8_peak,
+                "fp8_peak_source": "2 x measured bf16 burst"},
+            "work": {"pairs": r["pairs"], "unique_kv_pages": r["upages"]},
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "clocks": r["clocks"], "device_status": r["status"],
+        }
+        if r["e2e"]:
+            line["e2e"] = {"value": world * flops / (r["e2e_ms"] / 1e3) / 1e12,
+                           "unit": "TFLOP/s",
+                           "h2d_bytes_per_step": r["e2e"]["h2d"],
+                           "d2h_bytes_per_step": r["e2e"]["d2h"],
+                           "ms_per_step": r["e2e_ms"]}
+        if not args.no_cpu_baseline:
+            wc = w.to("cpu")
+            nthreads = os.cpu_count() or 1
+            rate, dt, ntok, desc = oracle_sample_rate(wc, 12.0, nthreads)
+            line["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s",
+                                    "cores": nthreads, "kind": "oracle",
+                                    "sample": desc + ", %.1f s" % dt}
+        print(json.dumps(line))
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,451 @@
+// Block-sparse attention over the planned (KV head, page, token chunk) work
+// items, for sm_103a: TMA page loads gathered through block_table, E4M3
+// tensor-core MMAs (tcgen05, kind::f8f6f4) accumulating S = Q K^T and
+// O = P V in tensor memory, softmax in registers with the probabilities
+// rounded to E4M3, and one normalised partial (O, lse) per (token, query
+// head, top-k slot).
+//
+// What it computes follows vLLM PR 60684 (Details / "Kernel capability":
+// E4M3 query over E4M3 K/V with E4M3 QK and PV MMAs; Details / "Numerics":
+// softmax probabilities rounded to E4M3; Details / "Scales": q scale folded
+// into the softmax scale) and the vLLM docs for sparse_attention_msa
+// (MiniMaxM3SparseMSAImpl.forward: sparse_atten_func over the k2q CSR,
+// causal=True, page_table=block_table).  The kernel design is this
+// library's own.
+//
+// One CTA per SM, persistent over a contiguous range of the work list.
+// Warp roles (12 warps):
+//   warp 0      TMA producer: K and V halves of the item's page (2 x 16 KB)
+//   warp 1      tcgen05 issuer (one thread) and TMEM owner (512 columns)
+//   warps 2-3   Q gather: C tokens x G heads rows of 128 B with cp.async,
+//               written in the 128-byte-swizzled K-major layout
+//   warps 4-7   softmax / epilogue group 0 (even items)
+//   warps 8-11  softmax / epilogue group 1 (odd items)
+// Shared memory: 3 stages of {K, V, Q} 16 KB tiles + 2 P tiles = 176 KB.
+// TMEM: per group an S tile (128 cols) and an O tile (128 cols).
+// MMA order: QK(0), QK(1), PV(0), QK(2), PV(1), ... so that the tensor
+// cores compute item n+1's scores while item n's softmax runs.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kStages = 3;
+constexpr int kTile = 128 * 128;  // one 128 x 128 E4M3 tile, bytes
+constexpr int kThreads = 384;
+constexpr int kQLoaderThreads = 64;
+constexpr int kSoftmaxThreads = 128;
+constexpr int kTmemCols = 512;
+
+// offsets from the 1024-byte aligned base
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kStages * kTile;
+constexpr int kOffQ = kOffV + kStages * kTile;
+constexpr int kOffP = kOffQ + kStages * kTile;
+constexpr int kOffBar = kOffP + 2 * kTile;
+
+struct Barriers {
+  uint64_t kv_full[kStages];
+  uint64_t q_full[kStages];
+  uint64_t stage_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full[2];
+  uint64_t o_free[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr int kSmemBytes = kOffBar + (int)sizeof(Barriers) + 1024;
+
+struct Params {
+  const uint8_t* q;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  const int32_t* q_idx;
+  const uint8_t* slot;
+  const int4* work;
+  const int32_t* counters;
+  uint16_t* part_o;
+  float* part_lse;
+  uint32_t* status;
+  int Hq, Hkv, G;
+  float score_log2;
+  float v_scale;
+};
+
+__device__ __forceinline__ void set_timeout(Barriers* bars, uint32_t* status) {
+  bars->abort = 1;
+  atomicOr(status, (unsigned)MSA_STATUS_TIMEOUT);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+attention_kernel(const __grid_constant__ CUtensorMap kv_map, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + kOffBar);
+  const volatile int* abort = &bars->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int num_work = p.counters[1];
+  const int begin = (int)((int64_t)blockIdx.x * num_work / gridDim.x);
+  const int end = (int)((int64_t)(blockIdx.x + 1) * num_work / gridDim.x);
+  const int cnt = end - begin;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->q_full[s], kQLoaderThreads);
+      mbar_init(&bars->stage_empty[s], 1);
+    }
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(&bars->s_full[w], 1);
+      mbar_init(&bars->p_full[w], kSoftmaxThreads);
+      mbar_init(&bars->o_full[w], 1);
+      mbar_init(&bars->o_free[w], kSoftmaxThreads);
+    }
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int li = 0; li < cnt; ++li) {
+        const int s = li % kStages, round = li / kStages;
+        if (round > 0 && !bounded_wait(&bars->stage_empty[s], (round - 1) & 1,
+                                       abort, kWaitLimitNs)) {
+          if (!*abort) set_timeout(bars, p.status);
+          break;
+        }
+        const int4 it = p.work[begin + li];
+        const int h = it.w >> 24, lp = it.w & 0xFFFFFF;
+        const int32_t phys = p.block_table[(int64_t)it.z * p.bt_stride + lp];
+        const int32_t row = (phys * p.Hkv + h) * kPage;
+        mbar_arrive_expect_tx(&bars->kv_full[s], 2 * kTile);
+        tma_load_2d(smem + kOffK + s * kTile, &kv_map, &bars->kv_full[s], 0, row);
+        tma_load_2d(smem + kOffV + s * kTile, &kv_map, &bars->kv_full[s], kD, row);
+        issued = li + 1;
+      }
+      // every copy this thread started must land before the CTA exits
+      for (int li = issued > kStages ? issued - kStages : 0; li < issued; ++li)
+        bounded_wait(&bars->kv_full[li % kStages], (li / kStages) & 1, nullptr,
+                     kWaitLimitNs);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_e4m3_f32(128, 128, false);
+      constexpr uint32_t idesc_pv = idesc_e4m3_f32(128, 128, true);
+      bool ok = true;
+      auto issue_qk = [&](int li) -> bool {
+        const int s = li % kStages, round = li / kStages, w = li & 1;
+        if (!bounded_wait(&bars->kv_full[s], round & 1, abort, kWaitLimitNs))
+          return false;
+        if (!bounded_wait(&bars->q_full[s], round & 1, abort, kWaitLimitNs))
+          return false;
+        tc_fence_after();
+        const uint64_t a = smem_desc_sw128(smem_u32(smem + kOffQ + s * kTile), 16, 1024);
+        const uint64_t b = smem_desc_sw128(smem_u32(smem + kOffK + s * kTile), 16, 1024);
+        const uint32_t d = tmem + (uint32_t)(w * 256);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // K = 128 bytes = 4 x 32
+          mma_f8f6f4(d, a + (uint64_t)(kk * 2), b + (uint64_t)(kk * 2), idesc_qk,
+                     kk > 0);
+        mma_commit(&bars->s_full[w]);
+        return true;
+      };
+      auto issue_pv = [&](int li) -> bool {
+        const int s = li % kStages, w = li & 1, k = li >> 1;
+        if (!bounded_wait(&bars->p_full[w], k & 1, abort, kWaitLimitNs))
+          return false;
+        if (k > 0 &&
+            !bounded_wait(&bars->o_free[w], (k - 1) & 1, abort, kWaitLimitNs))
+          return false;
+        tc_fence_after();
+        const uint64_t a = smem_desc_sw128(smem_u32(smem + kOffP + w * kTile), 16, 1024);
+        const uint64_t b = smem_desc_sw128(smem_u32(smem + kOffV + s * kTile), 1024, 1024);
+        const uint32_t d = tmem + (uint32_t)(w * 256 + 128);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // 128 keys = 4 x 32; V rows advance 4 KB
+          mma_f8f6f4(d, a + (uint64_t)(kk * 2), b + (uint64_t)(kk * 256),
+                     idesc_pv, kk > 0);
+        mma_commit(&bars->o_full[w]);
+        mma_commit(&bars->stage_empty[s]);
+        return true;
+      };
+      if (cnt > 0) ok = issue_qk(0);
+      for (int li = 0; ok && li < cnt; ++li) {
+        if (li + 1 < cnt && !issue_qk(li + 1)) { ok = false; break; }
+        if (!issue_pv(li)) { ok = false; break; }
+      }
+      if (!ok && !*abort) set_timeout(bars, p.status);
+      mma_commit(&bars->mma_done);
+      bounded_wait(&bars->mma_done, 0, nullptr, kWaitLimitNs);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ Q gather
+    const int qt = threadIdx.x - 64;
+    bool ok = true;
+    for (int li = 0; li < cnt; ++li) {
+      const int s = li % kStages, round = li / kStages;
+      if (round > 0 && !bounded_wait(&bars->stage_empty[s], (round - 1) & 1,
+                                     abort, kWaitLimitNs)) {
+        ok = false;
+        break;
+      }
+      const int4 it = p.work[begin + li];
+      const int h = it.w >> 24;
+      const int rows = it.y * p.G;
+      const uint32_t dst0 = smem_u32(smem + kOffQ + s * kTile);
+      for (int e = qt; e < rows * 8; e += kQLoaderThreads) {
+        const int row = e >> 3, ch = e & 7;
+        const int i = row / p.G, g = row - i * p.G;
+        const int t = p.q_idx[it.x + i];
+        const uint8_t* src =
+            p.q + ((int64_t)t * p.Hq + (int64_t)h * p.G + g) * kD + ch * 16;
+        cp_async_16(dst0 + row * 128 + ((ch ^ (row & 7)) << 4), src);
+      }
+      cp_async_commit();
+      if (li > 0) {
+        cp_async_wait<1>();
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->q_full[(li - 1) % kStages]);
+      }
+    }
+    cp_async_wait<0>();
+    if (ok && cnt > 0) {
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->q_full[(cnt - 1) % kStages]);
+    }
+    if (!ok && lane == 0 && !*abort) set_timeout(bars, p.status);
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int w = (warp - 4) >> 2;       // group
+    const int quad = warp & 3;           // TMEM lane quadrant
+    const int row = quad * 32 + lane;    // tile row = token i * G + head g
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t s_tmem = tmem + lane_off + (uint32_t)(w * 256);
+    const uint32_t o_tmem = s_tmem + 128;
+    uint8_t* sP = smem + kOffP + w * kTile;
+    for (int k = 0;; ++k) {
+      const int li = 2 * k + w;
+      if (li >= cnt) break;
+      const int4 it = p.work[begin + li];
+      const int h = it.w >> 24, lp = it.w & 0xFFFFFF, b = it.z;
+      const int i = row / p.G, g = row - i * p.G;
+      const bool valid = i < it.y;
+      const bool warp_valid = quad * 32 < it.y * p.G;
+      int t = 0, j = 0, kv_lim = 127;
+      if (valid) {
+        t = p.q_idx[it.x + i];
+        j = p.slot[it.x + i];
+        const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
+        const int k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
+        const int pos = (t - q0) + (k1 - k0) - (q1 - q0);
+        kv_lim = min(pos - lp * kPage, 127);
+      }
+      if (!bounded_wait(&bars->s_full[w], k & 1, abort, kWaitLimitNs)) {
+        if (lane == 0 && !*abort) set_timeout(bars, p.status);
+        break;
+      }
+      tc_fence_after();
+      float m2 = -INFINITY, l = 0.f;
+      if (warp_valid) {
+        __syncwarp();
+        uint32_t r[32];
+        float m = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(s_tmem + c * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e <= kv_lim) m = fmaxf(m, __uint_as_float(r[e]));
+        }
+        m2 = m * p.score_log2;
+        // p = 2^(x * c - m2 + 8): probabilities scaled by 256 so that small
+        // ones stay out of E4M3's subnormal range; l and O carry the same
+        // factor, which cancels.
+        const float off = (m2 == -INFINITY) ? 0.f : 8.f - m2;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(s_tmem + c * 32, r);
+          tmem_wait_ld();
+          uint32_t packed[8];
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            float pv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float x = __uint_as_float(r[e + u]);
+              pv[u] = (c * 32 + e + u <= kv_lim)
+                          ? ex2_approx(fmaf(x, p.score_log2, off))
+                          : 0.f;
+              l += pv[u];
+            }
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+                make_float2(pv[0], pv[1]), __NV_SATFINITE, __NV_E4M3);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+                make_float2(pv[2], pv[3]), __NV_SATFINITE, __NV_E4M3);
+            packed[e / 4] = lo | (hi << 16);
+          }
+          uint8_t* prow = sP + row * 128;
+          const int c0 = 2 * c, c1 = 2 * c + 1;
+          *reinterpret_cast<uint4*>(prow + ((c0 ^ (row & 7)) << 4)) =
+              make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          *reinterpret_cast<uint4*>(prow + ((c1 ^ (row & 7)) << 4)) =
+              make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[w]);
+      if (!bounded_wait(&bars->o_full[w], k & 1, abort, kWaitLimitNs)) {
+        if (lane == 0 && !*abort) set_timeout(bars, p.status);
+        break;
+      }
+      tc_fence_after();
+      if (warp_valid) {
+        const float inv = l > 0.f ? p.v_scale / l : 0.f;
+        const int hq = h * p.G + g;
+        uint16_t* dst =
+            p.part_o + (((int64_t)t * p.Hq + hq) * kTopK + j) * (int64_t)kD;
+        uint32_t r[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          __syncwarp();
+          tmem_ld32(o_tmem + c * 32, r);
+          tmem_wait_ld();
+          if (valid) {
+            uint32_t o[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              __nv_bfloat162 v2 = __floats2bfloat162_rn(
+                  __uint_as_float(r[2 * e]) * inv,
+                  __uint_as_float(r[2 * e + 1]) * inv);
+              o[e] = *reinterpret_cast<uint32_t*>(&v2);
+            }
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+            d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            d4[2] = make_uint4(o[8], o[9], o[10], o[11]);
+            d4[3] = make_uint4(o[12], o[13], o[14], o[15]);
+          }
+        }
+        if (valid)
+          p.part_lse[((int64_t)t * p.Hq + hq) * kTopK + j] =
+              l > 0.f ? (m2 + __log2f(l) - 8.f) * 0.69314718055994530942f
+                      : -INFINITY;
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->o_free[w]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
+                                   void*, const cuuint64_t*, const cuuint64_t*,
+                                   const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+}  // namespace
+
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
+  const msa_plan_t& pl = *a.plan;
+  if (pl.max_work == 0) return cudaSuccess;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  // The page pool as a 2-D byte tensor: rows = (page, KV head, token),
+  // 256 bytes per row (K then V); boxes of 128 rows x 128 bytes with the
+  // 128-byte swizzle that the MMA descriptors expect.
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {2 * (cuuint64_t)kD,
+                              (cuuint64_t)a.num_pages * pl.Hkv * kPage};
+  const cuuint64_t strides[1] = {2 * (cuuint64_t)kD};
+  const cuuint32_t box[2] = {128, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                   const_cast<uint8_t*>(a.kv), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+
+  Params p;
+  p.q = a.q;
+  p.block_table = a.block_table;
+  p.bt_stride = a.bt_stride;
+  p.cu_q = pl.cu_seqlens_q;
+  p.cu_k = pl.cu_seqlens_k;
+  p.q_idx = pl.q_idx;
+  p.slot = pl.slot;
+  p.work = reinterpret_cast<const int4*>(pl.work);
+  p.counters = pl.counters;
+  p.part_o = a.part_o;
+  p.part_lse = a.part_lse;
+  p.status = pl.status;
+  p.Hq = (int)pl.Hq;
+  p.Hkv = (int)pl.Hkv;
+  p.G = (int)(pl.Hq / pl.Hkv);
+  p.score_log2 = a.score_log2;
+  p.v_scale = a.v_scale;
+
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(
+        attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int64_t grid = std::min<int64_t>(num_sms(), pl.max_work);
+  attention_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(map, p);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

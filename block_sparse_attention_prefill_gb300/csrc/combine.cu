@@ -1,0 +1,166 @@
+// Split-KV combine: merge the per-slot partials of every (token, query head)
+// by log-sum-exp and round to bf16.  (vLLM PR 60684, Performance: the
+// per-layer call is build_k2q_csr + attention + combine; Validation: the
+// E4M3 probabilities are rounded per split and the splits are merged.)
+//
+// For row r with filled slots j:  M = max lse_j,  sum = sum_j e^(lse_j - M),
+// out = sum_j (e^(lse_j - M) / sum) * O_j,  lse = M + ln(sum).
+// HBM-bound: one warp per row, each lane owns 4 of the 128 columns, so a
+// partial row is one coalesced 256 B (bf16) or 512 B (fp32) read.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+__device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
+  const float4 x = *reinterpret_cast<const float4*>(p);
+  v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
+  const uint2 x = *reinterpret_cast<const uint2*>(p);
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&x.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&x.y);
+  const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+  v[0] = fa.x; v[1] = fa.y; v[2] = fb.x; v[3] = fb.y;
+}
+
+template <typename TIn, bool kMask>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+combine_kernel(const TIn* __restrict__ part_o, const float* __restrict__ part_lse,
+               const uint16_t* __restrict__ slot_mask, int64_t group,
+               int64_t rows, int S, uint16_t* __restrict__ out,
+               float* __restrict__ lse_out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  uint32_t mask = 0xffffffffu;
+  if (kMask) mask = slot_mask[r / group];
+  // split j = lane and j = lane + 32
+  float l0 = -INFINITY, l1 = -INFINITY;
+  if (lane < S && ((mask >> lane) & 1u)) l0 = part_lse[r * S + lane];
+  if (!kMask && lane + 32 < S) l1 = part_lse[r * S + lane + 32];
+  float M = fmaxf(l0, l1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  uint2* dst = reinterpret_cast<uint2*>(out + r * kD + lane * 4);
+  if (M == -INFINITY) {
+    *dst = make_uint2(0u, 0u);
+    if (lse_out && lane == 0) lse_out[r] = -INFINITY;
+    return;
+  }
+  const float w0 = (l0 == -INFINITY) ? 0.f : __expf(l0 - M);
+  const float w1 = (l1 == -INFINITY) ? 0.f : __expf(l1 - M);
+  float sum = w0 + w1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float inv = 1.f / sum;
+  const uint32_t live0 = __ballot_sync(0xffffffffu, w0 > 0.f);
+  const uint32_t live1 = __ballot_sync(0xffffffffu, w1 > 0.f);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const TIn* base = part_o + r * (int64_t)S * kD + lane * 4;
+  for (uint32_t bits = live0; bits; bits &= bits - 1) {
+    const int j = __ffs(bits) - 1;
+    const float wj = __shfl_sync(0xffffffffu, w0, j) * inv;
+    float v[4];
+    load4(base + (int64_t)j * kD, v);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc[u] = fmaf(wj, v[u], acc[u]);
+  }
+  for (uint32_t bits = live1; bits; bits &= bits - 1) {
+    const int j = __ffs(bits) - 1;
+    const float wj = __shfl_sync(0xffffffffu, w1, j) * inv;
+    float v[4];
+    load4(base + (int64_t)(j + 32) * kD, v);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc[u] = fmaf(wj, v[u], acc[u]);
+  }
+  __nv_bfloat162 a = __floats2bfloat162_rn(acc[0], acc[1]);
+  __nv_bfloat162 b = __floats2bfloat162_rn(acc[2], acc[3]);
+  *dst = make_uint2(*reinterpret_cast<uint32_t*>(&a),
+                    *reinterpret_cast<uint32_t*>(&b));
+  if (lse_out && lane == 0) lse_out[r] = M + __logf(sum);
+}
+
+__global__ void __launch_bounds__(1024)
+decode_seqlens_kernel(const int32_t* seq_lens, int64_t B, int64_t n,
+                      int32_t* cu_q, int32_t* cu_k) {
+  __shared__ int warp_sums[33];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int carry = 0;
+  for (int64_t base = 0; base < B; base += 1024) {
+    const int64_t b = base + threadIdx.x;
+    const int v = b < B ? seq_lens[b] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int s = warp_sums[lane];
+      int si = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, si, o);
+        if (lane >= o) si += x;
+      }
+      warp_sums[lane] = si - s;
+      if (lane == 31) warp_sums[32] = si;
+    }
+    __syncthreads();
+    if (b < B) {
+      cu_k[b + 1] = carry + warp_sums[warp] + incl;
+      cu_q[b + 1] = (int32_t)((b + 1) * n);
+    }
+    carry += warp_sums[32];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    cu_q[0] = 0;
+    cu_k[0] = 0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const void* part_o, int part_dtype,
+                           const float* part_lse, const uint16_t* slot_mask,
+                           int64_t group, int64_t rows, int64_t splits,
+                           uint16_t* out, float* lse, cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)ceil_div(rows, kWarpsPerBlock);
+  const int S = (int)splits;
+  if (part_dtype == MSA_DTYPE_BF16) {
+    auto po = static_cast<const __nv_bfloat16*>(part_o);
+    if (slot_mask)
+      combine_kernel<__nv_bfloat16, true><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
+          po, part_lse, slot_mask, group, rows, S, out, lse);
+    else
+      combine_kernel<__nv_bfloat16, false><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
+          po, part_lse, nullptr, 1, rows, S, out, lse);
+  } else {
+    auto po = static_cast<const float*>(part_o);
+    if (slot_mask)
+      combine_kernel<float, true><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
+          po, part_lse, slot_mask, group, rows, S, out, lse);
+    else
+      combine_kernel<float, false><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
+          po, part_lse, nullptr, 1, rows, S, out, lse);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_seqlens(const int32_t* seq_lens, int64_t B,
+                                  int64_t n, int32_t* cu_q, int32_t* cu_k,
+                                  cudaStream_t stream) {
+  decode_seqlens_kernel<<<1, 1024, 0, stream>>>(seq_lens, B, n, cu_q, cu_k);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

@@ -1,0 +1,61 @@
+// Shared declarations of the libmsa translation units (plan, attention,
+// combine, C ABI).  Shape constants follow the MSA pages: head dim 128,
+// 128-token pages, top-16 pages per (token, KV head).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/msa.h"
+
+namespace msa {
+
+constexpr int kD = MSA_HEAD_DIM;      // head dim
+constexpr int kPage = MSA_PAGE_SIZE;  // tokens per KV page
+constexpr int kTopK = MSA_TOPK;       // pages per (token, KV head)
+constexpr int kTileM = 128;           // MMA rows per work item (tokens x G)
+
+// Rows per CTA in the plan's count / fill kernels.
+constexpr int kPlanTile = 256;
+
+// Wall-time bound of every device-side wait (about a second).
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+__host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) {
+  return (a + b - 1) / b;
+}
+
+// Launchers (each returns a cudaError_t from the launch).
+cudaError_t launch_plan(const msa_plan_t& plan, const int32_t* topk,
+                        const int32_t* block_table, cudaStream_t stream);
+
+struct AttnArgs {
+  const uint8_t* q;
+  const uint8_t* kv;
+  int64_t num_pages;
+  float score_log2;   // q_scale * k_scale * softmax_scale * log2(e)
+  float v_scale;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const msa_plan_t* plan;
+  uint16_t* part_o;   // [T][Hq][16][128] bf16, normalised partial outputs
+  float* part_lse;    // [T][Hq][16]
+};
+
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
+
+// Combine over `splits` partials per row.  With slot_mask != nullptr, the
+// mask of row r is slot_mask[r / group] and empty slots are not read.
+cudaError_t launch_combine(const void* part_o, int part_dtype,
+                           const float* part_lse, const uint16_t* slot_mask,
+                           int64_t group, int64_t rows, int64_t splits,
+                           uint16_t* out, float* lse, cudaStream_t stream);
+
+cudaError_t launch_decode_seqlens(const int32_t* seq_lens, int64_t B,
+                                  int64_t n, int32_t* cu_q, int32_t* cu_k,
+                                  cudaStream_t stream);
+
+int num_sms();
+
+}  // namespace msa

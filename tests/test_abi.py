@@ -1,0 +1,98 @@
+"""The C ABI without a GPU: libmsa.so builds for sm_103a, loads, exports
+every function include/msa.h declares, sizes its workspaces, and rejects bad
+arguments on the host before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_sparse_attention_prefill_gb300 as msa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "msa.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MSA_API\s+[\w\s\*]*?\b(msa_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return msa.load()
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for n in ("msa_plan", "msa_prefill", "msa_decode", "msa_combine",
+              "msa_plan_workspace_bytes", "msa_prefill_workspace_bytes",
+              "msa_decode_workspace_bytes", "msa_read_status",
+              "msa_status_string", "msa_version", "msa_read_counters"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(msa.library_path())
+    for n in declared_functions():
+        assert hasattr(raw, n), n
+
+
+def test_version_and_strings(lib):
+    assert lib.msa_version() >= 100
+    assert msa.status_string(0) == "ok"
+    assert "workspace" in msa.status_string(4)
+
+
+def test_workspace_sizes(lib):
+    a = msa.plan_workspace_bytes(1, 2048, 16, 2, 8192, 2048)
+    b = msa.plan_workspace_bytes(1, 4096, 16, 2, 8192, 4096)
+    assert 0 < a < b
+    assert msa.prefill_workspace_bytes(2048, 16) >= 2048 * 16 * 16 * (256 + 4)
+    assert msa.decode_workspace_bytes(64, 8, 16, 2, 131072) > 0
+
+
+def _err(fn, *args):
+    with pytest.raises(msa.MsaError) as e:
+        fn(*args)
+    return str(e.value)
+
+
+def test_sizing_rejects_bad_shapes(lib):
+    assert "unsupported" in _err(msa.plan_workspace_bytes, 1, 10, 6, 4, 8, 10)
+    assert "unsupported" in _err(msa.plan_workspace_bytes, 1, 10, 256, 1, 8, 10)
+    assert "out of range" in _err(msa.plan_workspace_bytes, -1, 10, 8, 1, 8, 10)
+    assert "out of range" in _err(msa.decode_workspace_bytes, 4, 9, 16, 2, 1000)
+    assert "out of range" in _err(msa.decode_workspace_bytes, 4, 8, 16, 2, 4)
+
+
+def test_host_validation_before_launch(lib):
+    P = ctypes.c_void_p
+    plan = msa.MsaPlanStruct()
+    fake = P(4096)  # never dereferenced: every call below fails on the host
+    # NULL plan
+    assert lib.msa_plan(fake, fake, fake, fake, 4, 8, 1, 10, 16, 2, 8, 10,
+                        100, fake, 1 << 20, None, None) == 6
+    # group size not an integer
+    assert lib.msa_plan(fake, fake, fake, fake, 4, 8, 1, 10, 6, 4, 8, 10, 100,
+                        fake, 1 << 20, ctypes.byref(plan), None) == 2
+    # workspace too small
+    assert lib.msa_plan(fake, fake, fake, fake, 4, 8, 1, 10, 16, 2, 8, 10, 100,
+                        fake, 16, ctypes.byref(plan), None) == 4
+    # max_seqlen_q above max_seqlen_k
+    assert lib.msa_plan(fake, fake, fake, fake, 4, 8, 1, 10, 16, 2, 8, 200,
+                        100, fake, 1 << 30, ctypes.byref(plan), None) == 1
+    # misaligned workspace
+    assert lib.msa_plan(fake, fake, fake, fake, 4, 8, 1, 10, 16, 2, 8, 10, 100,
+                        P(4096 + 8), 1 << 30, ctypes.byref(plan), None) == 3
+    # combine: bad split count, bad dtype
+    assert lib.msa_combine(fake, 0, fake, 10, 0, fake, None, None) == 1
+    assert lib.msa_combine(fake, 7, fake, 10, 4, fake, None, None) == 2
+    assert lib.msa_combine(P(4100), 0, fake, 10, 4, fake, None, None) == 3
+    # prefill: NULL plan
+    assert lib.msa_prefill(fake, fake, 4, 1.0, 1.0, 1.0, 0.1, fake, 4, None,
+                           fake, 1 << 20, fake, None, None) == 6
+    # decode: n out of range
+    assert lib.msa_decode(fake, fake, 4, 1.0, 1.0, 1.0, 0.1, fake, fake, 4,
+                          fake, 2, 9, 16, 2, 1000, fake, 1 << 30, fake, None,
+                          None, None) == 1

@@ -1,0 +1,114 @@
+"""build_k2q_csr + schedule on the GPU, bit-exact against the oracle's CSR
+(plain loops) and its work-list rule (vLLM docs, sparse_attention_msa,
+MiniMaxM3SparseMSAImpl.forward: build_k2q_csr over [H, T, 16] page lists,
+total_rows = total_kv_blocks)."""
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_attention_prefill_gb300 as msa
+import oracle
+import pins
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_plan(w, total_rows=None):
+    wd = w.to("cuda")
+    R = w.total_rows if total_rows is None else total_rows
+    plan = msa.msa_plan(wd.topk, wd.cu_q, wd.cu_k, wd.block_table,
+                        w.num_pages, w.Hq, R, max(w.max_seqlen_q, 1),
+                        max(w.max_seqlen_k, 1))
+    torch.cuda.synchronize()
+    nnz, nwork = plan.counters()
+    return plan, nnz, nwork
+
+
+def compare_plan(w, total_rows=None):
+    plan, nnz, nwork = gpu_plan(w, total_rows)
+    R = w.total_rows if total_rows is None else total_rows
+    row_ptr, q_idx, slot, mask = oracle.k2q_csr(w, total_rows=R)
+    assert nnz == len(q_idx)
+    assert np.array_equal(plan.row_ptr().cpu().numpy(), row_ptr)
+    assert np.array_equal(plan.q_idx()[:nnz].cpu().numpy(), q_idx)
+    assert np.array_equal(plan.slot()[:nnz].cpu().numpy(), slot)
+    got_mask = plan.slot_mask().cpu().numpy().view(np.uint16).reshape(
+        mask.shape)
+    assert np.array_equal(got_mask, mask)
+    items = oracle.schedule(row_ptr, w, total_rows=R)
+    assert nwork == len(items)
+    work = plan.work()[:nwork].cpu().numpy()
+    got = [(int(a), int(b), int(c), int(d) >> 24, int(d) & 0xFFFFFF)
+           for a, b, c, d in work]
+    assert got == items
+    return plan
+
+
+@pytest.mark.parametrize("name", ["tiny_full_prefill", "chunked_prefill_32k",
+                                  "ragged_batch_8"])
+def test_plan_matches_oracle(name):
+    w = workloads.make_config(name, seed=0)
+    plan = compare_plan(w)
+    assert plan.status() == 0
+
+
+@pytest.mark.parametrize("seed", [3, 4])
+def test_plan_invalid_entries(seed):
+    w = pins.tiny_sparse_workload(seed)
+    plan = compare_plan(w)
+    st = plan.status()
+    assert st & msa.STATUS_BAD_PAGE_ID
+    assert st & msa.STATUS_BAD_BLOCK
+
+
+def test_plan_group_sizes():
+    for hq, hkv in ((16, 1), (12, 4), (8, 8), (128, 1)):
+        w = workloads.make_batch("g", [300, 40], [2000, 900], hq, hkv, seed=hq)
+        compare_plan(w)
+
+
+def test_plan_long_rows():
+    # a prefill from empty cache: page 0 is selected by thousands of tokens
+    w = workloads.make_batch("ctx0", [8192], [8192], 16, 1, seed=1)
+    compare_plan(w)
+
+
+def test_plan_decode_shape_and_spare_rows():
+    sl = workloads.decode_lengths(0, 16, 4096, 20000)
+    w = workloads.make_batch("dec", [8] * 16, sl, 16, 2, seed=2)
+    compare_plan(w, total_rows=w.total_rows + 37)
+
+
+def test_plan_all_padding_and_empty_requests():
+    w = workloads.make_batch("pad", [64, 0, 32], [5000, 300, 32], 8, 2, seed=5)
+    w = pins._replace(w, topk=torch.full_like(w.topk, -1))
+    plan, nnz, nwork = gpu_plan(w)
+    assert nnz == 0 and nwork == 0 and plan.status() == 0
+    w2 = workloads.make_batch("pad2", [64, 0, 32], [5000, 300, 32], 8, 2, seed=5)
+    compare_plan(w2)
+
+
+def test_plan_bad_seqlens_gives_empty_plan():
+    w = workloads.make_batch("bad", [64], [5000], 8, 2, seed=6)
+    cu_k = w.cu_k.clone()
+    cu_k[1] = 30                       # seq_len < q_len
+    w = pins._replace(w, cu_k=cu_k)
+    plan, nnz, nwork = gpu_plan(w, total_rows=64)
+    assert nnz == 0 and nwork == 0
+    assert plan.status() & msa.STATUS_BAD_SEQLENS
+
+
+def test_plan_rows_overflow():
+    w = workloads.make_batch("ovf", [16], [5000], 8, 2, seed=7)
+    plan, nnz, nwork = gpu_plan(w, total_rows=10)
+    assert nnz == 0 and plan.status() & msa.STATUS_ROWS_OVERFLOW
+
+
+def test_plan_is_deterministic():
+    w = workloads.make_config("chunked_prefill_32k", seed=1)
+    p1, n1, _ = gpu_plan(w)
+    a = p1.q_idx()[:n1].clone()
+    for _ in range(3):
+        p2, n2, _ = gpu_plan(w)
+        assert n2 == n1 and torch.equal(p2.q_idx()[:n2], a)
