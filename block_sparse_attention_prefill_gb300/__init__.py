@@ -37,10 +37,10 @@ STATUS_BAD_WORK = 1 << 5
 
 _I64 = ("B", "T", "Hq", "Hkv", "total_rows", "max_seqlen_q", "max_seqlen_k",
         "num_pages", "bt_stride", "bitmap_words", "chunk_tokens", "max_nnz",
-        "max_work", "rows")
-_PTR = ("cu_seqlens_q", "cu_seqlens_k", "req_off", "bitmap", "row_cnt",
-        "tile_sums", "row_ptr", "q_idx", "slot", "work", "counters",
-        "slot_mask", "status")
+        "max_work", "rows", "record_bytes")
+_PTR = ("cu_seqlens_q", "cu_seqlens_k", "req_off", "bitmap", "word_pre",
+        "row_cnt", "row_wptr", "tile_sums", "row_ptr", "q_idx", "slot", "work",
+        "records", "counters", "slot_mask", "status")
 
 
 class MsaPlanStruct(ctypes.Structure):
@@ -197,6 +197,11 @@ class Plan:
     def work(self):
         return self._view("work", 4 * self.struct.max_work,
                           torch.int32).view(-1, 4)
+
+    def records(self):
+        n = self.struct.record_bytes // 16
+        return self._view("records", self.struct.max_work * n * 4,
+                          torch.int32).view(-1, n, 4)
 
     def slot_mask(self):
         return self._view("slot_mask", self.struct.T * self.struct.Hkv,

@@ -14,15 +14,19 @@
 // library's own.
 //
 // One CTA per SM, persistent over a contiguous range of the work list.
-// Warp roles (12 warps):
-//   warp 0      TMA producer: K and V halves of the item's page (2 x 16 KB)
+// Every work item has a record written by the plan: {KV row of the page in
+// the pool, token count n, first key position, first query head} and, per
+// token, {token id, query position, top-k slot}.  Warp roles (12 warps):
+//   warp 0      producer: bulk copy of the item's record, TMA loads of the
+//               K and V halves of the page (2 x 16 KB, 128-byte swizzle)
 //   warp 1      tcgen05 issuer (one thread) and TMEM owner (512 columns)
-//   warps 2-3   Q gather: C tokens x G heads rows of 128 B with cp.async,
-//               written in the 128-byte-swizzled K-major layout
+//   warps 2-3   Q gather: n tokens x G heads rows of 128 B into the
+//               128-byte-swizzled K-major tile -- one TMA box per token
+//               when G is a multiple of 8, cp.async otherwise
 //   warps 4-7   softmax / epilogue group 0 (even items)
 //   warps 8-11  softmax / epilogue group 1 (odd items)
-// Shared memory: 3 stages of {K, V, Q} 16 KB tiles + 2 P tiles = 176 KB.
-// TMEM: per group an S tile (128 cols) and an O tile (128 cols).
+// Shared memory: 3 stages of {K, V, Q} 16 KB tiles and a record, 2 P tiles.
+// TMEM: per group an S tile (128 columns) and an O tile (128 columns).
 // MMA order: QK(0), QK(1), PV(0), QK(2), PV(1), ... so that the tensor
 // cores compute item n+1's scores while item n's softmax runs.
 #include <cuda.h>
@@ -38,18 +42,20 @@ namespace {
 constexpr int kStages = 3;
 constexpr int kTile = 128 * 128;  // one 128 x 128 E4M3 tile, bytes
 constexpr int kThreads = 384;
-constexpr int kQLoaderThreads = 64;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kTmemCols = 512;
+constexpr int kRecMax = 16 * (1 + kTileM);  // header + up to 128 tokens
 
 // offsets from the 1024-byte aligned base
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kStages * kTile;
 constexpr int kOffQ = kOffV + kStages * kTile;
 constexpr int kOffP = kOffQ + kStages * kTile;
-constexpr int kOffBar = kOffP + 2 * kTile;
+constexpr int kOffRec = kOffP + 2 * kTile;
+constexpr int kOffBar = kOffRec + kStages * kRecMax;
 
 struct Barriers {
+  uint64_t rec_full[kStages];
   uint64_t kv_full[kStages];
   uint64_t q_full[kStages];
   uint64_t stage_empty[kStages];
@@ -66,18 +72,14 @@ constexpr int kSmemBytes = kOffBar + (int)sizeof(Barriers) + 1024;
 
 struct Params {
   const uint8_t* q;
-  const int32_t* block_table;
-  int64_t bt_stride;
-  const int32_t* cu_q;
-  const int32_t* cu_k;
-  const int32_t* q_idx;
-  const uint8_t* slot;
-  const int4* work;
+  const int4* records;
+  int rec_stride;  // int4 per record
   const int32_t* counters;
   uint16_t* part_o;
   float* part_lse;
   uint32_t* status;
-  int Hq, Hkv, G;
+  int Hq, G;
+  int q_tma;       // 1: Q rows by TMA (G % 8 == 0), 0: by cp.async
   float score_log2;
   float v_scale;
 };
@@ -88,7 +90,8 @@ __device__ __forceinline__ void set_timeout(Barriers* bars, uint32_t* status) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-attention_kernel(const __grid_constant__ CUtensorMap kv_map, const Params p) {
+attention_kernel(const __grid_constant__ CUtensorMap kv_map,
+                 const __grid_constant__ CUtensorMap q_map, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -105,8 +108,9 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map, const Params p) {
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->rec_full[s], 1);
       mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->q_full[s], kQLoaderThreads);
+      mbar_init(&bars->q_full[s], p.q_tma ? 1 : 32);
       mbar_init(&bars->stage_empty[s], 1);
     }
     for (int w = 0; w < 2; ++w) {
@@ -133,26 +137,34 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map, const Params p) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int issued = 0;
+      int4 next = cnt > 0 ? p.records[(int64_t)begin * p.rec_stride]
+                          : make_int4(0, 0, 0, 0);
       for (int li = 0; li < cnt; ++li) {
         const int s = li % kStages, round = li / kStages;
+        const int4 hdr = next;
+        if (li + 1 < cnt) next = p.records[(int64_t)(begin + li + 1) * p.rec_stride];
         if (round > 0 && !bounded_wait(&bars->stage_empty[s], (round - 1) & 1,
                                        abort, kWaitLimitNs)) {
           if (!*abort) set_timeout(bars, p.status);
           break;
         }
-        const int4 it = p.work[begin + li];
-        const int h = it.w >> 24, lp = it.w & 0xFFFFFF;
-        const int32_t phys = p.block_table[(int64_t)it.z * p.bt_stride + lp];
-        const int32_t row = (phys * p.Hkv + h) * kPage;
+        const uint32_t rec_bytes = 16u * (1u + (uint32_t)hdr.y);
+        mbar_arrive_expect_tx(&bars->rec_full[s], rec_bytes);
+        bulk_load(smem + kOffRec + s * kRecMax,
+                  p.records + (int64_t)(begin + li) * p.rec_stride, rec_bytes,
+                  &bars->rec_full[s]);
         mbar_arrive_expect_tx(&bars->kv_full[s], 2 * kTile);
-        tma_load_2d(smem + kOffK + s * kTile, &kv_map, &bars->kv_full[s], 0, row);
-        tma_load_2d(smem + kOffV + s * kTile, &kv_map, &bars->kv_full[s], kD, row);
+        tma_load_2d(smem + kOffK + s * kTile, &kv_map, &bars->kv_full[s], 0, hdr.x);
+        tma_load_2d(smem + kOffV + s * kTile, &kv_map, &bars->kv_full[s], kD, hdr.x);
         issued = li + 1;
       }
       // every copy this thread started must land before the CTA exits
-      for (int li = issued > kStages ? issued - kStages : 0; li < issued; ++li)
+      for (int li = issued > kStages ? issued - kStages : 0; li < issued; ++li) {
+        bounded_wait(&bars->rec_full[li % kStages], (li / kStages) & 1, nullptr,
+                     kWaitLimitNs);
         bounded_wait(&bars->kv_full[li % kStages], (li / kStages) & 1, nullptr,
                      kWaitLimitNs);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -207,40 +219,57 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map, const Params p) {
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------ Q gather
-    const int qt = threadIdx.x - 64;
     bool ok = true;
-    for (int li = 0; li < cnt; ++li) {
-      const int s = li % kStages, round = li / kStages;
-      if (round > 0 && !bounded_wait(&bars->stage_empty[s], (round - 1) & 1,
-                                     abort, kWaitLimitNs)) {
-        ok = false;
-        break;
+    if (p.q_tma) {
+      // one thread, no blocking on the copies: TMA boxes of G rows
+      if (warp == 2 && lane == 0) {
+        for (int li = 0; li < cnt; ++li) {
+          const int s = li % kStages;
+          if (!bounded_wait(&bars->rec_full[s], (li / kStages) & 1, abort,
+                            kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          const int4* rec = reinterpret_cast<const int4*>(smem + kOffRec + s * kRecMax);
+          const int4 hdr = rec[0];
+          mbar_arrive_expect_tx(&bars->q_full[s], (uint32_t)(hdr.y * p.G * 128));
+          uint8_t* dst = smem + kOffQ + s * kTile;
+          for (int i = 0; i < hdr.y; ++i)
+            tma_load_2d(dst + i * p.G * 128, &q_map, &bars->q_full[s], 0,
+                        rec[1 + i].x * p.Hq + hdr.w);
+        }
+        if (!ok && !*abort) set_timeout(bars, p.status);
       }
-      const int4 it = p.work[begin + li];
-      const int h = it.w >> 24;
-      const int rows = it.y * p.G;
-      const uint32_t dst0 = smem_u32(smem + kOffQ + s * kTile);
-      for (int e = qt; e < rows * 8; e += kQLoaderThreads) {
-        const int row = e >> 3, ch = e & 7;
-        const int i = row / p.G, g = row - i * p.G;
-        const int t = p.q_idx[it.x + i];
-        const uint8_t* src =
-            p.q + ((int64_t)t * p.Hq + (int64_t)h * p.G + g) * kD + ch * 16;
-        cp_async_16(dst0 + row * 128 + ((ch ^ (row & 7)) << 4), src);
-      }
-      cp_async_commit();
-      if (li > 0) {
-        cp_async_wait<1>();
+    } else {
+      // two warps take alternate items; 16-byte cp.async into the swizzled
+      // layout, then a proxy fence so the tensor cores see the rows
+      for (int li = warp - 2; li < cnt; li += 2) {
+        const int s = li % kStages;
+        if (!bounded_wait(&bars->rec_full[s], (li / kStages) & 1, abort,
+                          kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        const int4* rec = reinterpret_cast<const int4*>(smem + kOffRec + s * kRecMax);
+        const int4 hdr = rec[0];
+        const int rows = hdr.y * p.G;
+        const uint32_t dst0 = smem_u32(smem + kOffQ + s * kTile);
+        for (int e = lane; e < rows * 8; e += 32) {
+          const int row = e >> 3, ch = e & 7;
+          const int i = row / p.G, g = row - i * p.G;
+          const int t = rec[1 + i].x;
+          const uint8_t* src =
+              p.q + ((int64_t)t * p.Hq + hdr.w + g) * kD + ch * 16;
+          cp_async_16(dst0 + row * 128 + ((ch ^ (row & 7)) << 4), src);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
         fence_proxy_async_smem();
-        mbar_arrive(&bars->q_full[(li - 1) % kStages]);
+        mbar_arrive(&bars->q_full[s]);
       }
+      cp_async_wait<0>();
+      if (!ok && lane == 0 && !*abort) set_timeout(bars, p.status);
     }
-    cp_async_wait<0>();
-    if (ok && cnt > 0) {
-      fence_proxy_async_smem();
-      mbar_arrive(&bars->q_full[(cnt - 1) % kStages]);
-    }
-    if (!ok && lane == 0 && !*abort) set_timeout(bars, p.status);
   } else {
     // ------------------------------------------------------------ softmax
     const int w = (warp - 4) >> 2;       // group
@@ -250,23 +279,28 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map, const Params p) {
     const uint32_t s_tmem = tmem + lane_off + (uint32_t)(w * 256);
     const uint32_t o_tmem = s_tmem + 128;
     uint8_t* sP = smem + kOffP + w * kTile;
+    const int i = row / p.G, g = row - i * p.G;
     for (int k = 0;; ++k) {
       const int li = 2 * k + w;
       if (li >= cnt) break;
-      const int4 it = p.work[begin + li];
-      const int h = it.w >> 24, lp = it.w & 0xFFFFFF, b = it.z;
-      const int i = row / p.G, g = row - i * p.G;
-      const bool valid = i < it.y;
-      const bool warp_valid = quad * 32 < it.y * p.G;
+      const int s = li % kStages;
+      if (!bounded_wait(&bars->rec_full[s], (li / kStages) & 1, abort,
+                        kWaitLimitNs)) {
+        if (lane == 0 && !*abort) set_timeout(bars, p.status);
+        break;
+      }
+      const int4* rec = reinterpret_cast<const int4*>(smem + kOffRec + s * kRecMax);
+      const int4 hdr = rec[0];
+      const bool valid = i < hdr.y;
+      const bool warp_valid = quad * 32 < hdr.y * p.G;
       int t = 0, j = 0, kv_lim = 127;
       if (valid) {
-        t = p.q_idx[it.x + i];
-        j = p.slot[it.x + i];
-        const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
-        const int k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
-        const int pos = (t - q0) + (k1 - k0) - (q1 - q0);
-        kv_lim = min(pos - lp * kPage, 127);
+        const int4 tok = rec[1 + i];
+        t = tok.x;
+        j = tok.z;
+        kv_lim = min(tok.y - hdr.z, 127);
       }
+      const int hq = hdr.w + g;
       if (!bounded_wait(&bars->s_full[w], k & 1, abort, kWaitLimitNs)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
@@ -330,7 +364,6 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map, const Params p) {
       tc_fence_after();
       if (warp_valid) {
         const float inv = l > 0.f ? p.v_scale / l : 0.f;
-        const int hq = h * p.G + g;
         uint16_t* dst =
             p.part_o + (((int64_t)t * p.Hq + hq) * kTopK + j) * (int64_t)kD;
         uint32_t r[32];
@@ -394,6 +427,20 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// A 2-D byte tensor of `rows` rows of `row_bytes`, read in boxes of
+// box_rows x 128 bytes with the 128-byte swizzle the MMA descriptors expect.
+bool encode_rows(EncodeTiledFn enc, CUtensorMap* map, const void* base,
+                 uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+  const cuuint64_t dims[2] = {row_bytes, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base),
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
@@ -401,38 +448,33 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   if (pl.max_work == 0) return cudaSuccess;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  // The page pool as a 2-D byte tensor: rows = (page, KV head, token),
-  // 256 bytes per row (K then V); boxes of 128 rows x 128 bytes with the
-  // 128-byte swizzle that the MMA descriptors expect.
-  CUtensorMap map;
-  const cuuint64_t dims[2] = {2 * (cuuint64_t)kD,
-                              (cuuint64_t)a.num_pages * pl.Hkv * kPage};
-  const cuuint64_t strides[1] = {2 * (cuuint64_t)kD};
-  const cuuint32_t box[2] = {128, 128};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
-                   const_cast<uint8_t*>(a.kv), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  const int G = (int)(pl.Hq / pl.Hkv);
+  // page pool: rows = (page, KV head, token), 256 bytes each (K then V)
+  CUtensorMap kv_map, q_map;
+  if (!encode_rows(enc, &kv_map, a.kv, 2 * kD,
+                   (uint64_t)a.num_pages * pl.Hkv * kPage, 128))
+    return cudaErrorInvalidValue;
+  // queries: rows = (token, query head), 128 bytes each; one box = the G
+  // heads of one KV head of one token
+  const bool q_tma = (G % 8) == 0;
+  if (q_tma) {
+    if (!encode_rows(enc, &q_map, a.q, kD, (uint64_t)pl.T * pl.Hq, (uint32_t)G))
+      return cudaErrorInvalidValue;
+  } else {
+    q_map = kv_map;  // unused
+  }
 
   Params p;
   p.q = a.q;
-  p.block_table = a.block_table;
-  p.bt_stride = a.bt_stride;
-  p.cu_q = pl.cu_seqlens_q;
-  p.cu_k = pl.cu_seqlens_k;
-  p.q_idx = pl.q_idx;
-  p.slot = pl.slot;
-  p.work = reinterpret_cast<const int4*>(pl.work);
+  p.records = reinterpret_cast<const int4*>(pl.records);
+  p.rec_stride = (int)(pl.record_bytes / 16);
   p.counters = pl.counters;
   p.part_o = a.part_o;
   p.part_lse = a.part_lse;
   p.status = pl.status;
   p.Hq = (int)pl.Hq;
-  p.Hkv = (int)pl.Hkv;
-  p.G = (int)(pl.Hq / pl.Hkv);
+  p.G = G;
+  p.q_tma = q_tma ? 1 : 0;
   p.score_log2 = a.score_log2;
   p.v_scale = a.v_scale;
 
@@ -444,7 +486,7 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
     attr_set = true;
   }
   const int64_t grid = std::min<int64_t>(num_sms(), pl.max_work);
-  attention_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(map, p);
+  attention_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(kv_map, q_map, p);
   return cudaGetLastError();
 }
 

@@ -85,6 +85,59 @@ combine_kernel(const TIn* __restrict__ part_o, const float* __restrict__ part_ls
   if (lse_out && lane == 0) lse_out[r] = M + __logf(sum);
 }
 
+// The attention path's combine: 16 slots per row, the slot mask of the
+// row's (token, KV head) says which slots hold a partial.  All of a row's
+// loads are issued before any is used.
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+combine16_kernel(const __nv_bfloat16* __restrict__ part_o,
+                 const float* __restrict__ part_lse,
+                 const uint16_t* __restrict__ slot_mask, int64_t group,
+                 int64_t rows, uint16_t* __restrict__ out,
+                 float* __restrict__ lse_out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const uint32_t mask = slot_mask[r / group];
+  const __nv_bfloat16* base = part_o + r * (int64_t)kTopK * kD + lane * 4;
+  float v[kTopK][4];
+#pragma unroll
+  for (int j = 0; j < kTopK; ++j) {
+    if ((mask >> j) & 1u) {
+      load4(base + j * kD, v[j]);
+    } else {
+      v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0.f;
+    }
+  }
+  float l = -INFINITY;
+  if (lane < kTopK && ((mask >> lane) & 1u)) l = part_lse[r * kTopK + lane];
+  float M = l;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  uint2* dst = reinterpret_cast<uint2*>(out + r * kD + lane * 4);
+  if (M == -INFINITY) {
+    *dst = make_uint2(0u, 0u);
+    if (lse_out && lane == 0) lse_out[r] = -INFINITY;
+    return;
+  }
+  const float wl = (l == -INFINITY) ? 0.f : __expf(l - M);
+  float sum = wl;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float inv = 1.f / sum;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < kTopK; ++j) {
+    const float wj = __shfl_sync(0xffffffffu, wl, j) * inv;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc[u] = fmaf(wj, v[j][u], acc[u]);
+  }
+  __nv_bfloat162 a = __floats2bfloat162_rn(acc[0], acc[1]);
+  __nv_bfloat162 b = __floats2bfloat162_rn(acc[2], acc[3]);
+  *dst = make_uint2(*reinterpret_cast<uint32_t*>(&a),
+                    *reinterpret_cast<uint32_t*>(&b));
+  if (lse_out && lane == 0) lse_out[r] = M + __logf(sum);
+}
+
 __global__ void __launch_bounds__(1024)
 decode_seqlens_kernel(const int32_t* seq_lens, int64_t B, int64_t n,
                       int32_t* cu_q, int32_t* cu_k) {
@@ -138,7 +191,10 @@ cudaError_t launch_combine(const void* part_o, int part_dtype,
   const int S = (int)splits;
   if (part_dtype == MSA_DTYPE_BF16) {
     auto po = static_cast<const __nv_bfloat16*>(part_o);
-    if (slot_mask)
+    if (slot_mask && S == kTopK)
+      combine16_kernel<<<grid, kWarpsPerBlock * 32, 0, stream>>>(
+          po, part_lse, slot_mask, group, rows, out, lse);
+    else if (slot_mask)
       combine_kernel<__nv_bfloat16, true><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
           po, part_lse, slot_mask, group, rows, S, out, lse);
     else

@@ -76,24 +76,34 @@ int plan_shape(int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t R,
   return MSA_OK;
 }
 
+// One work record: an int4 header plus one int4 per token of the chunk.
+int64_t record_bytes(const PlanShape& s) { return 16 * (1 + s.C); }
+
 // Lays out the plan workspace; with base == nullptr only the size counts.
 size_t plan_layout(const PlanShape& s, void* base, msa_plan_t* pl) {
   Carver c(base);
   int32_t* req_off = c.take<int32_t>(s.B + 1);
   uint32_t* bitmap = c.take<uint32_t>(s.rows * s.W);
+  int32_t* word_pre = c.take<int32_t>(s.rows * s.W);
   int32_t* row_cnt = c.take<int32_t>(s.rows);
+  int32_t* row_wptr = c.take<int32_t>(s.rows);
   int32_t* tile_sums = c.take<int32_t>(2 * s.ntiles + 2);
   int32_t* row_ptr = c.take<int32_t>(s.rows + 1);
   int32_t* q_idx = c.take<int32_t>(s.max_nnz);
   uint8_t* slot = c.take<uint8_t>(s.max_nnz);
   int32_t* work = c.take<int32_t>(4 * s.max_work);
+  char* records = c.take<char>(s.max_work * record_bytes(s));
   int32_t* counters = c.take<int32_t>(4);
   uint16_t* slot_mask = c.take<uint16_t>(s.T * s.Hkv);
   uint32_t* status = c.take<uint32_t>(1);
   if (pl) {
     pl->req_off = req_off;
     pl->bitmap = bitmap;
+    pl->word_pre = word_pre;
     pl->row_cnt = row_cnt;
+    pl->row_wptr = row_wptr;
+    pl->records = records;
+    pl->record_bytes = record_bytes(s);
     pl->tile_sums = tile_sums;
     pl->row_ptr = row_ptr;
     pl->q_idx = q_idx;

@@ -6,18 +6,22 @@
 // Details / "Host sync": the plan stays on the device, no host copy.)
 //
 // Steps, all on `stream`, no host synchronisation:
-//   memset  status word and the membership bitmap
-//   prep    per-request row offsets (sum of page counts), input checks
-//   mark    one thread per (token, KV head): validate its 16 ids, set one bit
-//           per kept page in the (row, token) membership bitmap, write the
-//           token's slot mask -- the histogram, kept as bits so that repeats
-//           collapse and the order of arrival cannot matter
-//   count   popcount of every row (row length) and of every tile of rows
-//   scan    exclusive scan of the tile sums (one CTA)
-//   fill    per tile: exclusive scan of its rows -> row_ptr; then one warp per
-//           row walks the row's bitmap words in order and scatters the token
-//           ids (ascending by construction) with their slot j, and writes the
-//           row's work items.
+//   memset   status word and the (row, token) membership bitmap
+//   prep     one CTA: per-request row offsets (sum of page counts), checks
+//   mark     one thread per (token, KV head): validate its 16 ids, set one
+//            bit per kept page in the membership bitmap, write the token's
+//            slot mask.  This is the histogram, kept as bits: repeats
+//            collapse and the order of arrival cannot change the result.
+//   rows     one thread per row: row length (popcount of its words), the
+//            running count in front of every word, and per-tile sums of the
+//            lengths and of the chunk counts
+//   scan     one CTA: exclusive scan of the tile sums
+//   emit     one thread per row: row_ptr, the row's first work item, and the
+//            work items / record headers of its chunks
+//   scatter  one thread per (token, KV head): each kept entry goes to
+//            row_ptr + (tokens of the same row before it), found in O(1)
+//            from the word prefix and a popcount; it also fills the token
+//            slot of the work record the attention kernel will read.
 // Every output is a function of the inputs alone: bit-exact and
 // deterministic run to run.
 #include "common.cuh"
@@ -75,30 +79,32 @@ struct PlanDev {
   const int32_t* cu_k;
   const int32_t* block_table;
   int64_t bt_stride, num_pages;
-  int B, T, Hkv, W, C;
+  int B, T, Hkv, G, W, C;
   int64_t total_rows, rows, max_q, max_k;
   int32_t* req_off;
   uint32_t* bitmap;
+  int32_t* word_pre;
   int32_t* row_cnt;
+  int32_t* row_wptr;
   int32_t* tile_sums;
   int ntiles;
   int32_t* row_ptr;
   int32_t* q_idx;
   uint8_t* slot;
   int32_t* work;
+  int4* records;
+  int rec_stride;  // int4 units per record: 1 header + C tokens
   int32_t* counters;
   uint16_t* slot_mask;
   uint32_t* status;
 };
 
 // counters[2] == 1 when the per-request metadata passed the checks.
-__global__ void __launch_bounds__(kScanThreads)
-plan_prep_kernel(PlanDev d) {
+__global__ void __launch_bounds__(kScanThreads) plan_prep_kernel(PlanDev d) {
   __shared__ int s_bad;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
-  bool overflow = false;
-  bool bad = false;
+  bool bad = false, overflow = false;
   if (threadIdx.x == 0) {
     if (d.B > 0 && (d.cu_q[0] != 0 || d.cu_q[d.B] != d.T)) bad = true;
     if (d.B == 0 && d.T != 0) bad = true;
@@ -133,6 +139,24 @@ plan_prep_kernel(PlanDev d) {
   }
 }
 
+struct TokenInfo {
+  int b, i, pos, own, P;
+  int64_t row0;
+};
+
+__device__ __forceinline__ TokenInfo token_info(const PlanDev& d, int t, int h) {
+  TokenInfo k;
+  k.b = upper_index(d.cu_q, d.B, t);
+  k.i = t - d.cu_q[k.b];
+  const int64_t ql = d.cu_q[k.b + 1] - d.cu_q[k.b];
+  const int64_t sl = d.cu_k[k.b + 1] - d.cu_k[k.b];
+  k.pos = (int)(sl - ql + k.i);
+  k.own = k.pos / kPage;
+  k.P = (int)ceil_div(sl, kPage);
+  k.row0 = (int64_t)h * d.total_rows + d.req_off[k.b];
+  return k;
+}
+
 __global__ void __launch_bounds__(256) plan_mark_kernel(PlanDev d) {
   const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (w >= (int64_t)d.T * d.Hkv) return;
@@ -140,63 +164,54 @@ __global__ void __launch_bounds__(256) plan_mark_kernel(PlanDev d) {
   const int h = (int)(w % d.Hkv);
   uint16_t mask = 0;
   if (d.counters[2] == 1) {
-    const int b = upper_index(d.cu_q, d.B, t);
-    const int i = t - d.cu_q[b];
-    const int64_t ql = d.cu_q[b + 1] - d.cu_q[b];
-    const int64_t sl = d.cu_k[b + 1] - d.cu_k[b];
-    const int64_t pos = sl - ql + i;
-    const int own = (int)(pos / kPage);
-    const int P = (int)ceil_div(sl, kPage);
-    const int64_t row0 = (int64_t)h * d.total_rows + d.req_off[b];
-    const int32_t* ids = d.topk + w * kTopK;
-    const int32_t* bt = d.block_table + (int64_t)b * d.bt_stride;
-    int32_t seen[kTopK];
+    const TokenInfo k = token_info(d, t, h);
+    int32_t ids[kTopK];
+    const int4* v = reinterpret_cast<const int4*>(d.topk + w * kTopK);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int4 x = v[q];
+      ids[4 * q] = x.x; ids[4 * q + 1] = x.y;
+      ids[4 * q + 2] = x.z; ids[4 * q + 3] = x.w;
+    }
+    const int32_t* bt = d.block_table + (int64_t)k.b * d.bt_stride;
     unsigned st = 0;
 #pragma unroll
     for (int j = 0; j < kTopK; ++j) {
       const int32_t p = ids[j];
-      seen[j] = p;
       if (p == -1) continue;
-      if (p < -1 || p >= P) { st |= MSA_STATUS_BAD_PAGE_ID; continue; }
+      if (p < -1 || p >= k.P) { st |= MSA_STATUS_BAD_PAGE_ID; continue; }
       bool dup = false;
 #pragma unroll
-      for (int k = 0; k < j; ++k) dup |= (seen[k] == p);
+      for (int q = 0; q < j; ++q) dup |= (ids[q] == p);
       if (dup) continue;
       const int32_t phys = bt[p];
       if (phys < 0 || (int64_t)phys >= d.num_pages) {
         st |= MSA_STATUS_BAD_BLOCK;
         continue;
       }
-      if (p > own) continue;
+      if (p > k.own) continue;
       mask |= (uint16_t)(1u << j);
-      atomicOr(d.bitmap + (row0 + p) * d.W + (i >> 5), 1u << (i & 31));
+      atomicOr(d.bitmap + (k.row0 + p) * d.W + (k.i >> 5), 1u << (k.i & 31));
     }
     if (st) atomicOr(d.status, st);
   }
   d.slot_mask[w] = mask;
 }
 
-// One CTA per tile of kPlanTile rows; warp k handles rows k*32 .. k*32+31.
-__global__ void __launch_bounds__(kPlanTile) plan_count_kernel(PlanDev d) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t tile0 = (int64_t)blockIdx.x * kPlanTile;
+// One thread per row, kPlanTile rows per CTA.
+__global__ void __launch_bounds__(kPlanTile) plan_rows_kernel(PlanDev d) {
+  const int64_t r = (int64_t)blockIdx.x * kPlanTile + threadIdx.x;
   const bool ok = d.counters[2] == 1;
-  __shared__ int s_cnt[kPlanTile];
-  for (int k = 0; k < 32; ++k) {
-    const int local = warp * 32 + k;
-    const int64_t r = tile0 + local;
-    int c = 0;
-    if (ok && r < d.rows) {
-      const uint32_t* words = d.bitmap + r * d.W;
-      for (int x = lane; x < d.W; x += 32) c += __popc(words[x]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-      if (lane == 0) d.row_cnt[r] = c;
+  int c = 0;
+  if (ok && r < d.rows) {
+    const uint32_t* words = d.bitmap + r * d.W;
+    int32_t* pre = d.word_pre + r * d.W;
+    for (int x = 0; x < d.W; ++x) {
+      pre[x] = c;
+      c += __popc(words[x]);
     }
-    if (lane == 0) s_cnt[local] = (r < d.rows) ? c : 0;
+    d.row_cnt[r] = c;
   }
-  __syncthreads();
-  const int c = s_cnt[threadIdx.x];
   const int chunks = (c + d.C - 1) / d.C;
   int tc, tw;
   block_excl_scan<kPlanTile>(c, &tc);
@@ -226,71 +241,58 @@ __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(PlanDev d) {
   }
 }
 
-__global__ void __launch_bounds__(kPlanTile) plan_fill_kernel(PlanDev d) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t tile0 = (int64_t)blockIdx.x * kPlanTile;
-  const int64_t r_me = tile0 + threadIdx.x;
+__global__ void __launch_bounds__(kPlanTile) plan_emit_kernel(PlanDev d) {
+  const int64_t r = (int64_t)blockIdx.x * kPlanTile + threadIdx.x;
   const bool ok = d.counters[2] == 1;
-  __shared__ int s_start[kPlanTile];
-  __shared__ int s_wstart[kPlanTile];
-  __shared__ int s_cnt[kPlanTile];
-  const int c = (ok && r_me < d.rows) ? d.row_cnt[r_me] : 0;
+  const int c = (ok && r < d.rows) ? d.row_cnt[r] : 0;
   const int chunks = (c + d.C - 1) / d.C;
   int tc, tw;
   const int ex_c = block_excl_scan<kPlanTile>(c, &tc);
   const int ex_w = block_excl_scan<kPlanTile>(chunks, &tw);
+  if (r >= d.rows) return;
   const int start = d.tile_sums[blockIdx.x] + ex_c;
   const int wstart = d.tile_sums[d.ntiles + blockIdx.x] + ex_w;
-  if (r_me < d.rows) d.row_ptr[r_me] = start;
-  s_start[threadIdx.x] = start;
-  s_wstart[threadIdx.x] = wstart;
-  s_cnt[threadIdx.x] = c;
-  __syncthreads();
-  if (!ok) return;
+  d.row_ptr[r] = start;
+  d.row_wptr[r] = wstart;
+  if (c == 0) return;
+  const int h = (int)(r / d.total_rows);
+  const int64_t rr = r - (int64_t)h * d.total_rows;
+  const int b = upper_index(d.req_off, d.B, rr);
+  const int p = (int)(rr - d.req_off[b]);
+  const int32_t phys = d.block_table[(int64_t)b * d.bt_stride + p];
+  for (int ch = 0; ch < chunks; ++ch) {
+    const int n = min(d.C, c - ch * d.C);
+    reinterpret_cast<int4*>(d.work)[wstart + ch] =
+        make_int4(start + ch * d.C, n, b, (h << 24) | p);
+    // record header: KV tile row of the pool, token count, first key
+    // position of the page, first query head of the KV head
+    d.records[(int64_t)(wstart + ch) * d.rec_stride] =
+        make_int4((phys * d.Hkv + h) * kPage, n, p * kPage, h * d.G);
+  }
+}
 
-  for (int k = 0; k < 32; ++k) {
-    const int local = warp * 32 + k;
-    const int64_t r = tile0 + local;
-    const int cnt = s_cnt[local];
-    if (r >= d.rows || cnt == 0) continue;
-    const int h = (int)(r / d.total_rows);
-    const int64_t rr = r - (int64_t)h * d.total_rows;
-    const int b = upper_index(d.req_off, d.B, rr);
-    const int p = (int)(rr - d.req_off[b]);
-    const int t0 = d.cu_q[b];
-    const int pos0 = s_start[local];
-    const uint32_t* words = d.bitmap + r * d.W;
-    // tokens, in ascending order
-    int done = 0;
-    for (int base = 0; base < d.W && done < cnt; base += 32) {
-      const uint32_t word = (base + lane < d.W) ? words[base + lane] : 0u;
-      const int n = __popc(word);
-      const int incl = warp_incl_scan(n);
-      int at = pos0 + done + incl - n;
-      uint32_t bits = word;
-      while (bits) {
-        const int bit = __ffs(bits) - 1;
-        bits &= bits - 1;
-        const int t = t0 + (base + lane) * 32 + bit;
-        const int32_t* ids = d.topk + ((int64_t)t * d.Hkv + h) * kTopK;
-        int j = 0;
-        while (j < kTopK - 1 && ids[j] != p) ++j;
-        d.q_idx[at] = t;
-        d.slot[at] = (uint8_t)j;
-        ++at;
-      }
-      done += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    // work items of this row
-    const int nch = (cnt + d.C - 1) / d.C;
-    for (int ch = lane; ch < nch; ch += 32) {
-      int4 item;
-      item.x = pos0 + ch * d.C;
-      item.y = min(d.C, cnt - ch * d.C);
-      item.z = b;
-      item.w = (h << 24) | p;
-      reinterpret_cast<int4*>(d.work)[s_wstart[local] + ch] = item;
-    }
+__global__ void __launch_bounds__(256) plan_scatter_kernel(PlanDev d) {
+  const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (w >= (int64_t)d.T * d.Hkv) return;
+  if (d.counters[2] != 1) return;
+  const uint32_t mask = d.slot_mask[w];
+  if (mask == 0) return;
+  const int t = (int)(w / d.Hkv);
+  const int h = (int)(w % d.Hkv);
+  const TokenInfo k = token_info(d, t, h);
+  const int32_t* ids = d.topk + w * kTopK;
+  const int word = k.i >> 5;
+  const uint32_t below = (1u << (k.i & 31)) - 1u;
+  for (uint32_t m = mask; m; m &= m - 1) {
+    const int j = __ffs(m) - 1;
+    const int64_t r = k.row0 + ids[j];
+    const int64_t wi = r * d.W + word;
+    const int rank = d.word_pre[wi] + __popc(d.bitmap[wi] & below);
+    const int at = d.row_ptr[r] + rank;
+    d.q_idx[at] = t;
+    d.slot[at] = (uint8_t)j;
+    const int64_t rec = d.row_wptr[r] + rank / d.C;
+    d.records[rec * d.rec_stride + 1 + rank % d.C] = make_int4(t, k.pos, j, 0);
   }
 }
 
@@ -308,6 +310,7 @@ cudaError_t launch_plan(const msa_plan_t& pl, const int32_t* topk,
   d.B = (int)pl.B;
   d.T = (int)pl.T;
   d.Hkv = (int)pl.Hkv;
+  d.G = (int)(pl.Hq / pl.Hkv);
   d.W = (int)pl.bitmap_words;
   d.C = (int)pl.chunk_tokens;
   d.total_rows = pl.total_rows;
@@ -316,13 +319,17 @@ cudaError_t launch_plan(const msa_plan_t& pl, const int32_t* topk,
   d.max_k = pl.max_seqlen_k;
   d.req_off = pl.req_off;
   d.bitmap = pl.bitmap;
+  d.word_pre = pl.word_pre;
   d.row_cnt = pl.row_cnt;
+  d.row_wptr = pl.row_wptr;
   d.tile_sums = pl.tile_sums;
   d.ntiles = (int)ceil_div(pl.rows, kPlanTile);
   d.row_ptr = pl.row_ptr;
   d.q_idx = pl.q_idx;
   d.slot = pl.slot;
   d.work = pl.work;
+  d.records = reinterpret_cast<int4*>(pl.records);
+  d.rec_stride = (int)(pl.record_bytes / 16);
   d.counters = pl.counters;
   d.slot_mask = pl.slot_mask;
   d.status = pl.status;
@@ -334,15 +341,14 @@ cudaError_t launch_plan(const msa_plan_t& pl, const int32_t* topk,
     e = cudaMemsetAsync(pl.bitmap, 0, bm, stream);
     if (e != cudaSuccess) return e;
   }
-  plan_prep_kernel<<<1, kScanThreads, 0, stream>>>(d);
   const int64_t marks = (int64_t)pl.T * pl.Hkv;
-  if (marks > 0)
-    plan_mark_kernel<<<(unsigned)ceil_div(marks, 256), 256, 0, stream>>>(d);
-  if (d.ntiles > 0)
-    plan_count_kernel<<<d.ntiles, kPlanTile, 0, stream>>>(d);
+  const unsigned mgrid = (unsigned)ceil_div(marks, 256);
+  plan_prep_kernel<<<1, kScanThreads, 0, stream>>>(d);
+  if (marks > 0) plan_mark_kernel<<<mgrid, 256, 0, stream>>>(d);
+  if (d.ntiles > 0) plan_rows_kernel<<<d.ntiles, kPlanTile, 0, stream>>>(d);
   plan_scan_kernel<<<1, kScanThreads, 0, stream>>>(d);
-  if (d.ntiles > 0)
-    plan_fill_kernel<<<d.ntiles, kPlanTile, 0, stream>>>(d);
+  if (d.ntiles > 0) plan_emit_kernel<<<d.ntiles, kPlanTile, 0, stream>>>(d);
+  if (marks > 0) plan_scatter_kernel<<<mgrid, 256, 0, stream>>>(d);
   return cudaGetLastError();
 }
 

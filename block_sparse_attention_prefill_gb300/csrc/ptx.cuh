@@ -91,6 +91,17 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst,
       : "memory");
 }
 
+// 1-D bulk copy global -> shared (size and both addresses multiples of 16),
+// completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc,
+                                          uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 
 __device__ __forceinline__ void cp_async_16(uint32_t smem_addr,

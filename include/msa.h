@@ -97,22 +97,30 @@ extern "C" {
  * each with `slot` = the list position j of that first occurrence.
  * work (the schedule): 4 int32 per item {csr start, token count, b,
  * (h << 24) | p}; rows in ascending order, each cut into chunks of
- * chunk_tokens = floor(128 / G) tokens; the item count is *num_work.
+ * chunk_tokens = floor(128 / G) tokens; the item count is counters[1].
+ * records: the same items as the attention kernel reads them, record_bytes
+ * each: an int4 header {KV row of the page in the pool, token count, first
+ * key position of the page, first query head} and one int4 per token
+ * {global token id, query position, slot j, 0}.
  */
 typedef struct msa_plan {
   int64_t B, T, Hq, Hkv, total_rows, max_seqlen_q, max_seqlen_k, num_pages;
   int64_t bt_stride, bitmap_words, chunk_tokens, max_nnz, max_work, rows;
+  int64_t record_bytes;
   const int32_t *cu_seqlens_q; /* caller's [B+1]                            */
   const int32_t *cu_seqlens_k; /* caller's [B+1]                            */
   int32_t *req_off;            /* [B+1]                                     */
   uint32_t *bitmap;            /* [rows * bitmap_words] token membership    */
+  int32_t *word_pre;           /* [rows * bitmap_words] tokens before word  */
   int32_t *row_cnt;            /* [rows]                                    */
+  int32_t *row_wptr;           /* [rows] first work item of the row         */
   int32_t *tile_sums;          /* [2 * tiles] row / chunk sums per tile     */
   int32_t *row_ptr;            /* [rows + 1]                                */
   int32_t *q_idx;              /* [max_nnz] global query token ids          */
   uint8_t *slot;               /* [max_nnz] top-k position j                */
   int32_t *work;               /* [max_work * 4]                            */
-  int32_t *counters;           /* [0] = nnz, [1] = num_work                 */
+  void *records;               /* [max_work * record_bytes]                 */
+  int32_t *counters;           /* [0] nnz, [1] work items, [2] plan valid   */
   uint16_t *slot_mask;         /* [T * Hkv] bit j: slot j holds a partial  */
   uint32_t *status;            /* [1] MSA_STATUS_* bits                     */
 } msa_plan_t;
@@ -158,7 +166,7 @@ MSA_API int msa_plan_workspace_bytes(int64_t B, int64_t T, int64_t Hq, int64_t H
  *   workspace     device buffer of msa_plan_workspace_bytes() bytes,
  *                 256-byte aligned; it holds the plan until it is rebuilt.
  *   plan          host struct, filled on return.
- * Launches 5 kernels and 2 memsets on `stream`; never synchronises.
+ * Launches 6 kernels and 2 memsets on `stream`; never synchronises.
  */
 MSA_API int msa_plan(const int32_t *topk, const int32_t *cu_seqlens_q,
              const int32_t *cu_seqlens_k, const int32_t *block_table,

@@ -42,6 +42,20 @@ def compare_plan(w, total_rows=None):
     got = [(int(a), int(b), int(c), int(d) >> 24, int(d) & 0xFFFFFF)
            for a, b, c, d in work]
     assert got == items
+    # the attention kernel's records: header {KV row, n, first key, first
+    # query head} and per token {t, position, slot}
+    recs = plan.records()[:nwork].cpu().numpy()
+    bt = w.block_table.numpy()
+    cu_q = w.cu_q.numpy()
+    G = w.G
+    for wi, (start, n, b, h, pg) in enumerate(items):
+        hdr = recs[wi, 0]
+        phys = int(bt[b, pg])
+        assert list(hdr) == [(phys * w.Hkv + h) * 128, n, pg * 128, h * G], wi
+        for k in range(n):
+            t = int(q_idx[start + k])
+            pos = w.seq_lens[b] - w.q_lens[b] + (t - int(cu_q[b]))
+            assert list(recs[wi, 1 + k, :3]) == [t, pos, int(slot[start + k])]
     return plan
 
 
