@@ -16,19 +16,22 @@
 // One CTA per SM, persistent over a contiguous range of the work list.
 // Every work item has a record written by the plan: {KV row of the page in
 // the pool, token count n, first key position, first query head} and, per
-// token, {token id, query position, top-k slot}.  Warp roles (12 warps):
+// token, {token id, query position, top-k slot}.  Warp roles (16 warps):
 //   warp 0      producer: bulk copy of the item's record, TMA loads of the
 //               K and V halves of the page (2 x 16 KB, 128-byte swizzle)
 //   warp 1      tcgen05 issuer (one thread) and TMEM owner (512 columns)
 //   warps 2-3   Q gather: n tokens x G heads rows of 128 B into the
 //               128-byte-swizzled K-major tile -- one TMA box per token
 //               when G is a multiple of 8, cp.async otherwise
-//   warps 4-7   softmax / epilogue group 0 (even items)
-//   warps 8-11  softmax / epilogue group 1 (odd items)
-// Shared memory: 3 stages of {K, V, Q} 16 KB tiles and a record, 2 P tiles.
+//   warps 4-7   softmax group 0 (even items)
+//   warps 8-11  softmax group 1 (odd items)
+//   warps 12-15 epilogue: O from TMEM, normalised, bf16 partials to HBM
+// Shared memory: 3 stages of {K, V, Q} 16 KB tiles and a record, 2 P
+// tiles, a 4-slot ring of per-row results handed from softmax to epilogue.
 // TMEM: per group an S tile (128 columns) and an O tile (128 columns).
-// MMA order: QK(0), QK(1), PV(0), QK(2), PV(1), ... so that the tensor
-// cores compute item n+1's scores while item n's softmax runs.
+// The MMA thread issues QK(n) and PV(n) as soon as each one's inputs are
+// ready, in order, so the tensor cores compute item n+1's scores while item
+// n's softmax runs and never wait on one item for the next one's data.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -41,9 +44,15 @@ namespace {
 
 constexpr int kStages = 3;
 constexpr int kTile = 128 * 128;  // one 128 x 128 E4M3 tile, bytes
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kTmemCols = 512;
+constexpr int kRegsControl = 40;
+constexpr int kRegsSoftmax = 176;
+constexpr int kRegsEpilogue = 120;
+static_assert(4 * 32 * kRegsControl + 8 * 32 * kRegsSoftmax +
+                  4 * 32 * kRegsEpilogue == 65536,
+              "register split must equal the launch allocation");
 constexpr int kRecMax = 16 * (1 + kTileM);  // header + up to 128 tokens
 
 // offsets from the 1024-byte aligned base
@@ -52,7 +61,15 @@ constexpr int kOffV = kOffK + kStages * kTile;
 constexpr int kOffQ = kOffV + kStages * kTile;
 constexpr int kOffP = kOffQ + kStages * kTile;
 constexpr int kOffRec = kOffP + 2 * kTile;
-constexpr int kOffBar = kOffRec + kStages * kRecMax;
+constexpr int kMetaSlots = 4;
+// per row: partial row index (int64, -1 = none), lse, 1/l * v_scale
+struct RowMeta {
+  int64_t prow;
+  float lse;
+  float inv;
+};
+constexpr int kOffMeta = kOffRec + kStages * kRecMax;
+constexpr int kOffBar = kOffMeta + kMetaSlots * kTileM * (int)sizeof(RowMeta);
 
 struct Barriers {
   uint64_t rec_full[kStages];
@@ -63,6 +80,7 @@ struct Barriers {
   uint64_t p_full[2];
   uint64_t o_full[2];
   uint64_t o_free[2];
+  uint64_t meta_full[kMetaSlots];
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -87,6 +105,58 @@ struct Params {
 __device__ __forceinline__ void set_timeout(Barriers* bars, uint32_t* status) {
   bars->abort = 1;
   atomicOr(status, (unsigned)MSA_STATUS_TIMEOUT);
+}
+
+// Rows of item li are placed rot(li) lanes further down the tile (mod 128)
+// so that small items -- a few tokens x G heads, fewer than 32 rows -- land
+// on a different TMEM lane quadrant, and so a different SM sub-partition,
+// from one item to the next.
+__device__ __forceinline__ int row_rotation(int li, int G) {
+  return (kTileM % G == 0) ? (li & 3) * 32 : 0;
+}
+
+// p = 2^(x * c + off) for 32 score columns, packed to E4M3 in pairs and
+// stored as two 16-byte chunks of the 128-byte-swizzled P row; returns the
+// sum of the (unrounded) probabilities.  kMask: columns past kv_lim are 0.
+template <bool kMask>
+__device__ __forceinline__ float exp_pack32(const uint32_t (&r)[32], int col0,
+                                            int kv_lim, float c, float off,
+                                            uint8_t* prow, int row) {
+  uint32_t packed[8];
+  float l = 0.f;
+#pragma unroll
+  for (int e = 0; e < 32; e += 4) {
+    float pv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float x = __uint_as_float(r[e + u]);
+      pv[u] = ex2_approx(fmaf(x, c, off));
+      if (kMask && col0 + e + u > kv_lim) pv[u] = 0.f;
+      l += pv[u];
+    }
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(pv[0], pv[1]),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(pv[2], pv[3]),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    packed[e / 4] = lo | (hi << 16);
+  }
+  const int c0 = col0 / 16, c1 = c0 + 1;
+  *reinterpret_cast<uint4*>(prow + ((c0 ^ (row & 7)) << 4)) =
+      make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  *reinterpret_cast<uint4*>(prow + ((c1 ^ (row & 7)) << 4)) =
+      make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  return l;
+}
+
+template <bool kMask>
+__device__ __forceinline__ float max32(const uint32_t (&r)[32], int col0,
+                                       int kv_lim, float m) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const float x = __uint_as_float(r[e]);
+    if (!kMask || col0 + e <= kv_lim) m = fmaxf(m, x);
+  }
+  return m;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -119,6 +189,8 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       mbar_init(&bars->o_full[w], 1);
       mbar_init(&bars->o_free[w], kSoftmaxThreads);
     }
+    for (int m = 0; m < kMetaSlots; ++m)
+      mbar_init(&bars->meta_full[m], kSoftmaxThreads);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -133,6 +205,12 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  // Launched with 128 registers per thread (512 threads); each role's
+  // warpgroup then resizes: softmax 176, epilogue 120, control warps 40
+  // (4*32*40 + 8*32*176 + 4*32*120 = 65536).
+
+  if (warp < 4) {
+  setmaxnreg_dec<kRegsControl>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -172,12 +250,8 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       constexpr uint32_t idesc_qk = idesc_e4m3_f32(128, 128, false);
       constexpr uint32_t idesc_pv = idesc_e4m3_f32(128, 128, true);
       bool ok = true;
-      auto issue_qk = [&](int li) -> bool {
-        const int s = li % kStages, round = li / kStages, w = li & 1;
-        if (!bounded_wait(&bars->kv_full[s], round & 1, abort, kWaitLimitNs))
-          return false;
-        if (!bounded_wait(&bars->q_full[s], round & 1, abort, kWaitLimitNs))
-          return false;
+      auto issue_qk = [&](int li) {
+        const int s = li % kStages, w = li & 1;
         tc_fence_after();
         const uint64_t a = smem_desc_sw128(smem_u32(smem + kOffQ + s * kTile), 16, 1024);
         const uint64_t b = smem_desc_sw128(smem_u32(smem + kOffK + s * kTile), 16, 1024);
@@ -187,15 +261,9 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
           mma_f8f6f4(d, a + (uint64_t)(kk * 2), b + (uint64_t)(kk * 2), idesc_qk,
                      kk > 0);
         mma_commit(&bars->s_full[w]);
-        return true;
       };
-      auto issue_pv = [&](int li) -> bool {
-        const int s = li % kStages, w = li & 1, k = li >> 1;
-        if (!bounded_wait(&bars->p_full[w], k & 1, abort, kWaitLimitNs))
-          return false;
-        if (k > 0 &&
-            !bounded_wait(&bars->o_free[w], (k - 1) & 1, abort, kWaitLimitNs))
-          return false;
+      auto issue_pv = [&](int li) {
+        const int s = li % kStages, w = li & 1;
         tc_fence_after();
         const uint64_t a = smem_desc_sw128(smem_u32(smem + kOffP + w * kTile), 16, 1024);
         const uint64_t b = smem_desc_sw128(smem_u32(smem + kOffV + s * kTile), 1024, 1024);
@@ -206,12 +274,37 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
                      idesc_pv, kk > 0);
         mma_commit(&bars->o_full[w]);
         mma_commit(&bars->stage_empty[s]);
-        return true;
       };
-      if (cnt > 0) ok = issue_qk(0);
-      for (int li = 0; ok && li < cnt; ++li) {
-        if (li + 1 < cnt && !issue_qk(li + 1)) { ok = false; break; }
-        if (!issue_pv(li)) { ok = false; break; }
+      // in-order issue of QK(qk) and PV(pv), each as soon as it is ready;
+      // QK(n) reuses the S tile of item n-2, free once PV(n-2) was issued
+      int qk = 0, pv = 0;
+      uint64_t idle_since = global_timer_ns();
+      while (pv < cnt) {
+        bool progressed = false;
+        if (qk < cnt && qk <= pv + 1) {
+          const int s = qk % kStages, ph = (qk / kStages) & 1;
+          if (mbar_test(&bars->kv_full[s], ph) &&
+              mbar_test(&bars->q_full[s], ph)) {
+            issue_qk(qk);
+            ++qk;
+            progressed = true;
+          }
+        }
+        if (pv < qk) {
+          const int w = pv & 1, k = pv >> 1;
+          if (mbar_test(&bars->p_full[w], k & 1) &&
+              (k == 0 || mbar_test(&bars->o_free[w], (k - 1) & 1))) {
+            issue_pv(pv);
+            ++pv;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          idle_since = global_timer_ns();
+        } else if (*abort || global_timer_ns() - idle_since > kWaitLimitNs) {
+          ok = false;
+          break;
+        }
       }
       if (!ok && !*abort) set_timeout(bars, p.status);
       mma_commit(&bars->mma_done);
@@ -234,9 +327,10 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
           const int4 hdr = rec[0];
           mbar_arrive_expect_tx(&bars->q_full[s], (uint32_t)(hdr.y * p.G * 128));
           uint8_t* dst = smem + kOffQ + s * kTile;
+          const int rot = row_rotation(li, p.G);
           for (int i = 0; i < hdr.y; ++i)
-            tma_load_2d(dst + i * p.G * 128, &q_map, &bars->q_full[s], 0,
-                        rec[1 + i].x * p.Hq + hdr.w);
+            tma_load_2d(dst + ((i * p.G + rot) & (kTileM - 1)) * 128, &q_map,
+                        &bars->q_full[s], 0, rec[1 + i].x * p.Hq + hdr.w);
         }
         if (!ok && !*abort) set_timeout(bars, p.status);
       }
@@ -253,10 +347,12 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         const int4* rec = reinterpret_cast<const int4*>(smem + kOffRec + s * kRecMax);
         const int4 hdr = rec[0];
         const int rows = hdr.y * p.G;
+        const int rot = row_rotation(li, p.G);
         const uint32_t dst0 = smem_u32(smem + kOffQ + s * kTile);
         for (int e = lane; e < rows * 8; e += 32) {
-          const int row = e >> 3, ch = e & 7;
-          const int i = row / p.G, g = row - i * p.G;
+          const int lrow = e >> 3, ch = e & 7;
+          const int i = lrow / p.G, g = lrow - i * p.G;
+          const int row = (lrow + rot) & (kTileM - 1);
           const int t = rec[1 + i].x;
           const uint8_t* src =
               p.q + ((int64_t)t * p.Hq + hdr.w + g) * kD + ch * 16;
@@ -270,16 +366,17 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       cp_async_wait<0>();
       if (!ok && lane == 0 && !*abort) set_timeout(bars, p.status);
     }
-  } else {
+  }
+  } else if (warp < 12) {
+    setmaxnreg_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
     const int w = (warp - 4) >> 2;       // group
     const int quad = warp & 3;           // TMEM lane quadrant
-    const int row = quad * 32 + lane;    // tile row = token i * G + head g
+    const int row = quad * 32 + lane;    // tile row = TMEM lane
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t s_tmem = tmem + lane_off + (uint32_t)(w * 256);
-    const uint32_t o_tmem = s_tmem + 128;
-    uint8_t* sP = smem + kOffP + w * kTile;
-    const int i = row / p.G, g = row - i * p.G;
+    uint8_t* prow_s = smem + kOffP + w * kTile + row * 128;
+    RowMeta* meta = reinterpret_cast<RowMeta*>(smem + kOffMeta);
     for (int k = 0;; ++k) {
       const int li = 2 * k + w;
       if (li >= cnt) break;
@@ -291,17 +388,26 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       }
       const int4* rec = reinterpret_cast<const int4*>(smem + kOffRec + s * kRecMax);
       const int4 hdr = rec[0];
+      // logical row (token i, head g) held by this lane for this item
+      const int lrow = (row - row_rotation(li, p.G)) & (kTileM - 1);
+      const int i = lrow / p.G, g = lrow - i * p.G;
       const bool valid = i < hdr.y;
-      const bool warp_valid = quad * 32 < hdr.y * p.G;
-      int t = 0, j = 0, kv_lim = 127;
+      const bool warp_valid = __any_sync(0xffffffffu, valid);
+      int64_t prow = -1;
+      int kv_lim = 127;
       if (valid) {
         const int4 tok = rec[1 + i];
-        t = tok.x;
-        j = tok.z;
+        prow = ((int64_t)tok.x * p.Hq + hdr.w + g) * kTopK + tok.z;
         kv_lim = min(tok.y - hdr.z, 127);
       }
-      const int hq = hdr.w + g;
+      const bool need_mask = __any_sync(0xffffffffu, valid && kv_lim < 127);
       if (!bounded_wait(&bars->s_full[w], k & 1, abort, kWaitLimitNs)) {
+        if (lane == 0 && !*abort) set_timeout(bars, p.status);
+        break;
+      }
+      // the P tile is free once PV of this group's previous item is done
+      if (k > 0 &&
+          !bounded_wait(&bars->o_full[w], (k - 1) & 1, abort, kWaitLimitNs)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
@@ -309,89 +415,105 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       float m2 = -INFINITY, l = 0.f;
       if (warp_valid) {
         __syncwarp();
-        uint32_t r[32];
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32(s_tmem + 0, r0);
+        tmem_ld32(s_tmem + 32, r1);
+        tmem_ld32(s_tmem + 64, r2);
+        tmem_ld32(s_tmem + 96, r3);
+        tmem_wait_ld();
         float m = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(s_tmem + c * 32, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e <= kv_lim) m = fmaxf(m, __uint_as_float(r[e]));
+        if (need_mask) {
+          m = max32<true>(r0, 0, kv_lim, m);
+          m = max32<true>(r1, 32, kv_lim, m);
+          m = max32<true>(r2, 64, kv_lim, m);
+          m = max32<true>(r3, 96, kv_lim, m);
+        } else {
+          m = max32<false>(r0, 0, kv_lim, m);
+          m = max32<false>(r1, 32, kv_lim, m);
+          m = max32<false>(r2, 64, kv_lim, m);
+          m = max32<false>(r3, 96, kv_lim, m);
         }
         m2 = m * p.score_log2;
         // p = 2^(x * c - m2 + 8): probabilities scaled by 256 so that small
         // ones stay out of E4M3's subnormal range; l and O carry the same
         // factor, which cancels.
         const float off = (m2 == -INFINITY) ? 0.f : 8.f - m2;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(s_tmem + c * 32, r);
-          tmem_wait_ld();
-          uint32_t packed[8];
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            float pv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float x = __uint_as_float(r[e + u]);
-              pv[u] = (c * 32 + e + u <= kv_lim)
-                          ? ex2_approx(fmaf(x, p.score_log2, off))
-                          : 0.f;
-              l += pv[u];
-            }
-            const uint32_t lo = __nv_cvt_float2_to_fp8x2(
-                make_float2(pv[0], pv[1]), __NV_SATFINITE, __NV_E4M3);
-            const uint32_t hi = __nv_cvt_float2_to_fp8x2(
-                make_float2(pv[2], pv[3]), __NV_SATFINITE, __NV_E4M3);
-            packed[e / 4] = lo | (hi << 16);
-          }
-          uint8_t* prow = sP + row * 128;
-          const int c0 = 2 * c, c1 = 2 * c + 1;
-          *reinterpret_cast<uint4*>(prow + ((c0 ^ (row & 7)) << 4)) =
-              make_uint4(packed[0], packed[1], packed[2], packed[3]);
-          *reinterpret_cast<uint4*>(prow + ((c1 ^ (row & 7)) << 4)) =
-              make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        const float c = p.score_log2;
+        if (need_mask) {
+          l += exp_pack32<true>(r0, 0, kv_lim, c, off, prow_s, row);
+          l += exp_pack32<true>(r1, 32, kv_lim, c, off, prow_s, row);
+          l += exp_pack32<true>(r2, 64, kv_lim, c, off, prow_s, row);
+          l += exp_pack32<true>(r3, 96, kv_lim, c, off, prow_s, row);
+        } else {
+          l += exp_pack32<false>(r0, 0, kv_lim, c, off, prow_s, row);
+          l += exp_pack32<false>(r1, 32, kv_lim, c, off, prow_s, row);
+          l += exp_pack32<false>(r2, 64, kv_lim, c, off, prow_s, row);
+          l += exp_pack32<false>(r3, 96, kv_lim, c, off, prow_s, row);
         }
       }
+      RowMeta mt;
+      mt.prow = prow;
+      mt.inv = l > 0.f ? p.v_scale / l : 0.f;
+      mt.lse = l > 0.f ? (m2 + __log2f(l) - 8.f) * 0.69314718055994530942f
+                       : -INFINITY;
+      meta[(li % kMetaSlots) * kTileM + row] = mt;
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->p_full[w]);
+      mbar_arrive(&bars->meta_full[li % kMetaSlots]);
+    }
+  } else {
+    setmaxnreg_dec<kRegsEpilogue>();
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const RowMeta* meta = reinterpret_cast<const RowMeta*>(smem + kOffMeta);
+    for (int li = 0; li < cnt; ++li) {
+      const int w = li & 1, k = li >> 1;
+      if (!bounded_wait(&bars->meta_full[li % kMetaSlots],
+                        (li / kMetaSlots) & 1, abort, kWaitLimitNs)) {
+        if (lane == 0 && !*abort) set_timeout(bars, p.status);
+        break;
+      }
+      const RowMeta mt = meta[(li % kMetaSlots) * kTileM + row];
+      const bool valid = mt.prow >= 0;
+      const bool warp_valid = __any_sync(0xffffffffu, valid);
       if (!bounded_wait(&bars->o_full[w], k & 1, abort, kWaitLimitNs)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
       tc_fence_after();
       if (warp_valid) {
-        const float inv = l > 0.f ? p.v_scale / l : 0.f;
-        uint16_t* dst =
-            p.part_o + (((int64_t)t * p.Hq + hq) * kTopK + j) * (int64_t)kD;
-        uint32_t r[32];
+        const uint32_t o_tmem = tmem + lane_off + (uint32_t)(w * 256 + 128);
+        uint16_t* dst = p.part_o + mt.prow * (int64_t)kD;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int half = 0; half < 2; ++half) {
+          uint32_t ra[32], rb[32];
           __syncwarp();
-          tmem_ld32(o_tmem + c * 32, r);
+          tmem_ld32(o_tmem + half * 64, ra);
+          tmem_ld32(o_tmem + half * 64 + 32, rb);
           tmem_wait_ld();
           if (valid) {
-            uint32_t o[16];
+            uint32_t o[32];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              __nv_bfloat162 v2 = __floats2bfloat162_rn(
-                  __uint_as_float(r[2 * e]) * inv,
-                  __uint_as_float(r[2 * e + 1]) * inv);
-              o[e] = *reinterpret_cast<uint32_t*>(&v2);
+              __nv_bfloat162 a2 = __floats2bfloat162_rn(
+                  __uint_as_float(ra[2 * e]) * mt.inv,
+                  __uint_as_float(ra[2 * e + 1]) * mt.inv);
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(
+                  __uint_as_float(rb[2 * e]) * mt.inv,
+                  __uint_as_float(rb[2 * e + 1]) * mt.inv);
+              o[e] = *reinterpret_cast<uint32_t*>(&a2);
+              o[16 + e] = *reinterpret_cast<uint32_t*>(&b2);
             }
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-            d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
-            d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
-            d4[2] = make_uint4(o[8], o[9], o[10], o[11]);
-            d4[3] = make_uint4(o[12], o[13], o[14], o[15]);
+            uint4* d4 = reinterpret_cast<uint4*>(dst + half * 64);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              d4[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
           }
         }
-        if (valid)
-          p.part_lse[((int64_t)t * p.Hq + hq) * kTopK + j] =
-              l > 0.f ? (m2 + __log2f(l) - 8.f) * 0.69314718055994530942f
-                      : -INFINITY;
+        if (valid) p.part_lse[mt.prow] = mt.lse;
       }
       tc_fence_before();
       mbar_arrive(&bars->o_free[w]);

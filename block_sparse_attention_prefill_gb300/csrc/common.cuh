@@ -7,7 +7,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/msa.h"
+#include "msa.h"
 
 namespace msa {
 

@@ -63,7 +63,7 @@ int plan_shape(int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t R,
   s->max_q = max_q;
   s->G = G;
   s->C = kTileM / G;
-  s->W = ceil_div(max_q, 32);
+  s->W = 4 * ceil_div(max_q, 128);  // 32-bit words, a multiple of 4
   s->rows = Hkv * R;
   s->ntiles = ceil_div(s->rows, kPlanTile);
   s->max_nnz = T * Hkv * kTopK;

@@ -8,9 +8,9 @@
 // Steps, all on `stream`, no host synchronisation:
 //   memset   status word and the (row, token) membership bitmap
 //   prep     one CTA: per-request row offsets (sum of page counts), checks
-//   mark     one thread per (token, KV head): validate its 16 ids, set one
-//            bit per kept page in the membership bitmap, write the token's
-//            slot mask.  This is the histogram, kept as bits: repeats
+//   mark     one thread per top-k entry: validate the id, drop repeats, set
+//            one bit per kept page in the membership bitmap; the (token,
+//            KV head) list's 16 threads together write its slot mask.  This is the histogram, kept as bits: repeats
 //            collapse and the order of arrival cannot change the result.
 //   rows     one thread per row: row length (popcount of its words), the
 //            running count in front of every word, and per-tile sums of the
@@ -18,7 +18,7 @@
 //   scan     one CTA: exclusive scan of the tile sums
 //   emit     one thread per row: row_ptr, the row's first work item, and the
 //            work items / record headers of its chunks
-//   scatter  one thread per (token, KV head): each kept entry goes to
+//   scatter  one thread per top-k entry: each kept entry goes to
 //            row_ptr + (tokens of the same row before it), found in O(1)
 //            from the word prefix and a popcount; it also fills the token
 //            slot of the work record the attention kernel will read.
@@ -157,58 +157,77 @@ __device__ __forceinline__ TokenInfo token_info(const PlanDev& d, int t, int h) 
   return k;
 }
 
+// One thread per top-k entry (t, h, j); the 16 entries of a (t, h) list sit
+// in one half-warp and see each other through shuffles.
 __global__ void __launch_bounds__(256) plan_mark_kernel(PlanDev d) {
-  const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (w >= (int64_t)d.T * d.Hkv) return;
-  const int t = (int)(w / d.Hkv);
-  const int h = (int)(w % d.Hkv);
-  uint16_t mask = 0;
-  if (d.counters[2] == 1) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t total = (int64_t)d.T * d.Hkv * kTopK;
+  const int lane = threadIdx.x & 31;
+  const int j = lane & (kTopK - 1);
+  const bool live = e < total;
+  const int64_t w = e / kTopK;
+  const int32_t p = live ? d.topk[e] : -1;
+  // ids of the same list at positions before j
+  bool dup = false;
+#pragma unroll
+  for (int q = 0; q < kTopK; ++q) {
+    const int32_t o = __shfl_sync(0xffffffffu, p, (lane & ~(kTopK - 1)) + q);
+    dup |= (q < j) && (o == p);
+  }
+  bool keep = false;
+  if (live && d.counters[2] == 1) {
+    const int t = (int)(w / d.Hkv);
+    const int h = (int)(w % d.Hkv);
     const TokenInfo k = token_info(d, t, h);
-    int32_t ids[kTopK];
-    const int4* v = reinterpret_cast<const int4*>(d.topk + w * kTopK);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int4 x = v[q];
-      ids[4 * q] = x.x; ids[4 * q + 1] = x.y;
-      ids[4 * q + 2] = x.z; ids[4 * q + 3] = x.w;
-    }
-    const int32_t* bt = d.block_table + (int64_t)k.b * d.bt_stride;
     unsigned st = 0;
-#pragma unroll
-    for (int j = 0; j < kTopK; ++j) {
-      const int32_t p = ids[j];
-      if (p == -1) continue;
-      if (p < -1 || p >= k.P) { st |= MSA_STATUS_BAD_PAGE_ID; continue; }
-      bool dup = false;
-#pragma unroll
-      for (int q = 0; q < j; ++q) dup |= (ids[q] == p);
-      if (dup) continue;
-      const int32_t phys = bt[p];
-      if (phys < 0 || (int64_t)phys >= d.num_pages) {
-        st |= MSA_STATUS_BAD_BLOCK;
-        continue;
+    if (p != -1) {
+      if (p < -1 || p >= k.P) {
+        st |= MSA_STATUS_BAD_PAGE_ID;
+      } else if (!dup) {
+        const int32_t phys = d.block_table[(int64_t)k.b * d.bt_stride + p];
+        if (phys < 0 || (int64_t)phys >= d.num_pages) {
+          st |= MSA_STATUS_BAD_BLOCK;
+        } else if (p <= k.own) {
+          keep = true;
+          atomicOr(d.bitmap + (k.row0 + p) * d.W + (k.i >> 5),
+                   1u << (k.i & 31));
+        }
       }
-      if (p > k.own) continue;
-      mask |= (uint16_t)(1u << j);
-      atomicOr(d.bitmap + (k.row0 + p) * d.W + (k.i >> 5), 1u << (k.i & 31));
     }
     if (st) atomicOr(d.status, st);
   }
-  d.slot_mask[w] = mask;
+  const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+  if (live && j == 0)
+    d.slot_mask[w] = (uint16_t)((bal >> (lane & ~(kTopK - 1))) & 0xFFFFu);
 }
 
-// One thread per row, kPlanTile rows per CTA.
+// One thread per row, kPlanTile rows per CTA.  Rows are 16-byte aligned
+// (W is a multiple of 4), read and written four words at a time.
 __global__ void __launch_bounds__(kPlanTile) plan_rows_kernel(PlanDev d) {
   const int64_t r = (int64_t)blockIdx.x * kPlanTile + threadIdx.x;
   const bool ok = d.counters[2] == 1;
   int c = 0;
   if (ok && r < d.rows) {
-    const uint32_t* words = d.bitmap + r * d.W;
-    int32_t* pre = d.word_pre + r * d.W;
-    for (int x = 0; x < d.W; ++x) {
-      pre[x] = c;
-      c += __popc(words[x]);
+    const uint4* __restrict__ words =
+        reinterpret_cast<const uint4*>(d.bitmap + r * d.W);
+    int4* __restrict__ pre = reinterpret_cast<int4*>(d.word_pre + r * d.W);
+    const int nv = d.W >> 2;
+    for (int x0 = 0; x0 < nv; x0 += 4) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (x0 + u < nv) v[u] = words[x0 + u];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (x0 + u < nv) {
+          int4 o;
+          o.x = c; c += __popc(v[u].x);
+          o.y = c; c += __popc(v[u].y);
+          o.z = c; c += __popc(v[u].z);
+          o.w = c; c += __popc(v[u].w);
+          pre[x0 + u] = o;
+        }
+      }
     }
     d.row_cnt[r] = c;
   }
@@ -271,29 +290,27 @@ __global__ void __launch_bounds__(kPlanTile) plan_emit_kernel(PlanDev d) {
   }
 }
 
+// One thread per kept top-k entry: its place in the row is the number of
+// tokens of the row before it, read from the word prefix plus a popcount.
 __global__ void __launch_bounds__(256) plan_scatter_kernel(PlanDev d) {
-  const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (w >= (int64_t)d.T * d.Hkv) return;
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= (int64_t)d.T * d.Hkv * kTopK) return;
   if (d.counters[2] != 1) return;
-  const uint32_t mask = d.slot_mask[w];
-  if (mask == 0) return;
+  const int64_t w = e / kTopK;
+  const int j = (int)(e % kTopK);
+  if (!((d.slot_mask[w] >> j) & 1u)) return;
   const int t = (int)(w / d.Hkv);
   const int h = (int)(w % d.Hkv);
   const TokenInfo k = token_info(d, t, h);
-  const int32_t* ids = d.topk + w * kTopK;
-  const int word = k.i >> 5;
+  const int64_t r = k.row0 + d.topk[e];
+  const int64_t wi = r * d.W + (k.i >> 5);
   const uint32_t below = (1u << (k.i & 31)) - 1u;
-  for (uint32_t m = mask; m; m &= m - 1) {
-    const int j = __ffs(m) - 1;
-    const int64_t r = k.row0 + ids[j];
-    const int64_t wi = r * d.W + word;
-    const int rank = d.word_pre[wi] + __popc(d.bitmap[wi] & below);
-    const int at = d.row_ptr[r] + rank;
-    d.q_idx[at] = t;
-    d.slot[at] = (uint8_t)j;
-    const int64_t rec = d.row_wptr[r] + rank / d.C;
-    d.records[rec * d.rec_stride + 1 + rank % d.C] = make_int4(t, k.pos, j, 0);
-  }
+  const int rank = d.word_pre[wi] + __popc(d.bitmap[wi] & below);
+  const int at = d.row_ptr[r] + rank;
+  const int64_t rec = d.row_wptr[r] + rank / d.C;
+  d.q_idx[at] = t;
+  d.slot[at] = (uint8_t)j;
+  d.records[rec * d.rec_stride + 1 + rank % d.C] = make_int4(t, k.pos, j, 0);
 }
 
 }  // namespace
@@ -341,7 +358,7 @@ cudaError_t launch_plan(const msa_plan_t& pl, const int32_t* topk,
     e = cudaMemsetAsync(pl.bitmap, 0, bm, stream);
     if (e != cudaSuccess) return e;
   }
-  const int64_t marks = (int64_t)pl.T * pl.Hkv;
+  const int64_t marks = (int64_t)pl.T * pl.Hkv * kTopK;
   const unsigned mgrid = (unsigned)ceil_div(marks, 256);
   plan_prep_kernel<<<1, kScanThreads, 0, stream>>>(d);
   if (marks > 0) plan_mark_kernel<<<mgrid, 256, 0, stream>>>(d);
