@@ -317,8 +317,10 @@ def run_ours(args, rank, world):
 # ---------------------------------------------------------------- oracle
 
 def oracle_sample_rate(w, budget_s, nthreads):
-    """Time the FP64 oracle on a bounded sample of tokens of ``w``; returns
-    (TFLOP/s, seconds, tokens, description)."""
+    """Time the FP64 oracle on a bounded sample of ``w``: a growing subset
+    of query tokens, or repeated passes over all of them once the whole
+    workload takes less than the budget; returns (TFLOP/s, seconds,
+    description)."""
     import oracle
 
     n = 8
@@ -332,9 +334,18 @@ def oracle_sample_rate(w, budget_s, nthreads):
             break
         n = int(min(w.T, max(n * 2, n * budget_s / max(dt, 1e-3) * 1.1)))
     flops = 4.0 * 128 * float(nk.sum()) * w.G
+    reps = 1
+    if dt < budget_s:
+        reps = int(math.ceil(budget_s / max(dt, 1e-3)))
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            oracle.attention(w, tokens=toks, nthreads=nthreads)
+        dt = time.perf_counter() - t0
     desc = "%d of %d query tokens (all %d heads, all their selected pages)" % (
         len(toks), w.T, w.Hq)
-    return flops / dt / 1e12, dt, len(toks), desc
+    if reps > 1:
+        desc += ", %d passes" % reps
+    return flops * reps / dt / 1e12, dt, desc
 
 
 def run_reference(args, rank, world):
@@ -458,7 +469,7 @@ def main():
         if not args.no_cpu_baseline:
             wc = w.to("cpu")
             nthreads = os.cpu_count() or 1
-            rate, dt, ntok, desc = oracle_sample_rate(wc, 12.0, nthreads)
+            rate, dt, desc = oracle_sample_rate(wc, 12.0, nthreads)
             line["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s",
                                     "cores": nthreads, "kind": "oracle",
                                     "sample": desc + ", %.1f s" % dt}

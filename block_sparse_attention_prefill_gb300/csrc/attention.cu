@@ -19,15 +19,19 @@
 // token, {token id, query position, top-k slot}.  Warp roles (16 warps):
 //   warp 0      producer: bulk copy of the item's record, TMA loads of the
 //               K and V halves of the page (2 x 16 KB, 128-byte swizzle)
+//               and, when G is a multiple of 8, of the Q rows: one box of G
+//               rows per token, issued by one lane per token from token ids
+//               prefetched out of the record in global memory
 //   warp 1      tcgen05 issuer (one thread) and TMEM owner (512 columns)
-//   warps 2-3   Q gather: n tokens x G heads rows of 128 B into the
-//               128-byte-swizzled K-major tile -- one TMA box per token
-//               when G is a multiple of 8, cp.async otherwise
+//   warps 2-3   Q gather when G is not a multiple of 8: cp.async of 16-byte
+//               chunks into the 128-byte-swizzled K-major tile
 //   warps 4-7   softmax group 0 (even items)
 //   warps 8-11  softmax group 1 (odd items)
 //   warps 12-15 epilogue: O from TMEM, normalised, bf16 partials to HBM
-// Shared memory: 3 stages of {K, V, Q} 16 KB tiles and a record, 2 P
-// tiles, a 4-slot ring of per-row results handed from softmax to epilogue.
+// Shared memory: a 4-slot ring of {K, V} 16 KB tiles with the item's record
+// (released when PV completes), a 3-slot ring of Q tiles (released when QK
+// completes), 2 P tiles, and a 4-slot ring of per-row results handed from
+// softmax to epilogue.
 // TMEM: per group an S tile (128 columns) and an O tile (128 columns).
 // The MMA thread issues QK(n) and PV(n) as soon as each one's inputs are
 // ready, in order, so the tensor cores compute item n+1's scores while item
@@ -42,24 +46,25 @@
 namespace msa {
 namespace {
 
-constexpr int kStages = 3;
+constexpr int kKvStages = 4;
+constexpr int kQStages = 3;
 constexpr int kTile = 128 * 128;  // one 128 x 128 E4M3 tile, bytes
 constexpr int kThreads = 512;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kTmemCols = 512;
-constexpr int kRegsControl = 40;
+constexpr int kRegsControl = 48;
 constexpr int kRegsSoftmax = 176;
-constexpr int kRegsEpilogue = 120;
+constexpr int kRegsEpilogue = 104;
 static_assert(4 * 32 * kRegsControl + 8 * 32 * kRegsSoftmax +
-                  4 * 32 * kRegsEpilogue == 65536,
+                  4 * 32 * kRegsEpilogue <= 65536,
               "register split must equal the launch allocation");
 constexpr int kRecMax = 16 * (1 + kTileM);  // header + up to 128 tokens
 
 // offsets from the 1024-byte aligned base
 constexpr int kOffK = 0;
-constexpr int kOffV = kOffK + kStages * kTile;
-constexpr int kOffQ = kOffV + kStages * kTile;
-constexpr int kOffP = kOffQ + kStages * kTile;
+constexpr int kOffV = kOffK + kKvStages * kTile;
+constexpr int kOffQ = kOffV + kKvStages * kTile;
+constexpr int kOffP = kOffQ + kQStages * kTile;
 constexpr int kOffRec = kOffP + 2 * kTile;
 constexpr int kMetaSlots = 4;
 // per row: partial row index (int64, -1 = none), lse, 1/l * v_scale
@@ -68,14 +73,15 @@ struct RowMeta {
   float lse;
   float inv;
 };
-constexpr int kOffMeta = kOffRec + kStages * kRecMax;
+constexpr int kOffMeta = kOffRec + kKvStages * kRecMax;
 constexpr int kOffBar = kOffMeta + kMetaSlots * kTileM * (int)sizeof(RowMeta);
 
 struct Barriers {
-  uint64_t rec_full[kStages];
-  uint64_t kv_full[kStages];
-  uint64_t q_full[kStages];
-  uint64_t stage_empty[kStages];
+  uint64_t rec_full[kKvStages];
+  uint64_t kv_full[kKvStages];
+  uint64_t kv_empty[kKvStages];
+  uint64_t q_full[kQStages];
+  uint64_t q_empty[kQStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_full[2];
@@ -87,6 +93,7 @@ struct Barriers {
 };
 
 constexpr int kSmemBytes = kOffBar + (int)sizeof(Barriers) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory above the 227 KB limit");
 
 struct Params {
   const uint8_t* q;
@@ -110,9 +117,11 @@ __device__ __forceinline__ void set_timeout(Barriers* bars, uint32_t* status) {
 // Rows of item li are placed rot(li) lanes further down the tile (mod 128)
 // so that small items -- a few tokens x G heads, fewer than 32 rows -- land
 // on a different TMEM lane quadrant, and so a different SM sub-partition,
-// from one item to the next.
+// from one item to the next.  Only for G dividing 32: then a token's G rows
+// start at a multiple of G and never straddle the end of the tile (a TMA
+// box does not wrap around).
 __device__ __forceinline__ int row_rotation(int li, int G) {
-  return (kTileM % G == 0) ? (li & 3) * 32 : 0;
+  return (G <= 32 && 32 % G == 0) ? (li & 3) * 32 : 0;
 }
 
 // p = 2^(x * c + off) for 32 score columns, packed to E4M3 in pairs and
@@ -177,11 +186,14 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
   const int cnt = end - begin;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKvStages; ++s) {
       mbar_init(&bars->rec_full[s], 1);
       mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int s = 0; s < kQStages; ++s) {
       mbar_init(&bars->q_full[s], p.q_tma ? 1 : 32);
-      mbar_init(&bars->stage_empty[s], 1);
+      mbar_init(&bars->q_empty[s], 1);
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(&bars->s_full[w], 1);
@@ -206,44 +218,77 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
   const uint32_t tmem = bars->tmem_base;
 
   // Launched with 128 registers per thread (512 threads); each role's
-  // warpgroup then resizes: softmax 176, epilogue 120, control warps 40
-  // (4*32*40 + 8*32*176 + 4*32*120 = 65536).
+  // warpgroup then resizes: softmax 176, epilogue 104, control warps 48
+  // (4*32*48 + 8*32*176 + 4*32*104 = 64512 <= 65536).
 
   if (warp < 4) {
   setmaxnreg_dec<kRegsControl>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int issued = 0;
-      int4 next = cnt > 0 ? p.records[(int64_t)begin * p.rec_stride]
-                          : make_int4(0, 0, 0, 0);
-      for (int li = 0; li < cnt; ++li) {
-        const int s = li % kStages, round = li / kStages;
-        const int4 hdr = next;
-        if (li + 1 < cnt) next = p.records[(int64_t)(begin + li + 1) * p.rec_stride];
-        if (round > 0 && !bounded_wait(&bars->stage_empty[s], (round - 1) & 1,
-                                       abort, kWaitLimitNs)) {
-          if (!*abort) set_timeout(bars, p.status);
-          break;
-        }
+    // whole warp: lane 0 waits for free slots and issues the record / K / V
+    // copies; in TMA-Q mode lane i issues the Q box of the item's token i
+    // (C = 128 / G <= 16 tokens).  Header and token ids of the next item
+    // are prefetched from the record in global memory.
+    const int4* grec = p.records + (int64_t)begin * p.rec_stride;
+    const int C = kTileM / p.G;
+    int4 hdr_next = cnt > 0 ? grec[0] : make_int4(0, 0, 0, 0);
+    int tok_next = (cnt > 0 && p.q_tma && lane < C) ? grec[1 + lane].x : 0;
+    int issued = 0;
+    for (int li = 0; li < cnt; ++li) {
+      const int ks = li % kKvStages, qs = li % kQStages;
+      const int4 hdr = hdr_next;
+      const int tok = tok_next;
+      if (li + 1 < cnt) {
+        const int4* nr = grec + (int64_t)(li + 1) * p.rec_stride;
+        hdr_next = nr[0];
+        if (p.q_tma && lane < C) tok_next = nr[1 + lane].x;
+      }
+      int ok = 1;
+      if (lane == 0) {
+        if (li >= kKvStages)
+          ok = bounded_wait(&bars->kv_empty[ks], ((li / kKvStages) - 1) & 1,
+                            abort, kWaitLimitNs);
+        if (ok && li >= kQStages)
+          ok = bounded_wait(&bars->q_empty[qs], ((li / kQStages) - 1) & 1,
+                            abort, kWaitLimitNs);
+        if (!ok && !*abort) set_timeout(bars, p.status);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (lane == 0) {
         const uint32_t rec_bytes = 16u * (1u + (uint32_t)hdr.y);
-        mbar_arrive_expect_tx(&bars->rec_full[s], rec_bytes);
-        bulk_load(smem + kOffRec + s * kRecMax,
+        mbar_arrive_expect_tx(&bars->rec_full[ks], rec_bytes);
+        bulk_load(smem + kOffRec + ks * kRecMax,
                   p.records + (int64_t)(begin + li) * p.rec_stride, rec_bytes,
-                  &bars->rec_full[s]);
-        mbar_arrive_expect_tx(&bars->kv_full[s], 2 * kTile);
-        tma_load_2d(smem + kOffK + s * kTile, &kv_map, &bars->kv_full[s], 0, hdr.x);
-        tma_load_2d(smem + kOffV + s * kTile, &kv_map, &bars->kv_full[s], kD, hdr.x);
-        issued = li + 1;
+                  &bars->rec_full[ks]);
+        mbar_arrive_expect_tx(&bars->kv_full[ks], 2 * kTile);
+        tma_load_2d(smem + kOffK + ks * kTile, &kv_map, &bars->kv_full[ks], 0, hdr.x);
+        tma_load_2d(smem + kOffV + ks * kTile, &kv_map, &bars->kv_full[ks], kD, hdr.x);
+        if (p.q_tma)
+          mbar_arrive_expect_tx(&bars->q_full[qs], (uint32_t)(hdr.y * p.G * 128));
       }
-      // every copy this thread started must land before the CTA exits
-      for (int li = issued > kStages ? issued - kStages : 0; li < issued; ++li) {
-        bounded_wait(&bars->rec_full[li % kStages], (li / kStages) & 1, nullptr,
-                     kWaitLimitNs);
-        bounded_wait(&bars->kv_full[li % kStages], (li / kStages) & 1, nullptr,
-                     kWaitLimitNs);
+      if (p.q_tma) {
+        __syncwarp();
+        if (lane < hdr.y)
+          tma_load_2d(smem + kOffQ + qs * kTile +
+                          ((lane * p.G + row_rotation(li, p.G)) & (kTileM - 1)) * 128,
+                      &q_map, &bars->q_full[qs], 0, tok * p.Hq + hdr.w);
       }
+      issued = li + 1;
     }
+    // every copy this warp started must land before the CTA exits
+    if (lane == 0) {
+      for (int li = issued > kKvStages ? issued - kKvStages : 0; li < issued; ++li) {
+        bounded_wait(&bars->rec_full[li % kKvStages], (li / kKvStages) & 1,
+                     nullptr, kWaitLimitNs);
+        bounded_wait(&bars->kv_full[li % kKvStages], (li / kKvStages) & 1,
+                     nullptr, kWaitLimitNs);
+      }
+      if (p.q_tma)
+        for (int li = issued > kQStages ? issued - kQStages : 0; li < issued; ++li)
+          bounded_wait(&bars->q_full[li % kQStages], (li / kQStages) & 1,
+                       nullptr, kWaitLimitNs);
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -251,29 +296,30 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       constexpr uint32_t idesc_pv = idesc_e4m3_f32(128, 128, true);
       bool ok = true;
       auto issue_qk = [&](int li) {
-        const int s = li % kStages, w = li & 1;
+        const int ks = li % kKvStages, qs = li % kQStages, w = li & 1;
         tc_fence_after();
-        const uint64_t a = smem_desc_sw128(smem_u32(smem + kOffQ + s * kTile), 16, 1024);
-        const uint64_t b = smem_desc_sw128(smem_u32(smem + kOffK + s * kTile), 16, 1024);
+        const uint64_t a = smem_desc_sw128(smem_u32(smem + kOffQ + qs * kTile), 16, 1024);
+        const uint64_t b = smem_desc_sw128(smem_u32(smem + kOffK + ks * kTile), 16, 1024);
         const uint32_t d = tmem + (uint32_t)(w * 256);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // K = 128 bytes = 4 x 32
           mma_f8f6f4(d, a + (uint64_t)(kk * 2), b + (uint64_t)(kk * 2), idesc_qk,
                      kk > 0);
         mma_commit(&bars->s_full[w]);
+        mma_commit(&bars->q_empty[qs]);
       };
       auto issue_pv = [&](int li) {
-        const int s = li % kStages, w = li & 1;
+        const int ks = li % kKvStages, w = li & 1;
         tc_fence_after();
         const uint64_t a = smem_desc_sw128(smem_u32(smem + kOffP + w * kTile), 16, 1024);
-        const uint64_t b = smem_desc_sw128(smem_u32(smem + kOffV + s * kTile), 1024, 1024);
+        const uint64_t b = smem_desc_sw128(smem_u32(smem + kOffV + ks * kTile), 1024, 1024);
         const uint32_t d = tmem + (uint32_t)(w * 256 + 128);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // 128 keys = 4 x 32; V rows advance 4 KB
           mma_f8f6f4(d, a + (uint64_t)(kk * 2), b + (uint64_t)(kk * 256),
                      idesc_pv, kk > 0);
         mma_commit(&bars->o_full[w]);
-        mma_commit(&bars->stage_empty[s]);
+        mma_commit(&bars->kv_empty[ks]);
       };
       // in-order issue of QK(qk) and PV(pv), each as soon as it is ready;
       // QK(n) reuses the S tile of item n-2, free once PV(n-2) was issued
@@ -282,9 +328,8 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       while (pv < cnt) {
         bool progressed = false;
         if (qk < cnt && qk <= pv + 1) {
-          const int s = qk % kStages, ph = (qk / kStages) & 1;
-          if (mbar_test(&bars->kv_full[s], ph) &&
-              mbar_test(&bars->q_full[s], ph)) {
+          if (mbar_test(&bars->kv_full[qk % kKvStages], (qk / kKvStages) & 1) &&
+              mbar_test(&bars->q_full[qk % kQStages], (qk / kQStages) & 1)) {
             issue_qk(qk);
             ++qk;
             progressed = true;
@@ -312,43 +357,26 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------ Q gather
-    bool ok = true;
-    if (p.q_tma) {
-      // one thread, no blocking on the copies: TMA boxes of G rows
-      if (warp == 2 && lane == 0) {
-        for (int li = 0; li < cnt; ++li) {
-          const int s = li % kStages;
-          if (!bounded_wait(&bars->rec_full[s], (li / kStages) & 1, abort,
-                            kWaitLimitNs)) {
-            ok = false;
-            break;
-          }
-          const int4* rec = reinterpret_cast<const int4*>(smem + kOffRec + s * kRecMax);
-          const int4 hdr = rec[0];
-          mbar_arrive_expect_tx(&bars->q_full[s], (uint32_t)(hdr.y * p.G * 128));
-          uint8_t* dst = smem + kOffQ + s * kTile;
-          const int rot = row_rotation(li, p.G);
-          for (int i = 0; i < hdr.y; ++i)
-            tma_load_2d(dst + ((i * p.G + rot) & (kTileM - 1)) * 128, &q_map,
-                        &bars->q_full[s], 0, rec[1 + i].x * p.Hq + hdr.w);
-        }
-        if (!ok && !*abort) set_timeout(bars, p.status);
-      }
-    } else {
-      // two warps take alternate items; 16-byte cp.async into the swizzled
-      // layout, then a proxy fence so the tensor cores see the rows
+    // (cp.async mode only) two warps take alternate items; 16-byte chunks
+    // into the swizzled layout, then a proxy fence so the tensor cores see
+    // the rows.
+    if (!p.q_tma) {
+      bool ok = true;
       for (int li = warp - 2; li < cnt; li += 2) {
-        const int s = li % kStages;
-        if (!bounded_wait(&bars->rec_full[s], (li / kStages) & 1, abort,
-                          kWaitLimitNs)) {
+        const int ks = li % kKvStages, qs = li % kQStages;
+        if (!bounded_wait(&bars->rec_full[ks], (li / kKvStages) & 1, abort,
+                          kWaitLimitNs) ||
+            (li >= kQStages &&
+             !bounded_wait(&bars->q_empty[qs], ((li / kQStages) - 1) & 1, abort,
+                           kWaitLimitNs))) {
           ok = false;
           break;
         }
-        const int4* rec = reinterpret_cast<const int4*>(smem + kOffRec + s * kRecMax);
+        const int4* rec = reinterpret_cast<const int4*>(smem + kOffRec + ks * kRecMax);
         const int4 hdr = rec[0];
         const int rows = hdr.y * p.G;
         const int rot = row_rotation(li, p.G);
-        const uint32_t dst0 = smem_u32(smem + kOffQ + s * kTile);
+        const uint32_t dst0 = smem_u32(smem + kOffQ + qs * kTile);
         for (int e = lane; e < rows * 8; e += 32) {
           const int lrow = e >> 3, ch = e & 7;
           const int i = lrow / p.G, g = lrow - i * p.G;
@@ -361,7 +389,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         cp_async_commit();
         cp_async_wait<0>();
         fence_proxy_async_smem();
-        mbar_arrive(&bars->q_full[s]);
+        mbar_arrive(&bars->q_full[qs]);
       }
       cp_async_wait<0>();
       if (!ok && lane == 0 && !*abort) set_timeout(bars, p.status);
@@ -380,13 +408,13 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     for (int k = 0;; ++k) {
       const int li = 2 * k + w;
       if (li >= cnt) break;
-      const int s = li % kStages;
-      if (!bounded_wait(&bars->rec_full[s], (li / kStages) & 1, abort,
+      const int ks = li % kKvStages;
+      if (!bounded_wait(&bars->rec_full[ks], (li / kKvStages) & 1, abort,
                         kWaitLimitNs)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
-      const int4* rec = reinterpret_cast<const int4*>(smem + kOffRec + s * kRecMax);
+      const int4* rec = reinterpret_cast<const int4*>(smem + kOffRec + ks * kRecMax);
       const int4 hdr = rec[0];
       // logical row (token i, head g) held by this lane for this item
       const int lrow = (row - row_rotation(li, p.G)) & (kTileM - 1);
