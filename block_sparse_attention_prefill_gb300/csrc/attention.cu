@@ -48,13 +48,14 @@ namespace {
 
 constexpr int kKvStages = 4;
 constexpr int kQStages = 3;
+constexpr int kBatch = 8;  // items whose headers / token ids are prefetched
 constexpr int kTile = 128 * 128;  // one 128 x 128 E4M3 tile, bytes
 constexpr int kThreads = 512;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kTmemCols = 512;
-constexpr int kRegsControl = 48;
+constexpr int kRegsControl = 72;
 constexpr int kRegsSoftmax = 176;
-constexpr int kRegsEpilogue = 104;
+constexpr int kRegsEpilogue = 80;
 static_assert(4 * 32 * kRegsControl + 8 * 32 * kRegsSoftmax +
                   4 * 32 * kRegsEpilogue <= 65536,
               "register split must equal the launch allocation");
@@ -218,76 +219,64 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
   const uint32_t tmem = bars->tmem_base;
 
   // Launched with 128 registers per thread (512 threads); each role's
-  // warpgroup then resizes: softmax 176, epilogue 104, control warps 48
-  // (4*32*48 + 8*32*176 + 4*32*104 = 64512 <= 65536).
+  // warpgroup then resizes: softmax 176, epilogue 80, control warps 72
+  // (4*32*72 + 8*32*176 + 4*32*80 = 64512 <= 65536).
 
   if (warp < 4) {
   setmaxnreg_dec<kRegsControl>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // whole warp: lane 0 waits for free slots and issues the record / K / V
-    // copies; in TMA-Q mode lane i issues the Q box of the item's token i
-    // (C = 128 / G <= 16 tokens).  Header and token ids of the next item
-    // are prefetched from the record in global memory.
+    // lane 0 waits for a free K|V slot and issues the record / K / V copies.
+    // Headers are prefetched kBatch items ahead: lane j of the warp holds
+    // the header of item base + j of the current batch and of the next one.
     const int4* grec = p.records + (int64_t)begin * p.rec_stride;
-    const int C = kTileM / p.G;
-    int4 hdr_next = cnt > 0 ? grec[0] : make_int4(0, 0, 0, 0);
-    int tok_next = (cnt > 0 && p.q_tma && lane < C) ? grec[1 + lane].x : 0;
+    int4 hcur = make_int4(0, 0, 0, 0), hnext = make_int4(0, 0, 0, 0);
+    if (lane < kBatch && lane < cnt) hcur = grec[(int64_t)lane * p.rec_stride];
     int issued = 0;
-    for (int li = 0; li < cnt; ++li) {
-      const int ks = li % kKvStages, qs = li % kQStages;
-      const int4 hdr = hdr_next;
-      const int tok = tok_next;
-      if (li + 1 < cnt) {
-        const int4* nr = grec + (int64_t)(li + 1) * p.rec_stride;
-        hdr_next = nr[0];
-        if (p.q_tma && lane < C) tok_next = nr[1 + lane].x;
+    bool ok = true;
+    for (int base = 0; ok && base < cnt; base += kBatch) {
+      if (lane < kBatch && base + kBatch + lane < cnt)
+        hnext = grec[(int64_t)(base + kBatch + lane) * p.rec_stride];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int li = base + j;
+        if (li >= cnt) break;
+        const int4 hdr = make_int4(__shfl_sync(0xffffffffu, hcur.x, j),
+                                   __shfl_sync(0xffffffffu, hcur.y, j), 0, 0);
+        const int ks = li % kKvStages;
+        if (lane == 0) {
+          int w_ok = 1;
+          if (li >= kKvStages)
+            w_ok = bounded_wait(&bars->kv_empty[ks], ((li / kKvStages) - 1) & 1,
+                                abort, kWaitLimitNs);
+          if (w_ok) {
+            const uint32_t rec_bytes = 16u * (1u + (uint32_t)hdr.y);
+            mbar_arrive_expect_tx(&bars->rec_full[ks], rec_bytes);
+            bulk_load(smem + kOffRec + ks * kRecMax,
+                      p.records + (int64_t)(begin + li) * p.rec_stride,
+                      rec_bytes, &bars->rec_full[ks]);
+            mbar_arrive_expect_tx(&bars->kv_full[ks], 2 * kTile);
+            tma_load_2d(smem + kOffK + ks * kTile, &kv_map, &bars->kv_full[ks], 0, hdr.x);
+            tma_load_2d(smem + kOffV + ks * kTile, &kv_map, &bars->kv_full[ks], kD, hdr.x);
+            issued = li + 1;
+          } else if (!*abort) {
+            set_timeout(bars, p.status);
+          }
+          ok = w_ok;
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
       }
-      int ok = 1;
-      if (lane == 0) {
-        if (li >= kKvStages)
-          ok = bounded_wait(&bars->kv_empty[ks], ((li / kKvStages) - 1) & 1,
-                            abort, kWaitLimitNs);
-        if (ok && li >= kQStages)
-          ok = bounded_wait(&bars->q_empty[qs], ((li / kQStages) - 1) & 1,
-                            abort, kWaitLimitNs);
-        if (!ok && !*abort) set_timeout(bars, p.status);
-      }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      if (lane == 0) {
-        const uint32_t rec_bytes = 16u * (1u + (uint32_t)hdr.y);
-        mbar_arrive_expect_tx(&bars->rec_full[ks], rec_bytes);
-        bulk_load(smem + kOffRec + ks * kRecMax,
-                  p.records + (int64_t)(begin + li) * p.rec_stride, rec_bytes,
-                  &bars->rec_full[ks]);
-        mbar_arrive_expect_tx(&bars->kv_full[ks], 2 * kTile);
-        tma_load_2d(smem + kOffK + ks * kTile, &kv_map, &bars->kv_full[ks], 0, hdr.x);
-        tma_load_2d(smem + kOffV + ks * kTile, &kv_map, &bars->kv_full[ks], kD, hdr.x);
-        if (p.q_tma)
-          mbar_arrive_expect_tx(&bars->q_full[qs], (uint32_t)(hdr.y * p.G * 128));
-      }
-      if (p.q_tma) {
-        __syncwarp();
-        if (lane < hdr.y)
-          tma_load_2d(smem + kOffQ + qs * kTile +
-                          ((lane * p.G + row_rotation(li, p.G)) & (kTileM - 1)) * 128,
-                      &q_map, &bars->q_full[qs], 0, tok * p.Hq + hdr.w);
-      }
-      issued = li + 1;
+      hcur = hnext;
     }
     // every copy this warp started must land before the CTA exits
-    if (lane == 0) {
+    if (lane == 0)
       for (int li = issued > kKvStages ? issued - kKvStages : 0; li < issued; ++li) {
         bounded_wait(&bars->rec_full[li % kKvStages], (li / kKvStages) & 1,
                      nullptr, kWaitLimitNs);
         bounded_wait(&bars->kv_full[li % kKvStages], (li / kKvStages) & 1,
                      nullptr, kWaitLimitNs);
       }
-      if (p.q_tma)
-        for (int li = issued > kQStages ? issued - kQStages : 0; li < issued; ++li)
-          bounded_wait(&bars->q_full[li % kQStages], (li / kQStages) & 1,
-                       nullptr, kWaitLimitNs);
-    }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -357,9 +346,71 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------ Q gather
-    // (cp.async mode only) two warps take alternate items; 16-byte chunks
-    // into the swizzled layout, then a proxy fence so the tensor cores see
-    // the rows.
+    if (p.q_tma) {
+      // warp 2: one TMA box of G rows per token, lane i issues token i
+      // (C = 128 / G <= 16).  Token ids and headers are prefetched kBatch
+      // items ahead from the records in global memory: lane i < C holds
+      // token i of each item of the batch, lane j < kBatch the header of
+      // item base + j.
+      if (warp == 2) {
+        const int4* grec = p.records + (int64_t)begin * p.rec_stride;
+        const int C = kTileM / p.G;
+        int tcur[kBatch], tnext[kBatch];
+        int4 hcur = make_int4(0, 0, 0, 0), hnext = make_int4(0, 0, 0, 0);
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+          tcur[j] = (j < cnt && lane < C) ? grec[(int64_t)j * p.rec_stride + 1 + lane].x : 0;
+          tnext[j] = 0;
+        }
+        if (lane < kBatch && lane < cnt) hcur = grec[(int64_t)lane * p.rec_stride];
+        int issued = 0;
+        bool ok = true;
+        for (int base = 0; ok && base < cnt; base += kBatch) {
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j) {
+            const int li = base + kBatch + j;
+            if (li < cnt && lane < C)
+              tnext[j] = grec[(int64_t)li * p.rec_stride + 1 + lane].x;
+          }
+          if (lane < kBatch && base + kBatch + lane < cnt)
+            hnext = grec[(int64_t)(base + kBatch + lane) * p.rec_stride];
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j) {
+            const int li = base + j;
+            if (li >= cnt) break;
+            const int n = __shfl_sync(0xffffffffu, hcur.y, j);
+            const int hq0 = __shfl_sync(0xffffffffu, hcur.w, j);
+            const int qs = li % kQStages;
+            if (lane == 0) {
+              int w_ok = 1;
+              if (li >= kQStages)
+                w_ok = bounded_wait(&bars->q_empty[qs], ((li / kQStages) - 1) & 1,
+                                    abort, kWaitLimitNs);
+              if (w_ok)
+                mbar_arrive_expect_tx(&bars->q_full[qs], (uint32_t)(n * p.G * 128));
+              else if (!*abort)
+                set_timeout(bars, p.status);
+              ok = w_ok;
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (lane < n)
+              tma_load_2d(smem + kOffQ + qs * kTile +
+                              ((lane * p.G + row_rotation(li, p.G)) & (kTileM - 1)) * 128,
+                          &q_map, &bars->q_full[qs], 0, tcur[j] * p.Hq + hq0);
+            issued = li + 1;
+          }
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j) tcur[j] = tnext[j];
+          hcur = hnext;
+        }
+        if (lane == 0)
+          for (int li = issued > kQStages ? issued - kQStages : 0; li < issued; ++li)
+            bounded_wait(&bars->q_full[li % kQStages], (li / kQStages) & 1,
+                         nullptr, kWaitLimitNs);
+        __syncwarp();
+      }
+    }
     if (!p.q_tma) {
       bool ok = true;
       for (int li = warp - 2; li < cnt; li += 2) {

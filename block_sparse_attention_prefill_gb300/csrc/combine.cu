@@ -86,8 +86,9 @@ combine_kernel(const TIn* __restrict__ part_o, const float* __restrict__ part_ls
 }
 
 // The attention path's combine: 16 slots per row, the slot mask of the
-// row's (token, KV head) says which slots hold a partial.  All of a row's
-// loads are issued before any is used.
+// row's (token, KV head) says which slots hold a partial.  A half-warp per
+// row, each lane owning 8 of the 128 columns: one 16-byte load per slot,
+// all of a row's loads issued before any is used.
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 combine16_kernel(const __nv_bfloat16* __restrict__ part_o,
                  const float* __restrict__ part_lse,
@@ -95,47 +96,59 @@ combine16_kernel(const __nv_bfloat16* __restrict__ part_o,
                  int64_t rows, uint16_t* __restrict__ out,
                  float* __restrict__ lse_out) {
   const int lane = threadIdx.x & 31;
-  const int64_t r = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (r >= rows) return;
-  const uint32_t mask = slot_mask[r / group];
-  const __nv_bfloat16* base = part_o + r * (int64_t)kTopK * kD + lane * 4;
-  float v[kTopK][4];
+  const int sub = lane & 15;                 // lane within the half-warp
+  const int64_t r = ((int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5)) * 2 +
+                    (lane >> 4);
+  const bool live = r < rows;
+  const uint32_t mask = live ? slot_mask[r / group] : 0u;
+  const __nv_bfloat16* base = part_o + r * (int64_t)kTopK * kD + sub * 8;
+  uint4 v[kTopK];
 #pragma unroll
   for (int j = 0; j < kTopK; ++j) {
-    if ((mask >> j) & 1u) {
-      load4(base + j * kD, v[j]);
-    } else {
-      v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0.f;
-    }
+    if ((mask >> j) & 1u)
+      v[j] = *reinterpret_cast<const uint4*>(base + j * kD);
+    else
+      v[j] = make_uint4(0u, 0u, 0u, 0u);
   }
+  // lane `sub` of the half-warp holds slot sub's lse
   float l = -INFINITY;
-  if (lane < kTopK && ((mask >> lane) & 1u)) l = part_lse[r * kTopK + lane];
+  if ((mask >> sub) & 1u) l = part_lse[r * kTopK + sub];
   float M = l;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  uint2* dst = reinterpret_cast<uint2*>(out + r * kD + lane * 4);
-  if (M == -INFINITY) {
-    *dst = make_uint2(0u, 0u);
-    if (lse_out && lane == 0) lse_out[r] = -INFINITY;
-    return;
-  }
+  for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   const float wl = (l == -INFINITY) ? 0.f : __expf(l - M);
   float sum = wl;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (!live) return;
+  uint4* dst = reinterpret_cast<uint4*>(out + r * kD + sub * 8);
+  if (M == -INFINITY) {
+    *dst = make_uint4(0u, 0u, 0u, 0u);
+    if (lse_out && sub == 0) lse_out[r] = -INFINITY;
+    return;
+  }
   const float inv = 1.f / sum;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int j = 0; j < kTopK; ++j) {
-    const float wj = __shfl_sync(0xffffffffu, wl, j) * inv;
+    const float wj = __shfl_sync(0xffffffffu, wl, (lane & 16) + j) * inv;
+    const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
-    for (int u = 0; u < 4; ++u) acc[u] = fmaf(wj, v[j][u], acc[u]);
+    for (int u = 0; u < 4; ++u) {
+      const float2 f = __bfloat1622float2(
+          *reinterpret_cast<const __nv_bfloat162*>(&w4[u]));
+      acc[2 * u] = fmaf(wj, f.x, acc[2 * u]);
+      acc[2 * u + 1] = fmaf(wj, f.y, acc[2 * u + 1]);
+    }
   }
-  __nv_bfloat162 a = __floats2bfloat162_rn(acc[0], acc[1]);
-  __nv_bfloat162 b = __floats2bfloat162_rn(acc[2], acc[3]);
-  *dst = make_uint2(*reinterpret_cast<uint32_t*>(&a),
-                    *reinterpret_cast<uint32_t*>(&b));
-  if (lse_out && lane == 0) lse_out[r] = M + __logf(sum);
+  uint32_t o[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * u], acc[2 * u + 1]);
+    o[u] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  *dst = make_uint4(o[0], o[1], o[2], o[3]);
+  if (lse_out && sub == 0) lse_out[r] = M + __logf(sum);
 }
 
 __global__ void __launch_bounds__(1024)
@@ -192,7 +205,8 @@ cudaError_t launch_combine(const void* part_o, int part_dtype,
   if (part_dtype == MSA_DTYPE_BF16) {
     auto po = static_cast<const __nv_bfloat16*>(part_o);
     if (slot_mask && S == kTopK)
-      combine16_kernel<<<grid, kWarpsPerBlock * 32, 0, stream>>>(
+      combine16_kernel<<<(unsigned)ceil_div(rows, 2 * kWarpsPerBlock),
+                         kWarpsPerBlock * 32, 0, stream>>>(
           po, part_lse, slot_mask, group, rows, out, lse);
     else if (slot_mask)
       combine_kernel<__nv_bfloat16, true><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
