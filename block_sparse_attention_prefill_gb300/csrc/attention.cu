@@ -38,6 +38,7 @@
 // n's softmax runs and never wait on one item for the next one's data.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -84,6 +85,7 @@ struct Barriers {
   uint64_t q_full[kQStages];
   uint64_t q_empty[kQStages];
   uint64_t s_full[2];
+  uint64_t s_free[2];
   uint64_t p_full[2];
   uint64_t o_full[2];
   uint64_t o_free[2];
@@ -125,29 +127,42 @@ __device__ __forceinline__ int row_rotation(int li, int G) {
   return (G <= 32 && 32 % G == 0) ? (li & 3) * 32 : 0;
 }
 
-// p = 2^(x * c + off) for 32 score columns, packed to E4M3 in pairs and
-// stored as two 16-byte chunks of the 128-byte-swizzled P row; returns the
-// sum of the (unrounded) probabilities.  kMask: columns past kv_lim are 0.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// p = 2^(x * c + off) for 32 score columns: x * c + off in packed fp32, the
+// power of two in packed f16 (the probabilities are rounded to E4M3
+// afterwards, whose 3-bit mantissa is far coarser), then E4M3 pairs stored
+// as two 16-byte chunks of the 128-byte-swizzled P row.  Returns the sum of
+// the probabilities (f16 partial sums of 16 values, at most 4096 each,
+// added in fp32).  kMask: columns past kv_lim give 0.
 template <bool kMask>
 __device__ __forceinline__ float exp_pack32(const uint32_t (&r)[32], int col0,
                                             int kv_lim, float c, float off,
                                             uint8_t* prow, int row) {
   uint32_t packed[8];
-  float l = 0.f;
+  __half2 acc = __float2half2_rn(0.f);
+  const float2 cc = make_float2(c, c), oo = make_float2(off, off);
 #pragma unroll
   for (int e = 0; e < 32; e += 4) {
-    float pv[4];
+    float x[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const float x = __uint_as_float(r[e + u]);
-      pv[u] = ex2_approx(fmaf(x, c, off));
-      if (kMask && col0 + e + u > kv_lim) pv[u] = 0.f;
-      l += pv[u];
+      x[u] = __uint_as_float(r[e + u]);
+      if (kMask && col0 + e + u > kv_lim) x[u] = -INFINITY;
     }
-    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(pv[0], pv[1]),
-                                                 __NV_SATFINITE, __NV_E4M3);
-    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(pv[2], pv[3]),
-                                                 __NV_SATFINITE, __NV_E4M3);
+    const float2 a = __ffma2_rn(make_float2(x[0], x[1]), cc, oo);
+    const float2 b = __ffma2_rn(make_float2(x[2], x[3]), cc, oo);
+    const __half2 ha = h2exp2(__floats2half2_rn(a.x, a.y));
+    const __half2 hb = h2exp2(__floats2half2_rn(b.x, b.y));
+    acc = __hadd2(acc, __hadd2(ha, hb));
+    const uint32_t lo = __nv_cvt_halfraw2_to_fp8x2(
+        *reinterpret_cast<const __half2_raw*>(&ha), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_halfraw2_to_fp8x2(
+        *reinterpret_cast<const __half2_raw*>(&hb), __NV_SATFINITE, __NV_E4M3);
     packed[e / 4] = lo | (hi << 16);
   }
   const int c0 = col0 / 16, c1 = c0 + 1;
@@ -155,16 +170,23 @@ __device__ __forceinline__ float exp_pack32(const uint32_t (&r)[32], int col0,
       make_uint4(packed[0], packed[1], packed[2], packed[3]);
   *reinterpret_cast<uint4*>(prow + ((c1 ^ (row & 7)) << 4)) =
       make_uint4(packed[4], packed[5], packed[6], packed[7]);
-  return l;
+  const float2 f = __half22float2(acc);
+  return f.x + f.y;
 }
 
 template <bool kMask>
 __device__ __forceinline__ float max32(const uint32_t (&r)[32], int col0,
                                        int kv_lim, float m) {
+  if (!kMask) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 2)
+      m = max3f(m, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+    return m;
+  }
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
     const float x = __uint_as_float(r[e]);
-    if (!kMask || col0 + e <= kv_lim) m = fmaxf(m, x);
+    if (col0 + e <= kv_lim) m = fmaxf(m, x);
   }
   return m;
 }
@@ -198,6 +220,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(&bars->s_full[w], 1);
+      mbar_init(&bars->s_free[w], kSoftmaxThreads);
       mbar_init(&bars->p_full[w], kSoftmaxThreads);
       mbar_init(&bars->o_full[w], 1);
       mbar_init(&bars->o_free[w], kSoftmaxThreads);
@@ -311,12 +334,14 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         mma_commit(&bars->kv_empty[ks]);
       };
       // in-order issue of QK(qk) and PV(pv), each as soon as it is ready;
-      // QK(n) reuses the S tile of item n-2, free once PV(n-2) was issued
+      // QK(n) reuses the S tile of item n-2, free once the softmax warps
+      // have read it into registers (s_free)
       int qk = 0, pv = 0;
       uint64_t idle_since = global_timer_ns();
       while (pv < cnt) {
         bool progressed = false;
-        if (qk < cnt && qk <= pv + 1) {
+        if (qk < cnt &&
+            (qk < 2 || mbar_test(&bars->s_free[qk & 1], ((qk >> 1) - 1) & 1))) {
           if (mbar_test(&bars->kv_full[qk % kKvStages], (qk / kKvStages) & 1) &&
               mbar_test(&bars->q_full[qk % kQStages], (qk / kQStages) & 1)) {
             issue_qk(qk);
@@ -484,15 +509,12 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
-      // the P tile is free once PV of this group's previous item is done
-      if (k > 0 &&
-          !bounded_wait(&bars->o_full[w], (k - 1) & 1, abort, kWaitLimitNs)) {
-        if (lane == 0 && !*abort) set_timeout(bars, p.status);
-        break;
-      }
       tc_fence_after();
       float m2 = -INFINITY, l = 0.f;
-      if (warp_valid) {
+      bool p_free = true;
+      if (!warp_valid) {
+        mbar_arrive(&bars->s_free[w]);
+      } else {
         __syncwarp();
         uint32_t r0[32], r1[32], r2[32], r3[32];
         tmem_ld32(s_tmem + 0, r0);
@@ -500,6 +522,9 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         tmem_ld32(s_tmem + 64, r2);
         tmem_ld32(s_tmem + 96, r3);
         tmem_wait_ld();
+        // S is in registers: the tile can take the next item's scores
+        tc_fence_before();
+        mbar_arrive(&bars->s_free[w]);
         float m = -INFINITY;
         if (need_mask) {
           m = max32<true>(r0, 0, kv_lim, m);
@@ -518,17 +543,26 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         // factor, which cancels.
         const float off = (m2 == -INFINITY) ? 0.f : 8.f - m2;
         const float c = p.score_log2;
-        if (need_mask) {
-          l += exp_pack32<true>(r0, 0, kv_lim, c, off, prow_s, row);
-          l += exp_pack32<true>(r1, 32, kv_lim, c, off, prow_s, row);
-          l += exp_pack32<true>(r2, 64, kv_lim, c, off, prow_s, row);
-          l += exp_pack32<true>(r3, 96, kv_lim, c, off, prow_s, row);
-        } else {
-          l += exp_pack32<false>(r0, 0, kv_lim, c, off, prow_s, row);
-          l += exp_pack32<false>(r1, 32, kv_lim, c, off, prow_s, row);
-          l += exp_pack32<false>(r2, 64, kv_lim, c, off, prow_s, row);
-          l += exp_pack32<false>(r3, 96, kv_lim, c, off, prow_s, row);
+        // the P tile is free once PV of this group's previous item is done
+        if (k > 0)
+          p_free = bounded_wait(&bars->o_full[w], (k - 1) & 1, abort, kWaitLimitNs);
+        if (p_free) {
+          if (need_mask) {
+            l += exp_pack32<true>(r0, 0, kv_lim, c, off, prow_s, row);
+            l += exp_pack32<true>(r1, 32, kv_lim, c, off, prow_s, row);
+            l += exp_pack32<true>(r2, 64, kv_lim, c, off, prow_s, row);
+            l += exp_pack32<true>(r3, 96, kv_lim, c, off, prow_s, row);
+          } else {
+            l += exp_pack32<false>(r0, 0, kv_lim, c, off, prow_s, row);
+            l += exp_pack32<false>(r1, 32, kv_lim, c, off, prow_s, row);
+            l += exp_pack32<false>(r2, 64, kv_lim, c, off, prow_s, row);
+            l += exp_pack32<false>(r3, 96, kv_lim, c, off, prow_s, row);
+          }
         }
+      }
+      if (!p_free) {
+        if (!*abort) set_timeout(bars, p.status);
+        break;
       }
       RowMeta mt;
       mt.prow = prow;
