@@ -511,7 +511,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       }
       tc_fence_after();
       float m2 = -INFINITY, l = 0.f;
-      bool p_free = true;
+      bool p_free = true, waited = false;
       if (!warp_valid) {
         mbar_arrive(&bars->s_free[w]);
       } else {
@@ -546,6 +546,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         // the P tile is free once PV of this group's previous item is done
         if (k > 0)
           p_free = bounded_wait(&bars->o_full[w], (k - 1) & 1, abort, kWaitLimitNs);
+        waited = true;
         if (p_free) {
           if (need_mask) {
             l += exp_pack32<true>(r0, 0, kv_lim, c, off, prow_s, row);
@@ -560,6 +561,11 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
           }
         }
       }
+      // Every thread, with or without rows, waits for PV of item li-2 before
+      // it writes the result ring: that PV needed the epilogue of item li-4,
+      // the last reader of this ring slot, to be done.
+      if (!waited && k > 0)
+        p_free = bounded_wait(&bars->o_full[w], (k - 1) & 1, abort, kWaitLimitNs);
       if (!p_free) {
         if (!*abort) set_timeout(bars, p.status);
         break;
