@@ -177,16 +177,16 @@ __device__ __forceinline__ float exp_pack32(const uint32_t (&r)[32], int col0,
 template <bool kMask>
 __device__ __forceinline__ float max32(const uint32_t (&r)[32], int col0,
                                        int kv_lim, float m) {
-  if (!kMask) {
+  if constexpr (!kMask) {
 #pragma unroll
     for (int e = 0; e < 32; e += 2)
       m = max3f(m, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
-    return m;
-  }
+  } else {
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    const float x = __uint_as_float(r[e]);
-    if (col0 + e <= kv_lim) m = fmaxf(m, x);
+    for (int e = 0; e < 32; ++e) {
+      const float x = __uint_as_float(r[e]);
+      if (col0 + e <= kv_lim) m = fmaxf(m, x);
+    }
   }
   return m;
 }
