@@ -156,8 +156,12 @@ __device__ __forceinline__ float exp_pack32(const uint32_t (&r)[32], int col0,
     }
     const float2 a = __ffma2_rn(make_float2(x[0], x[1]), cc, oo);
     const float2 b = __ffma2_rn(make_float2(x[2], x[3]), cc, oo);
-    const __half2 ha = h2exp2(__floats2half2_rn(a.x, a.y));
-    const __half2 hb = h2exp2(__floats2half2_rn(b.x, b.y));
+    const __half2 ia = __floats2half2_rn(a.x, a.y);
+    const __half2 ib = __floats2half2_rn(b.x, b.y);
+    const uint32_t ea = ex2_f16x2(*reinterpret_cast<const uint32_t*>(&ia));
+    const uint32_t eb = ex2_f16x2(*reinterpret_cast<const uint32_t*>(&ib));
+    const __half2 ha = *reinterpret_cast<const __half2*>(&ea);
+    const __half2 hb = *reinterpret_cast<const __half2*>(&eb);
     acc = __hadd2(acc, __hadd2(ha, hb));
     const uint32_t lo = __nv_cvt_halfraw2_to_fp8x2(
         *reinterpret_cast<const __half2_raw*>(&ha), __NV_SATFINITE, __NV_E4M3);
