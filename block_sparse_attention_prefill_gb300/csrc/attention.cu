@@ -367,6 +367,10 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         } else if (*abort || global_timer_ns() - idle_since > kWaitLimitNs) {
           ok = false;
           break;
+        } else {
+          // nothing ready: yield the issue slots to the softmax warps that
+          // share this SM sub-partition
+          __nanosleep(64);
         }
       }
       if (!ok && !*abort) set_timeout(bars, p.status);
