@@ -54,9 +54,9 @@ constexpr int kTile = 128 * 128;  // one 128 x 128 E4M3 tile, bytes
 constexpr int kThreads = 512;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kTmemCols = 512;
-constexpr int kRegsControl = 72;
+constexpr int kRegsControl = 64;
 constexpr int kRegsSoftmax = 176;
-constexpr int kRegsEpilogue = 80;
+constexpr int kRegsEpilogue = 96;
 static_assert(4 * 32 * kRegsControl + 8 * 32 * kRegsSoftmax +
                   4 * 32 * kRegsEpilogue <= 65536,
               "register split must equal the launch allocation");
@@ -117,14 +117,31 @@ __device__ __forceinline__ void set_timeout(Barriers* bars, uint32_t* status) {
   atomicOr(status, (unsigned)MSA_STATUS_TIMEOUT);
 }
 
-// Rows of item li are placed rot(li) lanes further down the tile (mod 128)
-// so that small items -- a few tokens x G heads, fewer than 32 rows -- land
-// on a different TMEM lane quadrant, and so a different SM sub-partition,
-// from one item to the next.  Only for G dividing 32: then a token's G rows
-// start at a multiple of G and never straddle the end of the tile (a TMA
-// box does not wrap around).
-__device__ __forceinline__ int row_rotation(int li, int G) {
-  return (G <= 32 && 32 % G == 0) ? (li & 3) * 32 : 0;
+// Where the rows (token i, query head g) of an item sit in the 128-row tile.
+// When G divides 32 the tokens are dealt round-robin over the four TMEM lane
+// quadrants (token i -> quadrant i % 4, G consecutive lanes), so that even a
+// small item keeps all four warps of a softmax group -- and all four SM
+// sub-partitions -- busy; otherwise tokens take consecutive rows.  Either
+// way a token's G rows are consecutive and start at a multiple of G, which
+// is what one TMA box of G rows needs.
+__device__ __forceinline__ int tile_row(int i, int g, int G) {
+  return (32 % G == 0) ? 32 * (i & 3) + (i >> 2) * G + g : i * G + g;
+}
+__device__ __forceinline__ void row_token(int q, int ql, int G, int& i, int& g) {
+  if (32 % G == 0) {
+    i = q + 4 * (ql / G);
+    g = ql % G;
+  } else {
+    const int r = 32 * q + ql;
+    i = r / G;
+    g = r % G;
+  }
+}
+// rows of quadrant q that hold queries of an n-token item: [0, result)
+__device__ __forceinline__ int quad_rows(int q, int n, int G) {
+  if (32 % G == 0) return (n > q ? (n - q + 3) >> 2 : 0) * G;
+  const int r = n * G - 32 * q;
+  return r < 0 ? 0 : (r > 32 ? 32 : r);
 }
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
@@ -133,66 +150,57 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   return r;
 }
 
-// p = 2^(x * c + off) for 32 score columns: x * c + off in packed fp32, the
-// power of two in packed f16 (the probabilities are rounded to E4M3
-// afterwards, whose 3-bit mantissa is far coarser), then E4M3 pairs stored
-// as two 16-byte chunks of the 128-byte-swizzled P row.  Returns the sum of
-// the probabilities (f16 partial sums of 16 values, at most 4096 each,
-// added in fp32).  kMask: columns past kv_lim give 0.
+// Row maximum over a thread's 32 columns of one row in a 16x256b fragment
+// (registers 4i + sel, 4i + sel + 1 for column block i), then over the four
+// threads that share the row.  Columns past kv_lim are masked when kMask.
 template <bool kMask>
-__device__ __forceinline__ float exp_pack32(const uint32_t (&r)[32], int col0,
-                                            int kv_lim, float c, float off,
-                                            uint8_t* prow, int row) {
-  uint32_t packed[8];
-  __half2 acc = __float2half2_rn(0.f);
-  const float2 cc = make_float2(c, c), oo = make_float2(off, off);
+__device__ __forceinline__ float frag_row_max(const uint32_t (&v)[64], int sel,
+                                              int tc, int kv_lim) {
+  float m = -INFINITY;
 #pragma unroll
-  for (int e = 0; e < 32; e += 4) {
-    float x[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      x[u] = __uint_as_float(r[e + u]);
-      if (kMask && col0 + e + u > kv_lim) x[u] = -INFINITY;
+  for (int i = 0; i < 16; ++i) {
+    float x0 = __uint_as_float(v[4 * i + sel]);
+    float x1 = __uint_as_float(v[4 * i + sel + 1]);
+    if (kMask) {
+      const int c = 8 * i + 2 * tc;
+      if (c > kv_lim) x0 = -INFINITY;
+      if (c + 1 > kv_lim) x1 = -INFINITY;
     }
-    const float2 a = __ffma2_rn(make_float2(x[0], x[1]), cc, oo);
-    const float2 b = __ffma2_rn(make_float2(x[2], x[3]), cc, oo);
-    const __half2 ia = __floats2half2_rn(a.x, a.y);
-    const __half2 ib = __floats2half2_rn(b.x, b.y);
-    const uint32_t ea = ex2_f16x2(*reinterpret_cast<const uint32_t*>(&ia));
-    const uint32_t eb = ex2_f16x2(*reinterpret_cast<const uint32_t*>(&ib));
-    const __half2 ha = *reinterpret_cast<const __half2*>(&ea);
-    const __half2 hb = *reinterpret_cast<const __half2*>(&eb);
-    acc = __hadd2(acc, __hadd2(ha, hb));
-    const uint32_t lo = __nv_cvt_halfraw2_to_fp8x2(
-        *reinterpret_cast<const __half2_raw*>(&ha), __NV_SATFINITE, __NV_E4M3);
-    const uint32_t hi = __nv_cvt_halfraw2_to_fp8x2(
-        *reinterpret_cast<const __half2_raw*>(&hb), __NV_SATFINITE, __NV_E4M3);
-    packed[e / 4] = lo | (hi << 16);
+    m = max3f(m, x0, x1);
   }
-  const int c0 = col0 / 16, c1 = c0 + 1;
-  *reinterpret_cast<uint4*>(prow + ((c0 ^ (row & 7)) << 4)) =
-      make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  *reinterpret_cast<uint4*>(prow + ((c1 ^ (row & 7)) << 4)) =
-      make_uint4(packed[4], packed[5], packed[6], packed[7]);
-  const float2 f = __half22float2(acc);
-  return f.x + f.y;
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+  return m;
 }
 
+// p = 2^(x * c + off) for the thread's 32 columns of one row, rounded to
+// E4M3 in pairs and stored into the 128-byte-swizzled P row `trow`; returns
+// the row sum over the four threads of the row.
 template <bool kMask>
-__device__ __forceinline__ float max32(const uint32_t (&r)[32], int col0,
-                                       int kv_lim, float m) {
-  if constexpr (!kMask) {
+__device__ __forceinline__ float frag_row_exp(const uint32_t (&v)[64], int sel,
+                                              int tc, int kv_lim, float c,
+                                              float off, uint8_t* sP,
+                                              int trow) {
+  float l = 0.f;
+  uint8_t* prow = sP + trow * 128 + 2 * tc;
 #pragma unroll
-    for (int e = 0; e < 32; e += 2)
-      m = max3f(m, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
-  } else {
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const float x = __uint_as_float(r[e]);
-      if (col0 + e <= kv_lim) m = fmaxf(m, x);
+  for (int i = 0; i < 16; ++i) {
+    float p0 = ex2_approx(fmaf(__uint_as_float(v[4 * i + sel]), c, off));
+    float p1 = ex2_approx(fmaf(__uint_as_float(v[4 * i + sel + 1]), c, off));
+    if (kMask) {
+      const int col = 8 * i + 2 * tc;
+      if (col > kv_lim) p0 = 0.f;
+      if (col + 1 > kv_lim) p1 = 0.f;
     }
+    l += p0 + p1;
+    const uint16_t e = __nv_cvt_float2_to_fp8x2(make_float2(p0, p1),
+                                                __NV_SATFINITE, __NV_E4M3);
+    *reinterpret_cast<uint16_t*>(prow + ((((i >> 1) ^ (trow & 7))) << 4) +
+                                 8 * (i & 1)) = e;
   }
-  return m;
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  return l;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -246,8 +254,8 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
   const uint32_t tmem = bars->tmem_base;
 
   // Launched with 128 registers per thread (512 threads); each role's
-  // warpgroup then resizes: softmax 176, epilogue 80, control warps 72
-  // (4*32*72 + 8*32*176 + 4*32*80 = 64512 <= 65536).
+  // warpgroup then resizes: softmax 176, epilogue 96, control warps 64
+  // (4*32*64 + 8*32*176 + 4*32*96 = 65536).
 
   if (warp < 4) {
   setmaxnreg_dec<kRegsControl>();
@@ -428,8 +436,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             if (lane < n)
-              tma_load_2d(smem + kOffQ + qs * kTile +
-                              ((lane * p.G + row_rotation(li, p.G)) & (kTileM - 1)) * 128,
+              tma_load_2d(smem + kOffQ + qs * kTile + tile_row(lane, 0, p.G) * 128,
                           &q_map, &bars->q_full[qs], 0, tcur[j] * p.Hq + hq0);
             issued = li + 1;
           }
@@ -459,12 +466,11 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         const int4* rec = reinterpret_cast<const int4*>(smem + kOffRec + ks * kRecMax);
         const int4 hdr = rec[0];
         const int rows = hdr.y * p.G;
-        const int rot = row_rotation(li, p.G);
         const uint32_t dst0 = smem_u32(smem + kOffQ + qs * kTile);
         for (int e = lane; e < rows * 8; e += 32) {
           const int lrow = e >> 3, ch = e & 7;
           const int i = lrow / p.G, g = lrow - i * p.G;
-          const int row = (lrow + rot) & (kTileM - 1);
+          const int row = tile_row(i, g, p.G);
           const int t = rec[1 + i].x;
           const uint8_t* src =
               p.q + ((int64_t)t * p.Hq + hdr.w + g) * kD + ch * 16;
@@ -482,12 +488,15 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
   } else if (warp < 12) {
     setmaxnreg_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
+    // Warp `quad` of group w owns TMEM lanes 32*quad .. +31 (tile rows).  It
+    // reads S with the 16x256b shape: thread t holds, per 16-lane half, rows
+    // t/4 and t/4 + 8 at columns 8i + 2(t%4) + {0,1}, so four threads share a
+    // row and a quadrant with 8 query rows costs each thread 32 columns.
     const int w = (warp - 4) >> 2;       // group
     const int quad = warp & 3;           // TMEM lane quadrant
-    const int row = quad * 32 + lane;    // tile row = TMEM lane
-    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t s_tmem = tmem + lane_off + (uint32_t)(w * 256);
-    uint8_t* prow_s = smem + kOffP + w * kTile + row * 128;
+    const int t4 = lane >> 2, tc = lane & 3;
+    const uint32_t s_tmem = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(w * 256);
+    uint8_t* sP = smem + kOffP + w * kTile;
     RowMeta* meta = reinterpret_cast<RowMeta*>(smem + kOffMeta);
     for (int k = 0;; ++k) {
       const int li = 2 * k + w;
@@ -500,90 +509,116 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       }
       const int4* rec = reinterpret_cast<const int4*>(smem + kOffRec + ks * kRecMax);
       const int4 hdr = rec[0];
-      // logical row (token i, head g) held by this lane for this item
-      const int lrow = (row - row_rotation(li, p.G)) & (kTileM - 1);
-      const int i = lrow / p.G, g = lrow - i * p.G;
-      const bool valid = i < hdr.y;
-      const bool warp_valid = __any_sync(0xffffffffu, valid);
-      int64_t prow = -1;
-      int kv_lim = 127;
-      if (valid) {
-        const int4 tok = rec[1 + i];
-        prow = ((int64_t)tok.x * p.Hq + hdr.w + g) * kTopK + tok.z;
-        kv_lim = min(tok.y - hdr.z, 127);
+      const int R = quad_rows(quad, hdr.y, p.G);
+      const int nh = (R + 15) >> 4;      // 16-lane halves holding rows
+      // my rows: r = 2h + b -> quadrant row 16h + t4 + 8b
+      int64_t prow[4];
+      int kvl[4];
+      bool any_mask = false;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int ql = 16 * (r >> 1) + t4 + 8 * (r & 1);
+        prow[r] = -1;
+        kvl[r] = 127;
+        if (ql < R) {
+          int i, g;
+          row_token(quad, ql, p.G, i, g);
+          const int4 tok = rec[1 + i];
+          prow[r] = ((int64_t)tok.x * p.Hq + hdr.w + g) * kTopK + tok.z;
+          kvl[r] = min(tok.y - hdr.z, 127);
+          any_mask |= kvl[r] < 127;
+        }
       }
-      const bool need_mask = __any_sync(0xffffffffu, valid && kv_lim < 127);
+      const bool need_mask = __any_sync(0xffffffffu, any_mask);
       if (!bounded_wait(&bars->s_full[w], k & 1, abort, kWaitLimitNs)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
       tc_fence_after();
-      float m2 = -INFINITY, l = 0.f;
-      bool p_free = true, waited = false;
-      if (!warp_valid) {
+      const float c = p.score_log2;
+      float m2[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      float l[4] = {0.f, 0.f, 0.f, 0.f};
+      bool p_free = true;
+      if (nh == 0) {
         mbar_arrive(&bars->s_free[w]);
       } else {
         __syncwarp();
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        tmem_ld32(s_tmem + 0, r0);
-        tmem_ld32(s_tmem + 32, r1);
-        tmem_ld32(s_tmem + 64, r2);
-        tmem_ld32(s_tmem + 96, r3);
+        uint32_t v0[64], v1[64];
+        tmem_ld_16x256b_x16(s_tmem, v0);
+        if (nh > 1) tmem_ld_16x256b_x16(s_tmem + (16u << 16), v1);
         tmem_wait_ld();
         // S is in registers: the tile can take the next item's scores
         tc_fence_before();
         mbar_arrive(&bars->s_free[w]);
-        float m = -INFINITY;
+        float m[4];
         if (need_mask) {
-          m = max32<true>(r0, 0, kv_lim, m);
-          m = max32<true>(r1, 32, kv_lim, m);
-          m = max32<true>(r2, 64, kv_lim, m);
-          m = max32<true>(r3, 96, kv_lim, m);
+          m[0] = frag_row_max<true>(v0, 0, tc, kvl[0]);
+          m[1] = frag_row_max<true>(v0, 2, tc, kvl[1]);
+          if (nh > 1) {
+            m[2] = frag_row_max<true>(v1, 0, tc, kvl[2]);
+            m[3] = frag_row_max<true>(v1, 2, tc, kvl[3]);
+          }
         } else {
-          m = max32<false>(r0, 0, kv_lim, m);
-          m = max32<false>(r1, 32, kv_lim, m);
-          m = max32<false>(r2, 64, kv_lim, m);
-          m = max32<false>(r3, 96, kv_lim, m);
+          m[0] = frag_row_max<false>(v0, 0, tc, 127);
+          m[1] = frag_row_max<false>(v0, 2, tc, 127);
+          if (nh > 1) {
+            m[2] = frag_row_max<false>(v1, 0, tc, 127);
+            m[3] = frag_row_max<false>(v1, 2, tc, 127);
+          }
         }
-        m2 = m * p.score_log2;
         // p = 2^(x * c - m2 + 8): probabilities scaled by 256 so that small
         // ones stay out of E4M3's subnormal range; l and O carry the same
         // factor, which cancels.
-        const float off = (m2 == -INFINITY) ? 0.f : 8.f - m2;
-        const float c = p.score_log2;
+        float off[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          m2[r] = (r < 2 * nh) ? m[r] * c : -INFINITY;
+          off[r] = (m2[r] == -INFINITY) ? 0.f : 8.f - m2[r];
+        }
         // the P tile is free once PV of this group's previous item is done
         if (k > 0)
           p_free = bounded_wait(&bars->o_full[w], (k - 1) & 1, abort, kWaitLimitNs);
-        waited = true;
         if (p_free) {
+          const int row0 = 32 * quad + t4;
           if (need_mask) {
-            l += exp_pack32<true>(r0, 0, kv_lim, c, off, prow_s, row);
-            l += exp_pack32<true>(r1, 32, kv_lim, c, off, prow_s, row);
-            l += exp_pack32<true>(r2, 64, kv_lim, c, off, prow_s, row);
-            l += exp_pack32<true>(r3, 96, kv_lim, c, off, prow_s, row);
+            l[0] = frag_row_exp<true>(v0, 0, tc, kvl[0], c, off[0], sP, row0);
+            if (R > 8) l[1] = frag_row_exp<true>(v0, 2, tc, kvl[1], c, off[1], sP, row0 + 8);
+            if (nh > 1) {
+              l[2] = frag_row_exp<true>(v1, 0, tc, kvl[2], c, off[2], sP, row0 + 16);
+              if (R > 24) l[3] = frag_row_exp<true>(v1, 2, tc, kvl[3], c, off[3], sP, row0 + 24);
+            }
           } else {
-            l += exp_pack32<false>(r0, 0, kv_lim, c, off, prow_s, row);
-            l += exp_pack32<false>(r1, 32, kv_lim, c, off, prow_s, row);
-            l += exp_pack32<false>(r2, 64, kv_lim, c, off, prow_s, row);
-            l += exp_pack32<false>(r3, 96, kv_lim, c, off, prow_s, row);
+            l[0] = frag_row_exp<false>(v0, 0, tc, 127, c, off[0], sP, row0);
+            if (R > 8) l[1] = frag_row_exp<false>(v0, 2, tc, 127, c, off[1], sP, row0 + 8);
+            if (nh > 1) {
+              l[2] = frag_row_exp<false>(v1, 0, tc, 127, c, off[2], sP, row0 + 16);
+              if (R > 24) l[3] = frag_row_exp<false>(v1, 2, tc, 127, c, off[3], sP, row0 + 24);
+            }
           }
         }
       }
       // Every thread, with or without rows, waits for PV of item li-2 before
       // it writes the result ring: that PV needed the epilogue of item li-4,
       // the last reader of this ring slot, to be done.
-      if (!waited && k > 0)
+      if (nh == 0 && k > 0)
         p_free = bounded_wait(&bars->o_full[w], (k - 1) & 1, abort, kWaitLimitNs);
       if (!p_free) {
         if (!*abort) set_timeout(bars, p.status);
         break;
       }
-      RowMeta mt;
-      mt.prow = prow;
-      mt.inv = l > 0.f ? p.v_scale / l : 0.f;
-      mt.lse = l > 0.f ? (m2 + __log2f(l) - 8.f) * 0.69314718055994530942f
+      if (tc == 0) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          RowMeta mt;
+          mt.prow = prow[r];
+          mt.inv = l[r] > 0.f ? p.v_scale / l[r] : 0.f;
+          mt.lse = l[r] > 0.f
+                       ? (m2[r] + __log2f(l[r]) - 8.f) * 0.69314718055994530942f
                        : -INFINITY;
-      meta[(li % kMetaSlots) * kTileM + row] = mt;
+          meta[(li % kMetaSlots) * kTileM + 32 * quad + 16 * (r >> 1) + t4 +
+               8 * (r & 1)] = mt;
+        }
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->p_full[w]);
@@ -592,9 +627,10 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
   } else {
     setmaxnreg_dec<kRegsEpilogue>();
     // ------------------------------------------------------------ epilogue
+    // Same 16x256b fragments as the softmax: thread t writes columns
+    // 8i + 2(t%4) + {0,1} of rows t/4 (+8, +16, +24) of its quadrant.
     const int quad = warp & 3;
-    const int row = quad * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const int t4 = lane >> 2, tc = lane & 3;
     const RowMeta* meta = reinterpret_cast<const RowMeta*>(smem + kOffMeta);
     for (int li = 0; li < cnt; ++li) {
       const int w = li & 1, k = li >> 1;
@@ -603,44 +639,42 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
-      const RowMeta mt = meta[(li % kMetaSlots) * kTileM + row];
-      const bool valid = mt.prow >= 0;
-      const bool warp_valid = __any_sync(0xffffffffu, valid);
+      RowMeta mt[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        mt[r] = meta[(li % kMetaSlots) * kTileM + 32 * quad + 16 * (r >> 1) +
+                     t4 + 8 * (r & 1)];
+      const bool h0 = __any_sync(0xffffffffu, mt[0].prow >= 0 || mt[1].prow >= 0);
+      const bool h1 = __any_sync(0xffffffffu, mt[2].prow >= 0 || mt[3].prow >= 0);
       if (!bounded_wait(&bars->o_full[w], k & 1, abort, kWaitLimitNs)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
       tc_fence_after();
-      if (warp_valid) {
-        const uint32_t o_tmem = tmem + lane_off + (uint32_t)(w * 256 + 128);
-        uint16_t* dst = p.part_o + mt.prow * (int64_t)kD;
+      const uint32_t o_tmem =
+          tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(w * 256 + 128);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t ra[32], rb[32];
-          __syncwarp();
-          tmem_ld32(o_tmem + half * 64, ra);
-          tmem_ld32(o_tmem + half * 64 + 32, rb);
-          tmem_wait_ld();
-          if (valid) {
-            uint32_t o[32];
+      for (int h = 0; h < 2; ++h) {
+        if (!(h == 0 ? h0 : h1)) continue;
+        uint32_t v[64];
+        __syncwarp();
+        tmem_ld_16x256b_x16(o_tmem + ((uint32_t)(16 * h) << 16), v);
+        tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              __nv_bfloat162 a2 = __floats2bfloat162_rn(
-                  __uint_as_float(ra[2 * e]) * mt.inv,
-                  __uint_as_float(ra[2 * e + 1]) * mt.inv);
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(
-                  __uint_as_float(rb[2 * e]) * mt.inv,
-                  __uint_as_float(rb[2 * e + 1]) * mt.inv);
-              o[e] = *reinterpret_cast<uint32_t*>(&a2);
-              o[16 + e] = *reinterpret_cast<uint32_t*>(&b2);
-            }
-            uint4* d4 = reinterpret_cast<uint4*>(dst + half * 64);
+        for (int b = 0; b < 2; ++b) {
+          const RowMeta& m = mt[2 * h + b];
+          if (m.prow < 0) continue;
+          uint32_t* dst = reinterpret_cast<uint32_t*>(
+              p.part_o + m.prow * (int64_t)kD + 2 * tc);
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              d4[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+          for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(
+                __uint_as_float(v[4 * i + 2 * b]) * m.inv,
+                __uint_as_float(v[4 * i + 2 * b + 1]) * m.inv);
+            dst[4 * i] = *reinterpret_cast<uint32_t*>(&h2);
           }
+          if (tc == 0) p.part_lse[m.prow] = m.lse;
         }
-        if (valid) p.part_lse[mt.prow] = mt.lse;
       }
       tc_fence_before();
       mbar_arrive(&bars->o_free[w]);
