@@ -38,7 +38,6 @@
 // n's softmax runs and never wait on one item for the next one's data.
 #include <cuda.h>
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -49,14 +48,13 @@ namespace {
 
 constexpr int kKvStages = 4;
 constexpr int kQStages = 3;
-constexpr int kBatch = 8;  // items whose headers / token ids are prefetched
 constexpr int kTile = 128 * 128;  // one 128 x 128 E4M3 tile, bytes
 constexpr int kThreads = 512;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kTmemCols = 512;
-constexpr int kRegsControl = 64;
+constexpr int kRegsControl = 48;
 constexpr int kRegsSoftmax = 176;
-constexpr int kRegsEpilogue = 96;
+constexpr int kRegsEpilogue = 104;
 static_assert(4 * 32 * kRegsControl + 8 * 32 * kRegsSoftmax +
                   4 * 32 * kRegsEpilogue <= 65536,
               "register split must equal the launch allocation");
@@ -85,7 +83,6 @@ struct Barriers {
   uint64_t q_full[kQStages];
   uint64_t q_empty[kQStages];
   uint64_t s_full[2];
-  uint64_t s_free[2];
   uint64_t p_full[2];
   uint64_t o_full[2];
   uint64_t o_free[2];
@@ -117,90 +114,58 @@ __device__ __forceinline__ void set_timeout(Barriers* bars, uint32_t* status) {
   atomicOr(status, (unsigned)MSA_STATUS_TIMEOUT);
 }
 
-// Where the rows (token i, query head g) of an item sit in the 128-row tile.
-// When G divides 32 the tokens are dealt round-robin over the four TMEM lane
-// quadrants (token i -> quadrant i % 4, G consecutive lanes), so that even a
-// small item keeps all four warps of a softmax group -- and all four SM
-// sub-partitions -- busy; otherwise tokens take consecutive rows.  Either
-// way a token's G rows are consecutive and start at a multiple of G, which
-// is what one TMA box of G rows needs.
-__device__ __forceinline__ int tile_row(int i, int g, int G) {
-  return (32 % G == 0) ? 32 * (i & 3) + (i >> 2) * G + g : i * G + g;
-}
-__device__ __forceinline__ void row_token(int q, int ql, int G, int& i, int& g) {
-  if (32 % G == 0) {
-    i = q + 4 * (ql / G);
-    g = ql % G;
-  } else {
-    const int r = 32 * q + ql;
-    i = r / G;
-    g = r % G;
-  }
-}
-// rows of quadrant q that hold queries of an n-token item: [0, result)
-__device__ __forceinline__ int quad_rows(int q, int n, int G) {
-  if (32 % G == 0) return (n > q ? (n - q + 3) >> 2 : 0) * G;
-  const int r = n * G - 32 * q;
-  return r < 0 ? 0 : (r > 32 ? 32 : r);
+// Rows of item li are placed rot(li) lanes further down the tile (mod 128)
+// so that small items -- a few tokens x G heads, fewer than 32 rows -- land
+// on a different TMEM lane quadrant, and so a different SM sub-partition,
+// from one item to the next.  Only for G dividing 32: then a token's G rows
+// start at a multiple of G and never straddle the end of the tile (a TMA
+// box does not wrap around).
+__device__ __forceinline__ int row_rotation(int li, int G) {
+  return (G <= 32 && 32 % G == 0) ? (li & 3) * 32 : 0;
 }
 
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
-// Row maximum over a thread's 32 columns of one row in a 16x256b fragment
-// (registers 4i + sel, 4i + sel + 1 for column block i), then over the four
-// threads that share the row.  Columns past kv_lim are masked when kMask.
+// p = 2^(x * c + off) for 32 score columns, packed to E4M3 in pairs and
+// stored as two 16-byte chunks of the 128-byte-swizzled P row; returns the
+// sum of the (unrounded) probabilities.  kMask: columns past kv_lim are 0.
 template <bool kMask>
-__device__ __forceinline__ float frag_row_max(const uint32_t (&v)[64], int sel,
-                                              int tc, int kv_lim) {
-  float m = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    float x0 = __uint_as_float(v[4 * i + sel]);
-    float x1 = __uint_as_float(v[4 * i + sel + 1]);
-    if (kMask) {
-      const int c = 8 * i + 2 * tc;
-      if (c > kv_lim) x0 = -INFINITY;
-      if (c + 1 > kv_lim) x1 = -INFINITY;
-    }
-    m = max3f(m, x0, x1);
-  }
-  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-  return m;
-}
-
-// p = 2^(x * c + off) for the thread's 32 columns of one row, rounded to
-// E4M3 in pairs and stored into the 128-byte-swizzled P row `trow`; returns
-// the row sum over the four threads of the row.
-template <bool kMask>
-__device__ __forceinline__ float frag_row_exp(const uint32_t (&v)[64], int sel,
-                                              int tc, int kv_lim, float c,
-                                              float off, uint8_t* sP,
-                                              int trow) {
+__device__ __forceinline__ float exp_pack32(const uint32_t (&r)[32], int col0,
+                                            int kv_lim, float c, float off,
+                                            uint8_t* prow, int row) {
+  uint32_t packed[8];
   float l = 0.f;
-  uint8_t* prow = sP + trow * 128 + 2 * tc;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    float p0 = ex2_approx(fmaf(__uint_as_float(v[4 * i + sel]), c, off));
-    float p1 = ex2_approx(fmaf(__uint_as_float(v[4 * i + sel + 1]), c, off));
-    if (kMask) {
-      const int col = 8 * i + 2 * tc;
-      if (col > kv_lim) p0 = 0.f;
-      if (col + 1 > kv_lim) p1 = 0.f;
+  for (int e = 0; e < 32; e += 4) {
+    float pv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float x = __uint_as_float(r[e + u]);
+      pv[u] = ex2_approx(fmaf(x, c, off));
+      if (kMask && col0 + e + u > kv_lim) pv[u] = 0.f;
+      l += pv[u];
     }
-    l += p0 + p1;
-    const uint16_t e = __nv_cvt_float2_to_fp8x2(make_float2(p0, p1),
-                                                __NV_SATFINITE, __NV_E4M3);
-    *reinterpret_cast<uint16_t*>(prow + ((((i >> 1) ^ (trow & 7))) << 4) +
-                                 8 * (i & 1)) = e;
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(pv[0], pv[1]),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(pv[2], pv[3]),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    packed[e / 4] = lo | (hi << 16);
   }
-  l += __shfl_xor_sync(0xffffffffu, l, 1);
-  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  const int c0 = col0 / 16, c1 = c0 + 1;
+  *reinterpret_cast<uint4*>(prow + ((c0 ^ (row & 7)) << 4)) =
+      make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  *reinterpret_cast<uint4*>(prow + ((c1 ^ (row & 7)) << 4)) =
+      make_uint4(packed[4], packed[5], packed[6], packed[7]);
   return l;
+}
+
+template <bool kMask>
+__device__ __forceinline__ float max32(const uint32_t (&r)[32], int col0,
+                                       int kv_lim, float m) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const float x = __uint_as_float(r[e]);
+    if (!kMask || col0 + e <= kv_lim) m = fmaxf(m, x);
+  }
+  return m;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -232,7 +197,6 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(&bars->s_full[w], 1);
-      mbar_init(&bars->s_free[w], kSoftmaxThreads);
       mbar_init(&bars->p_full[w], kSoftmaxThreads);
       mbar_init(&bars->o_full[w], 1);
       mbar_init(&bars->o_free[w], kSoftmaxThreads);
@@ -254,64 +218,76 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
   const uint32_t tmem = bars->tmem_base;
 
   // Launched with 128 registers per thread (512 threads); each role's
-  // warpgroup then resizes: softmax 176, epilogue 96, control warps 64
-  // (4*32*64 + 8*32*176 + 4*32*96 = 65536).
+  // warpgroup then resizes: softmax 176, epilogue 104, control warps 48
+  // (4*32*48 + 8*32*176 + 4*32*104 = 64512 <= 65536).
 
   if (warp < 4) {
   setmaxnreg_dec<kRegsControl>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // lane 0 waits for a free K|V slot and issues the record / K / V copies.
-    // Headers are prefetched kBatch items ahead: lane j of the warp holds
-    // the header of item base + j of the current batch and of the next one.
+    // whole warp: lane 0 waits for free slots and issues the record / K / V
+    // copies; in TMA-Q mode lane i issues the Q box of the item's token i
+    // (C = 128 / G <= 16 tokens).  Header and token ids of the next item
+    // are prefetched from the record in global memory.
     const int4* grec = p.records + (int64_t)begin * p.rec_stride;
-    int4 hcur = make_int4(0, 0, 0, 0), hnext = make_int4(0, 0, 0, 0);
-    if (lane < kBatch && lane < cnt) hcur = grec[(int64_t)lane * p.rec_stride];
+    const int C = kTileM / p.G;
+    int4 hdr_next = cnt > 0 ? grec[0] : make_int4(0, 0, 0, 0);
+    int tok_next = (cnt > 0 && p.q_tma && lane < C) ? grec[1 + lane].x : 0;
     int issued = 0;
-    bool ok = true;
-    for (int base = 0; ok && base < cnt; base += kBatch) {
-      if (lane < kBatch && base + kBatch + lane < cnt)
-        hnext = grec[(int64_t)(base + kBatch + lane) * p.rec_stride];
-#pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        const int li = base + j;
-        if (li >= cnt) break;
-        const int4 hdr = make_int4(__shfl_sync(0xffffffffu, hcur.x, j),
-                                   __shfl_sync(0xffffffffu, hcur.y, j), 0, 0);
-        const int ks = li % kKvStages;
-        if (lane == 0) {
-          int w_ok = 1;
-          if (li >= kKvStages)
-            w_ok = bounded_wait(&bars->kv_empty[ks], ((li / kKvStages) - 1) & 1,
-                                abort, kWaitLimitNs);
-          if (w_ok) {
-            const uint32_t rec_bytes = 16u * (1u + (uint32_t)hdr.y);
-            mbar_arrive_expect_tx(&bars->rec_full[ks], rec_bytes);
-            bulk_load(smem + kOffRec + ks * kRecMax,
-                      p.records + (int64_t)(begin + li) * p.rec_stride,
-                      rec_bytes, &bars->rec_full[ks]);
-            mbar_arrive_expect_tx(&bars->kv_full[ks], 2 * kTile);
-            tma_load_2d(smem + kOffK + ks * kTile, &kv_map, &bars->kv_full[ks], 0, hdr.x);
-            tma_load_2d(smem + kOffV + ks * kTile, &kv_map, &bars->kv_full[ks], kD, hdr.x);
-            issued = li + 1;
-          } else if (!*abort) {
-            set_timeout(bars, p.status);
-          }
-          ok = w_ok;
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
+    for (int li = 0; li < cnt; ++li) {
+      const int ks = li % kKvStages, qs = li % kQStages;
+      const int4 hdr = hdr_next;
+      const int tok = tok_next;
+      if (li + 1 < cnt) {
+        const int4* nr = grec + (int64_t)(li + 1) * p.rec_stride;
+        hdr_next = nr[0];
+        if (p.q_tma && lane < C) tok_next = nr[1 + lane].x;
       }
-      hcur = hnext;
+      int ok = 1;
+      if (lane == 0) {
+        if (li >= kKvStages)
+          ok = bounded_wait(&bars->kv_empty[ks], ((li / kKvStages) - 1) & 1,
+                            abort, kWaitLimitNs);
+        if (ok && li >= kQStages)
+          ok = bounded_wait(&bars->q_empty[qs], ((li / kQStages) - 1) & 1,
+                            abort, kWaitLimitNs);
+        if (!ok && !*abort) set_timeout(bars, p.status);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (lane == 0) {
+        const uint32_t rec_bytes = 16u * (1u + (uint32_t)hdr.y);
+        mbar_arrive_expect_tx(&bars->rec_full[ks], rec_bytes);
+        bulk_load(smem + kOffRec + ks * kRecMax,
+                  p.records + (int64_t)(begin + li) * p.rec_stride, rec_bytes,
+                  &bars->rec_full[ks]);
+        mbar_arrive_expect_tx(&bars->kv_full[ks], 2 * kTile);
+        tma_load_2d(smem + kOffK + ks * kTile, &kv_map, &bars->kv_full[ks], 0, hdr.x);
+        tma_load_2d(smem + kOffV + ks * kTile, &kv_map, &bars->kv_full[ks], kD, hdr.x);
+        if (p.q_tma)
+          mbar_arrive_expect_tx(&bars->q_full[qs], (uint32_t)(hdr.y * p.G * 128));
+      }
+      if (p.q_tma) {
+        __syncwarp();
+        if (lane < hdr.y)
+          tma_load_2d(smem + kOffQ + qs * kTile +
+                          ((lane * p.G + row_rotation(li, p.G)) & (kTileM - 1)) * 128,
+                      &q_map, &bars->q_full[qs], 0, tok * p.Hq + hdr.w);
+      }
+      issued = li + 1;
     }
     // every copy this warp started must land before the CTA exits
-    if (lane == 0)
+    if (lane == 0) {
       for (int li = issued > kKvStages ? issued - kKvStages : 0; li < issued; ++li) {
         bounded_wait(&bars->rec_full[li % kKvStages], (li / kKvStages) & 1,
                      nullptr, kWaitLimitNs);
         bounded_wait(&bars->kv_full[li % kKvStages], (li / kKvStages) & 1,
                      nullptr, kWaitLimitNs);
       }
+      if (p.q_tma)
+        for (int li = issued > kQStages ? issued - kQStages : 0; li < issued; ++li)
+          bounded_wait(&bars->q_full[li % kQStages], (li / kQStages) & 1,
+                       nullptr, kWaitLimitNs);
+    }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -346,14 +322,12 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         mma_commit(&bars->kv_empty[ks]);
       };
       // in-order issue of QK(qk) and PV(pv), each as soon as it is ready;
-      // QK(n) reuses the S tile of item n-2, free once the softmax warps
-      // have read it into registers (s_free)
+      // QK(n) reuses the S tile of item n-2, free once PV(n-2) was issued
       int qk = 0, pv = 0;
       uint64_t idle_since = global_timer_ns();
       while (pv < cnt) {
         bool progressed = false;
-        if (qk < cnt &&
-            (qk < 2 || mbar_test(&bars->s_free[qk & 1], ((qk >> 1) - 1) & 1))) {
+        if (qk < cnt && qk <= pv + 1) {
           if (mbar_test(&bars->kv_full[qk % kKvStages], (qk / kKvStages) & 1) &&
               mbar_test(&bars->q_full[qk % kQStages], (qk / kQStages) & 1)) {
             issue_qk(qk);
@@ -375,10 +349,6 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         } else if (*abort || global_timer_ns() - idle_since > kWaitLimitNs) {
           ok = false;
           break;
-        } else {
-          // nothing ready: yield the issue slots to the softmax warps that
-          // share this SM sub-partition
-          __nanosleep(64);
         }
       }
       if (!ok && !*abort) set_timeout(bars, p.status);
@@ -387,70 +357,9 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------ Q gather
-    if (p.q_tma) {
-      // warp 2: one TMA box of G rows per token, lane i issues token i
-      // (C = 128 / G <= 16).  Token ids and headers are prefetched kBatch
-      // items ahead from the records in global memory: lane i < C holds
-      // token i of each item of the batch, lane j < kBatch the header of
-      // item base + j.
-      if (warp == 2) {
-        const int4* grec = p.records + (int64_t)begin * p.rec_stride;
-        const int C = kTileM / p.G;
-        int tcur[kBatch], tnext[kBatch];
-        int4 hcur = make_int4(0, 0, 0, 0), hnext = make_int4(0, 0, 0, 0);
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-          tcur[j] = (j < cnt && lane < C) ? grec[(int64_t)j * p.rec_stride + 1 + lane].x : 0;
-          tnext[j] = 0;
-        }
-        if (lane < kBatch && lane < cnt) hcur = grec[(int64_t)lane * p.rec_stride];
-        int issued = 0;
-        bool ok = true;
-        for (int base = 0; ok && base < cnt; base += kBatch) {
-#pragma unroll
-          for (int j = 0; j < kBatch; ++j) {
-            const int li = base + kBatch + j;
-            if (li < cnt && lane < C)
-              tnext[j] = grec[(int64_t)li * p.rec_stride + 1 + lane].x;
-          }
-          if (lane < kBatch && base + kBatch + lane < cnt)
-            hnext = grec[(int64_t)(base + kBatch + lane) * p.rec_stride];
-#pragma unroll
-          for (int j = 0; j < kBatch; ++j) {
-            const int li = base + j;
-            if (li >= cnt) break;
-            const int n = __shfl_sync(0xffffffffu, hcur.y, j);
-            const int hq0 = __shfl_sync(0xffffffffu, hcur.w, j);
-            const int qs = li % kQStages;
-            if (lane == 0) {
-              int w_ok = 1;
-              if (li >= kQStages)
-                w_ok = bounded_wait(&bars->q_empty[qs], ((li / kQStages) - 1) & 1,
-                                    abort, kWaitLimitNs);
-              if (w_ok)
-                mbar_arrive_expect_tx(&bars->q_full[qs], (uint32_t)(n * p.G * 128));
-              else if (!*abort)
-                set_timeout(bars, p.status);
-              ok = w_ok;
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            if (lane < n)
-              tma_load_2d(smem + kOffQ + qs * kTile + tile_row(lane, 0, p.G) * 128,
-                          &q_map, &bars->q_full[qs], 0, tcur[j] * p.Hq + hq0);
-            issued = li + 1;
-          }
-#pragma unroll
-          for (int j = 0; j < kBatch; ++j) tcur[j] = tnext[j];
-          hcur = hnext;
-        }
-        if (lane == 0)
-          for (int li = issued > kQStages ? issued - kQStages : 0; li < issued; ++li)
-            bounded_wait(&bars->q_full[li % kQStages], (li / kQStages) & 1,
-                         nullptr, kWaitLimitNs);
-        __syncwarp();
-      }
-    }
+    // (cp.async mode only) two warps take alternate items; 16-byte chunks
+    // into the swizzled layout, then a proxy fence so the tensor cores see
+    // the rows.
     if (!p.q_tma) {
       bool ok = true;
       for (int li = warp - 2; li < cnt; li += 2) {
@@ -466,11 +375,12 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         const int4* rec = reinterpret_cast<const int4*>(smem + kOffRec + ks * kRecMax);
         const int4 hdr = rec[0];
         const int rows = hdr.y * p.G;
+        const int rot = row_rotation(li, p.G);
         const uint32_t dst0 = smem_u32(smem + kOffQ + qs * kTile);
         for (int e = lane; e < rows * 8; e += 32) {
           const int lrow = e >> 3, ch = e & 7;
           const int i = lrow / p.G, g = lrow - i * p.G;
-          const int row = tile_row(i, g, p.G);
+          const int row = (lrow + rot) & (kTileM - 1);
           const int t = rec[1 + i].x;
           const uint8_t* src =
               p.q + ((int64_t)t * p.Hq + hdr.w + g) * kD + ch * 16;
@@ -488,15 +398,12 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
   } else if (warp < 12) {
     setmaxnreg_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
-    // Warp `quad` of group w owns TMEM lanes 32*quad .. +31 (tile rows).  It
-    // reads S with the 16x256b shape: thread t holds, per 16-lane half, rows
-    // t/4 and t/4 + 8 at columns 8i + 2(t%4) + {0,1}, so four threads share a
-    // row and a quadrant with 8 query rows costs each thread 32 columns.
     const int w = (warp - 4) >> 2;       // group
     const int quad = warp & 3;           // TMEM lane quadrant
-    const int t4 = lane >> 2, tc = lane & 3;
-    const uint32_t s_tmem = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(w * 256);
-    uint8_t* sP = smem + kOffP + w * kTile;
+    const int row = quad * 32 + lane;    // tile row = TMEM lane
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t s_tmem = tmem + lane_off + (uint32_t)(w * 256);
+    uint8_t* prow_s = smem + kOffP + w * kTile + row * 128;
     RowMeta* meta = reinterpret_cast<RowMeta*>(smem + kOffMeta);
     for (int k = 0;; ++k) {
       const int li = 2 * k + w;
@@ -509,116 +416,75 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       }
       const int4* rec = reinterpret_cast<const int4*>(smem + kOffRec + ks * kRecMax);
       const int4 hdr = rec[0];
-      const int R = quad_rows(quad, hdr.y, p.G);
-      const int nh = (R + 15) >> 4;      // 16-lane halves holding rows
-      // my rows: r = 2h + b -> quadrant row 16h + t4 + 8b
-      int64_t prow[4];
-      int kvl[4];
-      bool any_mask = false;
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int ql = 16 * (r >> 1) + t4 + 8 * (r & 1);
-        prow[r] = -1;
-        kvl[r] = 127;
-        if (ql < R) {
-          int i, g;
-          row_token(quad, ql, p.G, i, g);
-          const int4 tok = rec[1 + i];
-          prow[r] = ((int64_t)tok.x * p.Hq + hdr.w + g) * kTopK + tok.z;
-          kvl[r] = min(tok.y - hdr.z, 127);
-          any_mask |= kvl[r] < 127;
-        }
+      // logical row (token i, head g) held by this lane for this item
+      const int lrow = (row - row_rotation(li, p.G)) & (kTileM - 1);
+      const int i = lrow / p.G, g = lrow - i * p.G;
+      const bool valid = i < hdr.y;
+      const bool warp_valid = __any_sync(0xffffffffu, valid);
+      int64_t prow = -1;
+      int kv_lim = 127;
+      if (valid) {
+        const int4 tok = rec[1 + i];
+        prow = ((int64_t)tok.x * p.Hq + hdr.w + g) * kTopK + tok.z;
+        kv_lim = min(tok.y - hdr.z, 127);
       }
-      const bool need_mask = __any_sync(0xffffffffu, any_mask);
+      const bool need_mask = __any_sync(0xffffffffu, valid && kv_lim < 127);
       if (!bounded_wait(&bars->s_full[w], k & 1, abort, kWaitLimitNs)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
+      // the P tile is free once PV of this group's previous item is done
+      if (k > 0 &&
+          !bounded_wait(&bars->o_full[w], (k - 1) & 1, abort, kWaitLimitNs)) {
+        if (lane == 0 && !*abort) set_timeout(bars, p.status);
+        break;
+      }
       tc_fence_after();
-      const float c = p.score_log2;
-      float m2[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      float l[4] = {0.f, 0.f, 0.f, 0.f};
-      bool p_free = true;
-      if (nh == 0) {
-        mbar_arrive(&bars->s_free[w]);
-      } else {
+      float m2 = -INFINITY, l = 0.f;
+      if (warp_valid) {
         __syncwarp();
-        uint32_t v0[64], v1[64];
-        tmem_ld_16x256b_x16(s_tmem, v0);
-        if (nh > 1) tmem_ld_16x256b_x16(s_tmem + (16u << 16), v1);
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32(s_tmem + 0, r0);
+        tmem_ld32(s_tmem + 32, r1);
+        tmem_ld32(s_tmem + 64, r2);
+        tmem_ld32(s_tmem + 96, r3);
         tmem_wait_ld();
-        // S is in registers: the tile can take the next item's scores
-        tc_fence_before();
-        mbar_arrive(&bars->s_free[w]);
-        float m[4];
+        float m = -INFINITY;
         if (need_mask) {
-          m[0] = frag_row_max<true>(v0, 0, tc, kvl[0]);
-          m[1] = frag_row_max<true>(v0, 2, tc, kvl[1]);
-          if (nh > 1) {
-            m[2] = frag_row_max<true>(v1, 0, tc, kvl[2]);
-            m[3] = frag_row_max<true>(v1, 2, tc, kvl[3]);
-          }
+          m = max32<true>(r0, 0, kv_lim, m);
+          m = max32<true>(r1, 32, kv_lim, m);
+          m = max32<true>(r2, 64, kv_lim, m);
+          m = max32<true>(r3, 96, kv_lim, m);
         } else {
-          m[0] = frag_row_max<false>(v0, 0, tc, 127);
-          m[1] = frag_row_max<false>(v0, 2, tc, 127);
-          if (nh > 1) {
-            m[2] = frag_row_max<false>(v1, 0, tc, 127);
-            m[3] = frag_row_max<false>(v1, 2, tc, 127);
-          }
+          m = max32<false>(r0, 0, kv_lim, m);
+          m = max32<false>(r1, 32, kv_lim, m);
+          m = max32<false>(r2, 64, kv_lim, m);
+          m = max32<false>(r3, 96, kv_lim, m);
         }
+        m2 = m * p.score_log2;
         // p = 2^(x * c - m2 + 8): probabilities scaled by 256 so that small
         // ones stay out of E4M3's subnormal range; l and O carry the same
         // factor, which cancels.
-        float off[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          m2[r] = (r < 2 * nh) ? m[r] * c : -INFINITY;
-          off[r] = (m2[r] == -INFINITY) ? 0.f : 8.f - m2[r];
-        }
-        // the P tile is free once PV of this group's previous item is done
-        if (k > 0)
-          p_free = bounded_wait(&bars->o_full[w], (k - 1) & 1, abort, kWaitLimitNs);
-        if (p_free) {
-          const int row0 = 32 * quad + t4;
-          if (need_mask) {
-            l[0] = frag_row_exp<true>(v0, 0, tc, kvl[0], c, off[0], sP, row0);
-            if (R > 8) l[1] = frag_row_exp<true>(v0, 2, tc, kvl[1], c, off[1], sP, row0 + 8);
-            if (nh > 1) {
-              l[2] = frag_row_exp<true>(v1, 0, tc, kvl[2], c, off[2], sP, row0 + 16);
-              if (R > 24) l[3] = frag_row_exp<true>(v1, 2, tc, kvl[3], c, off[3], sP, row0 + 24);
-            }
-          } else {
-            l[0] = frag_row_exp<false>(v0, 0, tc, 127, c, off[0], sP, row0);
-            if (R > 8) l[1] = frag_row_exp<false>(v0, 2, tc, 127, c, off[1], sP, row0 + 8);
-            if (nh > 1) {
-              l[2] = frag_row_exp<false>(v1, 0, tc, 127, c, off[2], sP, row0 + 16);
-              if (R > 24) l[3] = frag_row_exp<false>(v1, 2, tc, 127, c, off[3], sP, row0 + 24);
-            }
-          }
+        const float off = (m2 == -INFINITY) ? 0.f : 8.f - m2;
+        const float c = p.score_log2;
+        if (need_mask) {
+          l += exp_pack32<true>(r0, 0, kv_lim, c, off, prow_s, row);
+          l += exp_pack32<true>(r1, 32, kv_lim, c, off, prow_s, row);
+          l += exp_pack32<true>(r2, 64, kv_lim, c, off, prow_s, row);
+          l += exp_pack32<true>(r3, 96, kv_lim, c, off, prow_s, row);
+        } else {
+          l += exp_pack32<false>(r0, 0, kv_lim, c, off, prow_s, row);
+          l += exp_pack32<false>(r1, 32, kv_lim, c, off, prow_s, row);
+          l += exp_pack32<false>(r2, 64, kv_lim, c, off, prow_s, row);
+          l += exp_pack32<false>(r3, 96, kv_lim, c, off, prow_s, row);
         }
       }
-      // Every thread, with or without rows, waits for PV of item li-2 before
-      // it writes the result ring: that PV needed the epilogue of item li-4,
-      // the last reader of this ring slot, to be done.
-      if (nh == 0 && k > 0)
-        p_free = bounded_wait(&bars->o_full[w], (k - 1) & 1, abort, kWaitLimitNs);
-      if (!p_free) {
-        if (!*abort) set_timeout(bars, p.status);
-        break;
-      }
-      if (tc == 0) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          RowMeta mt;
-          mt.prow = prow[r];
-          mt.inv = l[r] > 0.f ? p.v_scale / l[r] : 0.f;
-          mt.lse = l[r] > 0.f
-                       ? (m2[r] + __log2f(l[r]) - 8.f) * 0.69314718055994530942f
+      RowMeta mt;
+      mt.prow = prow;
+      mt.inv = l > 0.f ? p.v_scale / l : 0.f;
+      mt.lse = l > 0.f ? (m2 + __log2f(l) - 8.f) * 0.69314718055994530942f
                        : -INFINITY;
-          meta[(li % kMetaSlots) * kTileM + 32 * quad + 16 * (r >> 1) + t4 +
-               8 * (r & 1)] = mt;
-        }
-      }
+      meta[(li % kMetaSlots) * kTileM + row] = mt;
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->p_full[w]);
@@ -627,10 +493,9 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
   } else {
     setmaxnreg_dec<kRegsEpilogue>();
     // ------------------------------------------------------------ epilogue
-    // Same 16x256b fragments as the softmax: thread t writes columns
-    // 8i + 2(t%4) + {0,1} of rows t/4 (+8, +16, +24) of its quadrant.
     const int quad = warp & 3;
-    const int t4 = lane >> 2, tc = lane & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const RowMeta* meta = reinterpret_cast<const RowMeta*>(smem + kOffMeta);
     for (int li = 0; li < cnt; ++li) {
       const int w = li & 1, k = li >> 1;
@@ -639,42 +504,44 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
-      RowMeta mt[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-        mt[r] = meta[(li % kMetaSlots) * kTileM + 32 * quad + 16 * (r >> 1) +
-                     t4 + 8 * (r & 1)];
-      const bool h0 = __any_sync(0xffffffffu, mt[0].prow >= 0 || mt[1].prow >= 0);
-      const bool h1 = __any_sync(0xffffffffu, mt[2].prow >= 0 || mt[3].prow >= 0);
+      const RowMeta mt = meta[(li % kMetaSlots) * kTileM + row];
+      const bool valid = mt.prow >= 0;
+      const bool warp_valid = __any_sync(0xffffffffu, valid);
       if (!bounded_wait(&bars->o_full[w], k & 1, abort, kWaitLimitNs)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
       tc_fence_after();
-      const uint32_t o_tmem =
-          tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(w * 256 + 128);
+      if (warp_valid) {
+        const uint32_t o_tmem = tmem + lane_off + (uint32_t)(w * 256 + 128);
+        uint16_t* dst = p.part_o + mt.prow * (int64_t)kD;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (!(h == 0 ? h0 : h1)) continue;
-        uint32_t v[64];
-        __syncwarp();
-        tmem_ld_16x256b_x16(o_tmem + ((uint32_t)(16 * h) << 16), v);
-        tmem_wait_ld();
+        for (int half = 0; half < 2; ++half) {
+          uint32_t ra[32], rb[32];
+          __syncwarp();
+          tmem_ld32(o_tmem + half * 64, ra);
+          tmem_ld32(o_tmem + half * 64 + 32, rb);
+          tmem_wait_ld();
+          if (valid) {
+            uint32_t o[32];
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          const RowMeta& m = mt[2 * h + b];
-          if (m.prow < 0) continue;
-          uint32_t* dst = reinterpret_cast<uint32_t*>(
-              p.part_o + m.prow * (int64_t)kD + 2 * tc);
+            for (int e = 0; e < 16; ++e) {
+              __nv_bfloat162 a2 = __floats2bfloat162_rn(
+                  __uint_as_float(ra[2 * e]) * mt.inv,
+                  __uint_as_float(ra[2 * e + 1]) * mt.inv);
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(
+                  __uint_as_float(rb[2 * e]) * mt.inv,
+                  __uint_as_float(rb[2 * e + 1]) * mt.inv);
+              o[e] = *reinterpret_cast<uint32_t*>(&a2);
+              o[16 + e] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            uint4* d4 = reinterpret_cast<uint4*>(dst + half * 64);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(
-                __uint_as_float(v[4 * i + 2 * b]) * m.inv,
-                __uint_as_float(v[4 * i + 2 * b + 1]) * m.inv);
-            dst[4 * i] = *reinterpret_cast<uint32_t*>(&h2);
+            for (int q = 0; q < 8; ++q)
+              d4[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
           }
-          if (tc == 0) p.part_lse[m.prow] = m.lse;
         }
+        if (valid) p.part_lse[mt.prow] = mt.lse;
       }
       tc_fence_before();
       mbar_arrive(&bars->o_free[w]);
