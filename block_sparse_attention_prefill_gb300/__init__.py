@@ -86,6 +86,8 @@ def load():
         "msa_decode_workspace_bytes": ([i64, i64, i64, i64, i64, SZ], i32),
         "msa_decode": ([P, P, i64, f32, f32, f32, f32, P, P, i64, P, i64, i64,
                         i64, i64, i64, P, ctypes.c_size_t, P, P, PL, P], i32),
+        "msa_decode_noalloc": ([P, P, i64, f32, f32, f32, f32, P, P, i64, P,
+                                i64, i64, i64, i64, i64, P, P, P], i32),
         "msa_read_status": ([PL, ctypes.POINTER(ctypes.c_uint32)], i32),
         "msa_read_counters": ([PL, ctypes.POINTER(ctypes.c_int64),
                                ctypes.POINTER(ctypes.c_int64)], i32),
@@ -362,6 +364,31 @@ def msa_decode(q, kv, q_scale, k_scale, v_scale, softmax_scale, topk,
                              need, _ptr(out), _ptr(lse), ctypes.byref(st),
                              _stream(stream)), "msa_decode")
     return out, lse, Plan(st, ws, (topk, seq_lens, block_table))
+
+
+def msa_decode_noalloc(q, kv, q_scale, k_scale, v_scale, softmax_scale,
+                       topk, block_table, seq_lens, n, max_seqlen_k, out, lse,
+                       stream=None):
+    """msa_decode with the library's fixed device scratch instead of a
+    workspace: for callers that cannot allocate device memory.  out and lse
+    are the caller's; nothing is allocated here or in the library call."""
+    _need(q, "q", _E4M3)
+    _need(kv, "kv", _E4M3)
+    _need(topk, "topk", (torch.int32,))
+    _need(block_table, "block_table", (torch.int32,))
+    _need(seq_lens, "seq_lens", (torch.int32,))
+    _need(out, "out", (torch.bfloat16,))
+    if lse is not None:
+        _need(lse, "lse", (torch.float32,))
+    B = int(seq_lens.numel())
+    bt_stride = int(block_table.shape[1]) if block_table.dim() == 2 else 1
+    _check(load().msa_decode_noalloc(
+        _ptr(_bytes(q)), _ptr(_bytes(kv)), int(kv.shape[0]), float(q_scale),
+        float(k_scale), float(v_scale), float(softmax_scale), _ptr(topk),
+        _ptr(block_table), bt_stride, _ptr(seq_lens), B, int(n),
+        int(q.shape[1]), int(topk.shape[1]), int(max_seqlen_k), _ptr(out),
+        _ptr(lse), _stream(stream)), "msa_decode_noalloc")
+    return out, lse
 
 
 def run_workload(w, stream=None):

@@ -4,6 +4,7 @@
 // msa_read_counters, which are documented to synchronise.
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -283,6 +284,8 @@ const char* msa_status_string(int code) {
     case MSA_ERR_WORKSPACE: return "workspace missing or too small";
     case MSA_ERR_CUDA: return "a CUDA call failed";
     case MSA_ERR_NULL: return "a required pointer is NULL";
+    case MSA_ERR_TOO_LARGE:
+      return "problem needs more scratch than msa_decode_noalloc's fixed array";
     default: return "unknown status";
   }
 }
@@ -420,6 +423,61 @@ int msa_decode(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
                       softmax_scale, block_table, bt_stride, plan,
                       ws + d.cu_bytes + d.plan_bytes, d.prefill_bytes, out,
                       lse, st);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Scratch of msa_decode_noalloc: one fixed array on every GPU that loads this
+// library, kept until the process exits.  Host code must not use its name
+// as a device address; it asks the runtime for the address once per device.
+static __device__ __align__(256) unsigned char
+    g_decode_scratch[MSA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+int decode_scratch(void** ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MSA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MSA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess ||
+        p == nullptr)
+      return MSA_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *ptr = g_scratch_ptr[dev];
+  return MSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int msa_decode_noalloc(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
+                       float q_scale, float k_scale, float v_scale,
+                       float softmax_scale, const int32_t* topk,
+                       const int32_t* block_table, int64_t bt_stride,
+                       const int32_t* seq_lens, int64_t B, int64_t n,
+                       int64_t Hq, int64_t Hkv, int64_t max_seqlen_k,
+                       uint16_t* out, float* lse, void* stream) {
+  size_t need = 0;
+  int rc = msa_decode_workspace_bytes(B, n, Hq, Hkv, max_seqlen_k, &need);
+  if (rc) return rc;
+  if (need > (size_t)MSA_NOALLOC_SCRATCH_BYTES) return MSA_ERR_TOO_LARGE;
+  if (B == 0) return MSA_OK;
+  void* scratch = nullptr;
+  rc = decode_scratch(&scratch);
+  if (rc) return rc;
+  return msa_decode(q, kv, num_pages, q_scale, k_scale, v_scale, softmax_scale,
+                    topk, block_table, bt_stride, seq_lens, B, n, Hq, Hkv,
+                    max_seqlen_k, scratch, MSA_NOALLOC_SCRATCH_BYTES, out, lse,
+                    nullptr, stream);
 }
 
 int msa_read_status(const msa_plan_t* plan, uint32_t* status) {

@@ -69,6 +69,7 @@ extern "C" {
 #define MSA_ERR_WORKSPACE 4   /* workspace NULL or smaller than required      */
 #define MSA_ERR_CUDA 5        /* a CUDA runtime / driver call failed          */
 #define MSA_ERR_NULL 6        /* a required pointer is NULL                   */
+#define MSA_ERR_TOO_LARGE 7   /* beyond msa_decode_noalloc's fixed scratch    */
 
 /* device status bits (msa_read_status) */
 #define MSA_STATUS_BAD_PAGE_ID (1u << 0)  /* top-k id >= page count, or < -1 */
@@ -280,6 +281,40 @@ MSA_API int msa_decode(const uint8_t *q, const uint8_t *kv, int64_t num_pages,
                int64_t Hkv, int64_t max_seqlen_k, void *workspace,
                size_t workspace_bytes, uint16_t *out, float *lse,
                msa_plan_t *plan_out, void *stream);
+
+/*
+ * msa_decode for callers that cannot allocate device memory -- for example
+ * code that only receives raw device pointers through a foreign-function
+ * boundary and has no access to an allocator, or that runs where allocating
+ * is not allowed.  It takes the same arguments as msa_decode except the
+ * workspace and plan_out, and computes the same result with the same
+ * kernels.  (The pages have no counterpart; this is a library convenience.)
+ *
+ * Its scratch -- the sequence prefix sums, the plan and the split partials
+ * that msa_decode keeps in the caller's workspace -- lives in one fixed
+ * array of MSA_NOALLOC_SCRATCH_BYTES (16 MiB) of device memory that every GPU
+ * which loads this library holds until the process exits.  The call itself
+ * allocates and frees nothing.
+ *   - A batch whose msa_decode_workspace_bytes() exceeds that size is
+ *     rejected with MSA_ERR_TOO_LARGE before anything is launched.
+ *   - The first call on a device looks up the array's device address (a
+ *     runtime call, made once per device with that device current); make
+ *     that first call before any stream capture.
+ *   - All calls share the one array and each overwrites it (the parts that
+ *     must start at zero are cleared by every call).  Calls whose work
+ *     overlaps on the GPU -- on different streams, or from several host
+ *     threads -- race and must not be issued.
+ *   - Device status bits are not returned (there is no plan_out).
+ */
+#define MSA_NOALLOC_SCRATCH_BYTES (16u << 20)
+MSA_API int msa_decode_noalloc(const uint8_t *q, const uint8_t *kv,
+                               int64_t num_pages, float q_scale,
+                               float k_scale, float v_scale,
+                               float softmax_scale, const int32_t *topk,
+                               const int32_t *block_table, int64_t bt_stride,
+                               const int32_t *seq_lens, int64_t B, int64_t n,
+                               int64_t Hq, int64_t Hkv, int64_t max_seqlen_k,
+                               uint16_t *out, float *lse, void *stream);
 
 /*
  * Copies the plan's device status word to *status.  This call synchronises
