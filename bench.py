@@ -66,6 +66,31 @@ def parse():
     return ap.parse_args()
 
 
+# ---------------------------------------------------------------- ranks
+# One process per GPU under torchrun; every rank runs its own independent
+# batch (its own seed).  Ranks exchange only timings and work counts.
+
+def rank_seed(seed, rank):
+    return seed + rank
+
+
+def reduce_over_ranks(values, world, device, op="max"):
+    """Element-wise max (timings) or sum (work) over the ranks."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(
+            t, op=torch.distributed.ReduceOp.MAX if op == "max"
+            else torch.distributed.ReduceOp.SUM)
+    return t.tolist()
+
+
+def job_tflops(total_pairs, step_ms):
+    """Whole-job selected-token TFLOP/s: 4 * 128 FLOPs per attended
+    (query head, key) pair, summed over ranks, over the slowest rank's
+    time."""
+    return 4.0 * 128 * total_pairs / (step_ms / 1e3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -203,7 +228,7 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     msa.load()
-    w = workloads.make_config(args.workload, seed=args.seed + rank,
+    w = workloads.make_config(args.workload, seed=rank_seed(args.seed, rank),
                               device="cpu", kv_device=dev)
     pairs, upages = pair_and_page_counts(w)
     wd = w.to(dev)
@@ -302,15 +327,14 @@ def run_ours(args, rank, world):
         e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h}
     clk = clocks.stop()
 
-    t = torch.tensor([total_ms, attn_ms, comb_ms, plan_ms, step_ms,
-                      e2e["ms"] if e2e else 0.0], dtype=torch.float64,
-                     device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    total_ms, attn_ms, comb_ms, plan_ms, step_ms, e2e_ms = t.tolist()
+    total_ms, attn_ms, comb_ms, plan_ms, step_ms, e2e_ms = reduce_over_ranks(
+        [total_ms, attn_ms, comb_ms, plan_ms, step_ms,
+         e2e["ms"] if e2e else 0.0], world, dev, "max")
+    (job_pairs,) = reduce_over_ranks([float(pairs)], world, dev, "sum")
     return dict(w=w, pairs=pairs, upages=upages, total_ms=total_ms,
                 attn_ms=attn_ms, comb_ms=comb_ms, plan_ms=plan_ms,
                 step_ms=step_ms, e2e=e2e, e2e_ms=e2e_ms, clocks=clk,
+                job_pairs=job_pairs,
                 status=status, t_wall=t_wall)
 
 
@@ -423,7 +447,7 @@ def main():
         peaks = load_peaks()
         flops = 4.0 * 128 * r["pairs"]
         step_s = r["step_ms"] / 1e3
-        value = world * flops / step_s / 1e12
+        value = job_tflops(r["job_pairs"], r["step_ms"])
         alg = algorithmic_bytes(w, r["upages"])
         attn_s = r["attn_ms"] / 1e3
         achieved = alg["attention"] / attn_s / 1e9
@@ -461,7 +485,7 @@ def main():
             "clocks": r["clocks"], "device_status": r["status"],
         }
         if r["e2e"]:
-            line["e2e"] = {"value": world * flops / (r["e2e_ms"] / 1e3) / 1e12,
+            line["e2e"] = {"value": job_tflops(r["job_pairs"], r["e2e_ms"]),
                            "unit": "TFLOP/s",
                            "h2d_bytes_per_step": r["e2e"]["h2d"],
                            "d2h_bytes_per_step": r["e2e"]["d2h"],
