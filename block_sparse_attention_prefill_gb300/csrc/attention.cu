@@ -74,7 +74,13 @@ struct RowMeta {
   float inv;
 };
 constexpr int kOffMeta = kOffRec + kKvStages * kRecMax;
-constexpr int kOffBar = kOffMeta + kMetaSlots * kTileM * (int)sizeof(RowMeta);
+// producer staging of prefetched record headers and token ids: two halves
+// of kBatch items each
+constexpr int kBatch = 8;
+constexpr int kOffStage = kOffMeta + kMetaSlots * kTileM * (int)sizeof(RowMeta);
+constexpr int kStageHdr = 2 * kBatch * 16;                   // int4 per item
+constexpr int kStageTok = 2 * kBatch * 16 * 4;               // 16 ids per item
+constexpr int kOffBar = kOffStage + kStageHdr + kStageTok;
 
 struct Barriers {
   uint64_t rec_full[kKvStages];
@@ -83,6 +89,7 @@ struct Barriers {
   uint64_t q_full[kQStages];
   uint64_t q_empty[kQStages];
   uint64_t s_full[2];
+  uint64_t s_free[2];
   uint64_t p_full[2];
   uint64_t o_full[2];
   uint64_t o_free[2];
@@ -181,9 +188,13 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
   const int lane = threadIdx.x & 31;
 
   const int num_work = p.counters[1];
-  const int begin = (int)((int64_t)blockIdx.x * num_work / gridDim.x);
-  const int end = (int)((int64_t)(blockIdx.x + 1) * num_work / gridDim.x);
-  const int cnt = end - begin;
+  // work items are dealt round-robin: CTA b takes items b, b + grid, ...
+  // Items of one heavily selected KV row are adjacent in the work list, so
+  // contiguous ranges would give a few CTAs all of the full 128-row items.
+  const int cnt = blockIdx.x < (unsigned)num_work
+                      ? (num_work - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
+                      : 0;
+  const int64_t rec_step = (int64_t)gridDim.x * p.rec_stride;  // int4s between own items
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kKvStages; ++s) {
@@ -197,6 +208,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(&bars->s_full[w], 1);
+      mbar_init(&bars->s_free[w], kSoftmaxThreads);
       mbar_init(&bars->p_full[w], kSoftmaxThreads);
       mbar_init(&bars->o_full[w], 1);
       mbar_init(&bars->o_free[w], kSoftmaxThreads);
@@ -227,54 +239,87 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     // ------------------------------------------------------------ producer
     // whole warp: lane 0 waits for free slots and issues the record / K / V
     // copies; in TMA-Q mode lane i issues the Q box of the item's token i
-    // (C = 128 / G <= 16 tokens).  Header and token ids of the next item
-    // are prefetched from the record in global memory.
-    const int4* grec = p.records + (int64_t)begin * p.rec_stride;
+    // (C = 128 / G <= 16 tokens).
+    const int4* grec = p.records + (int64_t)blockIdx.x * p.rec_stride;
     const int C = kTileM / p.G;
-    int4 hdr_next = cnt > 0 ? grec[0] : make_int4(0, 0, 0, 0);
-    int tok_next = (cnt > 0 && p.q_tma && lane < C) ? grec[1 + lane].x : 0;
-    int issued = 0;
-    for (int li = 0; li < cnt; ++li) {
-      const int ks = li % kKvStages, qs = li % kQStages;
-      const int4 hdr = hdr_next;
-      const int tok = tok_next;
-      if (li + 1 < cnt) {
-        const int4* nr = grec + (int64_t)(li + 1) * p.rec_stride;
-        hdr_next = nr[0];
-        if (p.q_tma && lane < C) tok_next = nr[1 + lane].x;
-      }
-      int ok = 1;
-      if (lane == 0) {
-        if (li >= kKvStages)
-          ok = bounded_wait(&bars->kv_empty[ks], ((li / kKvStages) - 1) & 1,
-                            abort, kWaitLimitNs);
-        if (ok && li >= kQStages)
-          ok = bounded_wait(&bars->q_empty[qs], ((li / kQStages) - 1) & 1,
-                            abort, kWaitLimitNs);
-        if (!ok && !*abort) set_timeout(bars, p.status);
-      }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      if (lane == 0) {
-        const uint32_t rec_bytes = 16u * (1u + (uint32_t)hdr.y);
-        mbar_arrive_expect_tx(&bars->rec_full[ks], rec_bytes);
-        bulk_load(smem + kOffRec + ks * kRecMax,
-                  p.records + (int64_t)(begin + li) * p.rec_stride, rec_bytes,
-                  &bars->rec_full[ks]);
-        mbar_arrive_expect_tx(&bars->kv_full[ks], 2 * kTile);
-        tma_load_2d(smem + kOffK + ks * kTile, &kv_map, &bars->kv_full[ks], 0, hdr.x);
-        tma_load_2d(smem + kOffV + ks * kTile, &kv_map, &bars->kv_full[ks], kD, hdr.x);
-        if (p.q_tma)
-          mbar_arrive_expect_tx(&bars->q_full[qs], (uint32_t)(hdr.y * p.G * 128));
-      }
+    // Headers and token ids are staged kBatch items ahead in shared memory
+    // by cp.async: the copies of batch b+1 are issued when batch b starts and
+    // waited for when it ends, so the producer never stalls on a global
+    // load.  Lane j < kBatch copies the header of item j; lane l copies the
+    // token ids at flat entries l, l+32, l+64, l+96 of the kBatch x 16 ids.
+    int4* shdr = reinterpret_cast<int4*>(smem + kOffStage);
+    int* stok = reinterpret_cast<int*>(smem + kOffStage + kStageHdr);
+    auto load_batch = [&](int base, int half) {
+      if (lane < kBatch && base + lane < cnt)
+        cp_async_16(smem_u32(shdr + half * kBatch + lane),
+                    grec + (base + lane) * rec_step);
       if (p.q_tma) {
-        __syncwarp();
-        if (lane < hdr.y)
-          tma_load_2d(smem + kOffQ + qs * kTile +
-                          ((lane * p.G + row_rotation(li, p.G)) & (kTileM - 1)) * 128,
-                      &q_map, &bars->q_full[qs], 0, tok * p.Hq + hdr.w);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = lane + 32 * u, j = e >> 4, i = e & 15;
+          if (i < C && base + j < cnt)
+            cp_async_4(smem_u32(stok + half * kBatch * 16 + e),
+                       grec + (base + j) * rec_step + 1 + i);
+        }
       }
-      issued = li + 1;
+      cp_async_commit();
+    };
+    auto wait_batch = [&]() {
+      cp_async_wait<0>();
+      __syncwarp();
+    };
+    load_batch(0, 0);
+    wait_batch();
+    int issued = 0;
+    bool ok_all = true;
+    for (int base = 0; ok_all && base < cnt; base += kBatch) {
+      const int half = (base / kBatch) & 1;
+      if (base + kBatch < cnt) load_batch(base + kBatch, half ^ 1);
+      for (int j = 0; j < kBatch && base + j < cnt; ++j) {
+        const int li = base + j;
+        const int ks = li % kKvStages, qs = li % kQStages;
+        const int4 hdr = shdr[half * kBatch + j];
+        const int tok = (lane < 16) ? stok[(half * kBatch + j) * 16 + lane] : 0;
+        int ok = 1;
+        if (lane == 0) {
+          if (li >= kKvStages)
+            ok = bounded_wait(&bars->kv_empty[ks], ((li / kKvStages) - 1) & 1,
+                              abort, kWaitLimitNs);
+          if (ok && li >= kQStages)
+            ok = bounded_wait(&bars->q_empty[qs], ((li / kQStages) - 1) & 1,
+                              abort, kWaitLimitNs);
+          if (!ok && !*abort) set_timeout(bars, p.status);
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          ok_all = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t rec_bytes = 16u * (1u + (uint32_t)hdr.y);
+          mbar_arrive_expect_tx(&bars->rec_full[ks], rec_bytes);
+          bulk_load(smem + kOffRec + ks * kRecMax,
+                    grec + li * rec_step, rec_bytes,
+                    &bars->rec_full[ks]);
+          mbar_arrive_expect_tx(&bars->kv_full[ks], 2 * kTile);
+          tma_load_2d(smem + kOffK + ks * kTile, &kv_map, &bars->kv_full[ks], 0, hdr.x);
+          tma_load_2d(smem + kOffV + ks * kTile, &kv_map, &bars->kv_full[ks], kD, hdr.x);
+          if (p.q_tma)
+            mbar_arrive_expect_tx(&bars->q_full[qs], (uint32_t)(hdr.y * p.G * 128));
+        }
+        if (p.q_tma) {
+          __syncwarp();
+          if (lane < hdr.y)
+            tma_load_2d(smem + kOffQ + qs * kTile +
+                            ((lane * p.G + row_rotation(li, p.G)) & (kTileM - 1)) * 128,
+                        &q_map, &bars->q_full[qs], 0, tok * p.Hq + hdr.w);
+        }
+        issued = li + 1;
+      }
+      // the other half is complete once this lane's copies have landed
+      // and every lane is past this point
+      if (base + kBatch < cnt) wait_batch();
     }
+    cp_async_wait<0>();
     // every copy this warp started must land before the CTA exits
     if (lane == 0) {
       for (int li = issued > kKvStages ? issued - kKvStages : 0; li < issued; ++li) {
@@ -322,13 +367,16 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         mma_commit(&bars->kv_empty[ks]);
       };
       // in-order issue of QK(qk) and PV(pv), each as soon as it is ready;
-      // QK(n) reuses the S tile of item n-2, free once PV(n-2) was issued
+      // QK(n) reuses the S tile of item n-2, free once the softmax has
+      // loaded S(n-2) into registers
       int qk = 0, pv = 0;
       uint64_t idle_since = global_timer_ns();
       while (pv < cnt) {
         bool progressed = false;
-        if (qk < cnt && qk <= pv + 1) {
-          if (mbar_test(&bars->kv_full[qk % kKvStages], (qk / kKvStages) & 1) &&
+        if (qk < cnt) {
+          const int k = qk >> 1;
+          if ((k == 0 || mbar_test(&bars->s_free[qk & 1], (k - 1) & 1)) &&
+              mbar_test(&bars->kv_full[qk % kKvStages], (qk / kKvStages) & 1) &&
               mbar_test(&bars->q_full[qk % kQStages], (qk / kQStages) & 1)) {
             issue_qk(qk);
             ++qk;
@@ -433,22 +481,27 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
+      tc_fence_after();
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      if (warp_valid) {
+        __syncwarp();
+        tmem_ld32(s_tmem + 0, r0);
+        tmem_ld32(s_tmem + 32, r1);
+        tmem_ld32(s_tmem + 64, r2);
+        tmem_ld32(s_tmem + 96, r3);
+        tmem_wait_ld();
+      }
+      // S is in registers: QK of this group's next item may overwrite it
+      tc_fence_before();
+      mbar_arrive(&bars->s_free[w]);
       // the P tile is free once PV of this group's previous item is done
       if (k > 0 &&
           !bounded_wait(&bars->o_full[w], (k - 1) & 1, abort, kWaitLimitNs)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
-      tc_fence_after();
       float m2 = -INFINITY, l = 0.f;
       if (warp_valid) {
-        __syncwarp();
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        tmem_ld32(s_tmem + 0, r0);
-        tmem_ld32(s_tmem + 32, r1);
-        tmem_ld32(s_tmem + 64, r2);
-        tmem_ld32(s_tmem + 96, r3);
-        tmem_wait_ld();
         float m = -INFINITY;
         if (need_mask) {
           m = max32<true>(r0, 0, kv_lim, m);

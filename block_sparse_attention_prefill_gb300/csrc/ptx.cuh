@@ -123,6 +123,12 @@ __device__ __forceinline__ void cp_async_16(uint32_t smem_addr,
                "l"(gptr)
                : "memory");
 }
+__device__ __forceinline__ void cp_async_4(uint32_t smem_addr,
+                                           const void* gptr) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr),
+               "l"(gptr)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
