@@ -187,6 +187,10 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // the plan's counters and records are written by the kernels before this
+  // one in the stream
+  pdl_wait();
+  pdl_trigger();
   const int num_work = p.counters[1];
   // work items are dealt round-robin: CTA b takes items b, b + grid, ...
   // Items of one heavily selected KV row are adjacent in the work list, so
@@ -689,8 +693,8 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
     attr_set = true;
   }
   const int64_t grid = std::min<int64_t>(num_sms(), pl.max_work);
-  attention_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(kv_map, q_map, p);
-  return cudaGetLastError();
+  return launch_pdl(attention_kernel, dim3((unsigned)grid), dim3(kThreads), kSmemBytes,
+                    stream, kv_map, q_map, p);
 }
 
 }  // namespace msa

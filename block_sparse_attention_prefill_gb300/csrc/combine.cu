@@ -34,6 +34,8 @@ combine_kernel(const TIn* __restrict__ part_o, const float* __restrict__ part_ls
                const uint16_t* __restrict__ slot_mask, int64_t group,
                int64_t rows, int S, uint16_t* __restrict__ out,
                float* __restrict__ lse_out) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   if (r >= rows) return;
@@ -95,6 +97,8 @@ combine16_kernel(const __nv_bfloat16* __restrict__ part_o,
                  const uint16_t* __restrict__ slot_mask, int64_t group,
                  int64_t rows, uint16_t* __restrict__ out,
                  float* __restrict__ lse_out) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int sub = lane & 15;                 // lane within the half-warp
   const int64_t r = ((int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5)) * 2 +
@@ -202,28 +206,26 @@ cudaError_t launch_combine(const void* part_o, int part_dtype,
   if (rows == 0) return cudaSuccess;
   const unsigned grid = (unsigned)ceil_div(rows, kWarpsPerBlock);
   const int S = (int)splits;
+  const dim3 block(kWarpsPerBlock * 32);
+  const uint16_t* no_mask = nullptr;
+  const int64_t one = 1;
   if (part_dtype == MSA_DTYPE_BF16) {
     auto po = static_cast<const __nv_bfloat16*>(part_o);
     if (slot_mask && S == kTopK)
-      combine16_kernel<<<(unsigned)ceil_div(rows, 2 * kWarpsPerBlock),
-                         kWarpsPerBlock * 32, 0, stream>>>(
-          po, part_lse, slot_mask, group, rows, out, lse);
-    else if (slot_mask)
-      combine_kernel<__nv_bfloat16, true><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
-          po, part_lse, slot_mask, group, rows, S, out, lse);
-    else
-      combine_kernel<__nv_bfloat16, false><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
-          po, part_lse, nullptr, 1, rows, S, out, lse);
-  } else {
-    auto po = static_cast<const float*>(part_o);
+      return launch_pdl(combine16_kernel, dim3((unsigned)ceil_div(rows, 2 * kWarpsPerBlock)),
+                        block, 0, stream, po, part_lse, slot_mask, group, rows, out, lse);
     if (slot_mask)
-      combine_kernel<float, true><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
-          po, part_lse, slot_mask, group, rows, S, out, lse);
-    else
-      combine_kernel<float, false><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
-          po, part_lse, nullptr, 1, rows, S, out, lse);
+      return launch_pdl(combine_kernel<__nv_bfloat16, true>, dim3(grid), block, 0, stream,
+                        po, part_lse, slot_mask, group, rows, S, out, lse);
+    return launch_pdl(combine_kernel<__nv_bfloat16, false>, dim3(grid), block, 0, stream,
+                      po, part_lse, no_mask, one, rows, S, out, lse);
   }
-  return cudaGetLastError();
+  auto po = static_cast<const float*>(part_o);
+  if (slot_mask)
+    return launch_pdl(combine_kernel<float, true>, dim3(grid), block, 0, stream, po,
+                      part_lse, slot_mask, group, rows, S, out, lse);
+  return launch_pdl(combine_kernel<float, false>, dim3(grid), block, 0, stream, po,
+                    part_lse, no_mask, one, rows, S, out, lse);
 }
 
 cudaError_t launch_decode_seqlens(const int32_t* seq_lens, int64_t B,

@@ -58,4 +58,34 @@ cudaError_t launch_decode_seqlens(const int32_t* seq_lens, int64_t B,
 
 int num_sms();
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may
+// start while the kernel before it in the stream is still running: it
+// calls pdl_wait() before its first global-memory access, which returns
+// once every earlier kernel of the stream has completed and its writes are
+// visible.  pdl_trigger() lets the next kernel be scheduled early.  With
+// no kernel in front (an event or a copy instead), pdl_wait() returns at
+// once and the launch is ordinary.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                       size_t smem, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 }  // namespace msa

@@ -5,9 +5,12 @@
 // total_kv_blocks, qhead_per_kv, return_schedule=True); vLLM PR 60930,
 // Details / "Host sync": the plan stays on the device, no host copy.)
 //
-// Steps, all on `stream`, no host synchronisation:
-//   memset   status word and the (row, token) membership bitmap
-//   prep     one CTA: per-request row offsets (sum of page counts), checks
+// Steps, all on `stream`, no host synchronisation; every kernel after the
+// first is a programmatic dependent launch (its launch overlaps the tail of
+// the kernel before it, its work does not):
+//   prep     CTA 0: per-request row offsets (sum of page counts), checks,
+//            status word; every CTA: clears its share of the (row, token)
+//            membership bitmap
 //   mark     one thread per top-k entry: validate the id, drop repeats, set
 //            one bit per kept page in the membership bitmap; the (token,
 //            KV head) list's 16 threads together write its slot mask.  This is the histogram, kept as bits: repeats
@@ -24,6 +27,8 @@
 //            slot of the work record the attention kernel will read.
 // Every output is a function of the inputs alone: bit-exact and
 // deterministic run to run.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace msa {
@@ -100,7 +105,16 @@ struct PlanDev {
 };
 
 // counters[2] == 1 when the per-request metadata passed the checks.
-__global__ void __launch_bounds__(kScanThreads) plan_prep_kernel(PlanDev d) {
+__global__ void __launch_bounds__(kScanThreads) plan_prep_kernel(PlanDev d,
+                                                                 int64_t bitmap_vec) {
+  pdl_trigger();
+  {
+    uint4* bm = reinterpret_cast<uint4*>(d.bitmap);
+    for (int64_t i = (int64_t)blockIdx.x * kScanThreads + threadIdx.x; i < bitmap_vec;
+         i += (int64_t)gridDim.x * kScanThreads)
+      bm[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (blockIdx.x != 0) return;
   __shared__ int s_bad;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
@@ -132,7 +146,7 @@ __global__ void __launch_bounds__(kScanThreads) plan_prep_kernel(PlanDev d) {
     unsigned st = 0;
     if (s_bad) st |= MSA_STATUS_BAD_SEQLENS;
     if (!s_bad && overflow) st |= MSA_STATUS_ROWS_OVERFLOW;
-    if (st) atomicOr(d.status, st);
+    *d.status = st;
     d.counters[0] = 0;
     d.counters[1] = 0;
     d.counters[2] = st ? 0 : 1;
@@ -160,6 +174,8 @@ __device__ __forceinline__ TokenInfo token_info(const PlanDev& d, int t, int h) 
 // One thread per top-k entry (t, h, j); the 16 entries of a (t, h) list sit
 // in one half-warp and see each other through shuffles.
 __global__ void __launch_bounds__(256) plan_mark_kernel(PlanDev d) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t total = (int64_t)d.T * d.Hkv * kTopK;
   const int lane = threadIdx.x & 31;
@@ -204,6 +220,8 @@ __global__ void __launch_bounds__(256) plan_mark_kernel(PlanDev d) {
 // One thread per row, kPlanTile rows per CTA.  Rows are 16-byte aligned
 // (W is a multiple of 4), read and written four words at a time.
 __global__ void __launch_bounds__(kPlanTile) plan_rows_kernel(PlanDev d) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t r = (int64_t)blockIdx.x * kPlanTile + threadIdx.x;
   const bool ok = d.counters[2] == 1;
   int c = 0;
@@ -242,6 +260,8 @@ __global__ void __launch_bounds__(kPlanTile) plan_rows_kernel(PlanDev d) {
 }
 
 __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(PlanDev d) {
+  pdl_wait();
+  pdl_trigger();
   for (int which = 0; which < 2; ++which) {
     int32_t* a = d.tile_sums + (int64_t)which * d.ntiles;
     int carry = 0;
@@ -261,6 +281,8 @@ __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(PlanDev d) {
 }
 
 __global__ void __launch_bounds__(kPlanTile) plan_emit_kernel(PlanDev d) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t r = (int64_t)blockIdx.x * kPlanTile + threadIdx.x;
   const bool ok = d.counters[2] == 1;
   const int c = (ok && r < d.rows) ? d.row_cnt[r] : 0;
@@ -293,6 +315,8 @@ __global__ void __launch_bounds__(kPlanTile) plan_emit_kernel(PlanDev d) {
 // One thread per kept top-k entry: its place in the row is the number of
 // tokens of the row before it, read from the word prefix plus a popcount.
 __global__ void __launch_bounds__(256) plan_scatter_kernel(PlanDev d) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= (int64_t)d.T * d.Hkv * kTopK) return;
   if (d.counters[2] != 1) return;
@@ -351,22 +375,26 @@ cudaError_t launch_plan(const msa_plan_t& pl, const int32_t* topk,
   d.slot_mask = pl.slot_mask;
   d.status = pl.status;
 
-  cudaError_t e = cudaMemsetAsync(pl.status, 0, sizeof(uint32_t), stream);
-  if (e != cudaSuccess) return e;
-  const size_t bm = (size_t)pl.rows * (size_t)pl.bitmap_words * sizeof(uint32_t);
-  if (bm) {
-    e = cudaMemsetAsync(pl.bitmap, 0, bm, stream);
-    if (e != cudaSuccess) return e;
-  }
+  // bitmap rows are W words, W a multiple of 4: whole 16-byte vectors
+  const int64_t bitmap_vec = pl.rows * pl.bitmap_words / 4;
+  const int64_t zgrid = std::min<int64_t>(ceil_div(bitmap_vec, kScanThreads),
+                                          2 * (int64_t)num_sms());
   const int64_t marks = (int64_t)pl.T * pl.Hkv * kTopK;
   const unsigned mgrid = (unsigned)ceil_div(marks, 256);
-  plan_prep_kernel<<<1, kScanThreads, 0, stream>>>(d);
-  if (marks > 0) plan_mark_kernel<<<mgrid, 256, 0, stream>>>(d);
-  if (d.ntiles > 0) plan_rows_kernel<<<d.ntiles, kPlanTile, 0, stream>>>(d);
-  plan_scan_kernel<<<1, kScanThreads, 0, stream>>>(d);
-  if (d.ntiles > 0) plan_emit_kernel<<<d.ntiles, kPlanTile, 0, stream>>>(d);
-  if (marks > 0) plan_scatter_kernel<<<mgrid, 256, 0, stream>>>(d);
-  return cudaGetLastError();
+  plan_prep_kernel<<<(unsigned)std::max<int64_t>(zgrid, 1), kScanThreads, 0, stream>>>(
+      d, bitmap_vec);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess && marks > 0)
+    e = launch_pdl(plan_mark_kernel, mgrid, 256, 0, stream, d);
+  if (e == cudaSuccess && d.ntiles > 0)
+    e = launch_pdl(plan_rows_kernel, (unsigned)d.ntiles, kPlanTile, 0, stream, d);
+  if (e == cudaSuccess)
+    e = launch_pdl(plan_scan_kernel, 1u, kScanThreads, 0, stream, d);
+  if (e == cudaSuccess && d.ntiles > 0)
+    e = launch_pdl(plan_emit_kernel, (unsigned)d.ntiles, kPlanTile, 0, stream, d);
+  if (e == cudaSuccess && marks > 0)
+    e = launch_pdl(plan_scatter_kernel, mgrid, 256, 0, stream, d);
+  return e;
 }
 
 }  // namespace msa
