@@ -48,7 +48,7 @@ import workloads  # noqa: E402
 
 WORKLOAD = "long_prefill_1m"
 L2_FLUSH_BYTES = 256 << 20
-KERNELS_PER_STEP = 7  # plan: prep, mark, count, scan, fill; attention; combine
+KERNELS_PER_STEP = 8  # plan: prep, mark, rows, scan, emit, scatter; attention; combine
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attention_kernel_traffic.json")
 ATTN_SOURCES = ["attention.cu", "ptx.cuh", "common.cuh"]
 
