@@ -49,6 +49,7 @@ import workloads  # noqa: E402
 WORKLOAD = "long_prefill_1m"
 L2_FLUSH_BYTES = 256 << 20
 KERNELS_PER_STEP = 8  # plan: prep, mark, rows, scan, emit, scatter; attention; combine
+DECODE_KERNELS_PER_STEP = 9  # msa_decode: seq-lens prefix sums, then the same 8
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attention_kernel_traffic.json")
 ATTN_SOURCES = ["attention.cu", "ptx.cuh", "common.cuh"]
 
@@ -242,8 +243,32 @@ def run_ours(args, rank, world):
     out = torch.empty((w.T, w.Hq, 128), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.T, w.Hq), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    decode = is_decode(w)
+    if decode:
+        # decode-shaped batches go through msa_decode: n tokens at the tail
+        # of every request, one call per step
+        n_dec = int(w.q_lens[0])
+        seq_lens_d = torch.tensor(w.seq_lens, dtype=torch.int32, device=dev)
+        ws_dec = torch.empty(msa.decode_workspace_bytes(
+            w.B, n_dec, w.Hq, w.Hkv, w.max_seqlen_k), dtype=torch.uint8,
+            device=dev)
+
+    def decode_step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        _, _, plan = msa.msa_decode(wd.q, wd.kv, w.q_scale, w.k_scale,
+                                    w.v_scale, w.softmax_scale, wd.topk,
+                                    wd.block_table, seq_lens_d, n_dec,
+                                    w.max_seqlen_k, workspace=ws_dec, out=out,
+                                    lse=lse, stream=stream)
+        if ev:
+            for e in ev[1:]:
+                e.record(stream)
+        return plan
 
     def step(ev=None):
+        if decode:
+            return decode_step(ev)
         if ev:
             ev[0].record(stream)
         plan = msa.msa_plan(wd.topk, wd.cu_q, wd.cu_k, wd.block_table,
@@ -300,9 +325,26 @@ def run_ours(args, rank, world):
         d2h = out_h.numel() * 2 + lse_h.numel() * 4
         e2e_steps = max(3, min(args.steps, 20))
 
+        if decode:
+            host["seq_lens"] = seq_lens_d.cpu().pin_memory()
+            dev_in["seq_lens"] = torch.empty_like(seq_lens_d)
+            h2d = sum(v.numel() * v.element_size() for k, v in host.items()
+                      if k not in ("cu_q", "cu_k"))
+
         def e2e_step():
             for k in host:
+                if decode and k in ("cu_q", "cu_k"):
+                    continue
                 dev_in[k].copy_(host[k], non_blocking=True)
+            if decode:
+                msa.msa_decode(dev_in["q"], dev_in["kv"], w.q_scale, w.k_scale,
+                               w.v_scale, w.softmax_scale, dev_in["topk"],
+                               dev_in["block_table"], dev_in["seq_lens"],
+                               n_dec, w.max_seqlen_k, workspace=ws_dec,
+                               out=out, lse=lse, stream=stream)
+                out_h.copy_(out, non_blocking=True)
+                lse_h.copy_(lse, non_blocking=True)
+                return
             p = msa.msa_plan(dev_in["topk"], dev_in["cu_q"], dev_in["cu_k"],
                              dev_in["block_table"], w.num_pages, w.Hq,
                              w.total_rows, w.max_seqlen_q, w.max_seqlen_k,
@@ -331,7 +373,7 @@ def run_ours(args, rank, world):
         [total_ms, attn_ms, comb_ms, plan_ms, step_ms,
          e2e["ms"] if e2e else 0.0], world, dev, "max")
     (job_pairs,) = reduce_over_ranks([float(pairs)], world, dev, "sum")
-    return dict(w=w, pairs=pairs, upages=upages, total_ms=total_ms,
+    return dict(w=w, decode=decode, pairs=pairs, upages=upages, total_ms=total_ms,
                 attn_ms=attn_ms, comb_ms=comb_ms, plan_ms=plan_ms,
                 step_ms=step_ms, e2e=e2e, e2e_ms=e2e_ms, clocks=clk,
                 job_pairs=job_pairs,
@@ -420,6 +462,10 @@ def run_reference(args, rank, world):
     return line
 
 
+def is_decode(w):
+    return w.name.startswith("decode")
+
+
 def config_of(w, args):
     return {"workload": "%s: %s" % (w.name, w.meta.get("description", "")),
             "T": w.T, "seq_lens": w.seq_lens if w.B <= 8 else "%d requests" % w.B,
@@ -449,12 +495,23 @@ def main():
         step_s = r["step_ms"] / 1e3
         value = job_tflops(r["job_pairs"], r["step_ms"])
         alg = algorithmic_bytes(w, r["upages"])
-        attn_s = r["attn_ms"] / 1e3
-        achieved = alg["attention"] / attn_s / 1e9
+        if r["decode"]:
+            # one msa_decode call per step: its kernels are not timed apart,
+            # so the roofline covers the whole call and the step's bytes
+            roof_bytes, roof_s, roof_kernel = alg["step"], step_s, "msa_decode (9 kernels)"
+            traffic = None
+            breakdown = {"decode": r["step_ms"] * 1e3}
+            launches = DECODE_KERNELS_PER_STEP * args.steps
+        else:
+            roof_bytes, roof_s, roof_kernel = alg["attention"], r["attn_ms"] / 1e3, "attention_kernel"
+            traffic = measured_traffic()
+            breakdown = {"plan": r["plan_ms"] * 1e3, "attention": r["attn_ms"] * 1e3,
+                         "combine": r["comb_ms"] * 1e3}
+            launches = KERNELS_PER_STEP * args.steps
+        achieved = roof_bytes / roof_s / 1e9
         fp8_peak = 2.0 * peaks["bf16_tflops"]
         t_hbm = alg["step"] / (peaks["hbm_gbs"] * 1e9)
         t_fp8 = flops / (fp8_peak * 1e12)
-        traffic = measured_traffic()
         line = {
             "metric": "selected-token attention TFLOP/s (and us per layer)",
             "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -463,15 +520,13 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
             "config": config_of(w, args),
-            "breakdown_us": {"plan": r["plan_ms"] * 1e3,
-                             "attention": r["attn_ms"] * 1e3,
-                             "combine": r["comb_ms"] * 1e3},
+            "breakdown_us": breakdown,
             "roofline": {"bound": "hbm", "achieved": achieved,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"],
                          "traffic": traffic,
-                         "kernel": "attention_kernel",
-                         "algorithmic_bytes": alg["attention"],
+                         "kernel": roof_kernel,
+                         "algorithmic_bytes": roof_bytes,
                          "peak_source": peaks["source"] + " (burst hbm_gbs)"},
             "roofline_step": {
                 "bound": "hbm" if t_hbm >= t_fp8 else "tensor",
@@ -481,7 +536,7 @@ def main():
                 "fp8_peak_tflops": fp8_peak,
                 "fp8_peak_source": "2 x measured bf16 burst"},
             "work": {"pairs": r["pairs"], "unique_kv_pages": r["upages"]},
-            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "gpu_launches": launches,
             "clocks": r["clocks"], "device_status": r["status"],
         }
         if r["e2e"]:

@@ -16,8 +16,10 @@ constexpr int kPage = MSA_PAGE_SIZE;  // tokens per KV page
 constexpr int kTopK = MSA_TOPK;       // pages per (token, KV head)
 constexpr int kTileM = 128;           // MMA rows per work item (tokens x G)
 
-// Rows per CTA in the plan's count / fill kernels.
+// Rows per CTA in the plan's fill kernel, and in its count kernel (a
+// half-warp per row there).
 constexpr int kPlanTile = 256;
+constexpr int kCountTile = 16;
 
 // Wall-time bound of every device-side wait (about a second).
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;

@@ -15,12 +15,13 @@
 //            one bit per kept page in the membership bitmap; the (token,
 //            KV head) list's 16 threads together write its slot mask.  This is the histogram, kept as bits: repeats
 //            collapse and the order of arrival cannot change the result.
-//   rows     one thread per row: row length (popcount of its words), the
-//            running count in front of every word, and per-tile sums of the
-//            lengths and of the chunk counts
+//   rows     a half-warp per row: row length (popcount of its words) and
+//            the running count in front of every word; per 16-row tile, the
+//            sums of the lengths and of the chunk counts
 //   scan     one CTA: exclusive scan of the tile sums
-//   emit     one thread per row: row_ptr, the row's first work item, and the
-//            work items / record headers of its chunks
+//   emit     one thread per row: row_ptr and the row's first work item;
+//            the work items / record headers of the CTA's rows dealt over
+//            all its threads
 //   scatter  one thread per top-k entry: each kept entry goes to
 //            row_ptr + (tokens of the same row before it), found in O(1)
 //            from the word prefix and a popcount; it also fills the token
@@ -217,43 +218,74 @@ __global__ void __launch_bounds__(256) plan_mark_kernel(PlanDev d) {
     d.slot_mask[w] = (uint16_t)((bal >> (lane & ~(kTopK - 1))) & 0xFFFFu);
 }
 
-// One thread per row, kPlanTile rows per CTA.  Rows are 16-byte aligned
-// (W is a multiple of 4), read and written four words at a time.
+// kCountTile rows per CTA, a half-warp per row: lane l of the half-warp
+// takes the 16-byte vectors [l * per, (l + 1) * per) of the row (rows are
+// 16-byte aligned, W a multiple of 4), so the row is read and written as
+// one contiguous span.  The running count in front of every word is the
+// lane's own popcounts plus an exclusive scan over the 16 lanes.  The CTA's
+// sums of the row lengths and chunk counts go to tile_sums.
 __global__ void __launch_bounds__(kPlanTile) plan_rows_kernel(PlanDev d) {
   pdl_wait();
   pdl_trigger();
-  const int64_t r = (int64_t)blockIdx.x * kPlanTile + threadIdx.x;
-  const bool ok = d.counters[2] == 1;
-  int c = 0;
-  if (ok && r < d.rows) {
-    const uint4* __restrict__ words =
-        reinterpret_cast<const uint4*>(d.bitmap + r * d.W);
-    int4* __restrict__ pre = reinterpret_cast<int4*>(d.word_pre + r * d.W);
-    const int nv = d.W >> 2;
-    for (int x0 = 0; x0 < nv; x0 += 4) {
+  static_assert(kPlanTile == 16 * kCountTile, "a half-warp per row");
+  __shared__ int s_c[kCountTile], s_w[kCountTile];
+  const int sub = threadIdx.x & 15, k = threadIdx.x >> 4;
+  const int64_t r = (int64_t)blockIdx.x * kCountTile + k;
+  const bool live = d.counters[2] == 1 && r < d.rows;
+  const int nv = d.W >> 2;
+  const int per = (nv + 15) >> 4;
+  const uint4* __restrict__ words = reinterpret_cast<const uint4*>(d.bitmap + r * d.W);
+  int own = 0;
+  if (live) {
+    for (int u0 = 0; u0 < per; u0 += 4) {
       uint4 v[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (x0 + u < nv) v[u] = words[x0 + u];
-#pragma unroll
       for (int u = 0; u < 4; ++u) {
-        if (x0 + u < nv) {
-          int4 o;
-          o.x = c; c += __popc(v[u].x);
-          o.y = c; c += __popc(v[u].y);
-          o.z = c; c += __popc(v[u].z);
-          o.w = c; c += __popc(v[u].w);
-          pre[x0 + u] = o;
-        }
+        const int x = sub * per + u0 + u;
+        v[u] = (u0 + u < per && x < nv) ? words[x] : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        own += __popc(v[u].x) + __popc(v[u].y) + __popc(v[u].z) + __popc(v[u].w);
+    }
+  }
+  // inclusive scan over the half-warp (all 32 lanes take part)
+  int incl = own;
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o, 16);
+    if (sub >= o) incl += n;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 15, 16);
+  if (live) {
+    int4* __restrict__ pre = reinterpret_cast<int4*>(d.word_pre + r * d.W);
+    int run = incl - own;
+    for (int u = 0; u < per; ++u) {
+      const int x = sub * per + u;
+      if (x < nv) {
+        const uint4 v = words[x];
+        int4 o;
+        o.x = run; run += __popc(v.x);
+        o.y = run; run += __popc(v.y);
+        o.z = run; run += __popc(v.z);
+        o.w = run; run += __popc(v.w);
+        pre[x] = o;
       }
     }
-    d.row_cnt[r] = c;
+    if (sub == 0) d.row_cnt[r] = total;
   }
-  const int chunks = (c + d.C - 1) / d.C;
-  int tc, tw;
-  block_excl_scan<kPlanTile>(c, &tc);
-  block_excl_scan<kPlanTile>(chunks, &tw);
+  if (sub == 0) {
+    s_c[k] = live ? total : 0;
+    s_w[k] = live ? (total + d.C - 1) / d.C : 0;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
+    int tc = 0, tw = 0;
+#pragma unroll
+    for (int i = 0; i < kCountTile; ++i) {
+      tc += s_c[i];
+      tw += s_w[i];
+    }
     d.tile_sums[blockIdx.x] = tc;
     d.tile_sums[d.ntiles + blockIdx.x] = tw;
   }
@@ -280,9 +312,19 @@ __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(PlanDev d) {
   }
 }
 
+// kPlanTile rows per CTA.  One thread per row finds the row's offsets (the
+// scanned sums of the count tiles in front of the CTA plus a block scan)
+// and its page; then the CTA's chunks are dealt to all its threads, each
+// finding its row by a search over the rows' first chunks, so a row with
+// many chunks does not serialise on one thread.
 __global__ void __launch_bounds__(kPlanTile) plan_emit_kernel(PlanDev d) {
   pdl_wait();
   pdl_trigger();
+  __shared__ int s_wex[kPlanTile];     // first chunk of the row, within the CTA
+  __shared__ int s_start[kPlanTile];   // first CSR entry of the row
+  __shared__ int s_cnt[kPlanTile];
+  __shared__ int4 s_hdr[kPlanTile];    // record header without the count
+  __shared__ int2 s_item[kPlanTile];   // work item: request, (KV head, page)
   const int64_t r = (int64_t)blockIdx.x * kPlanTile + threadIdx.x;
   const bool ok = d.counters[2] == 1;
   const int c = (ok && r < d.rows) ? d.row_cnt[r] : 0;
@@ -290,25 +332,38 @@ __global__ void __launch_bounds__(kPlanTile) plan_emit_kernel(PlanDev d) {
   int tc, tw;
   const int ex_c = block_excl_scan<kPlanTile>(c, &tc);
   const int ex_w = block_excl_scan<kPlanTile>(chunks, &tw);
-  if (r >= d.rows) return;
-  const int start = d.tile_sums[blockIdx.x] + ex_c;
-  const int wstart = d.tile_sums[d.ntiles + blockIdx.x] + ex_w;
-  d.row_ptr[r] = start;
-  d.row_wptr[r] = wstart;
-  if (c == 0) return;
-  const int h = (int)(r / d.total_rows);
-  const int64_t rr = r - (int64_t)h * d.total_rows;
-  const int b = upper_index(d.req_off, d.B, rr);
-  const int p = (int)(rr - d.req_off[b]);
-  const int32_t phys = d.block_table[(int64_t)b * d.bt_stride + p];
-  for (int ch = 0; ch < chunks; ++ch) {
-    const int n = min(d.C, c - ch * d.C);
-    reinterpret_cast<int4*>(d.work)[wstart + ch] =
-        make_int4(start + ch * d.C, n, b, (h << 24) | p);
-    // record header: KV tile row of the pool, token count, first key
-    // position of the page, first query head of the KV head
-    d.records[(int64_t)(wstart + ch) * d.rec_stride] =
-        make_int4((phys * d.Hkv + h) * kPage, n, p * kPage, h * d.G);
+  const int tile0 = blockIdx.x * (kPlanTile / kCountTile);
+  const int base_c = d.tile_sums[tile0];
+  const int base_w = d.tile_sums[d.ntiles + tile0];
+  s_wex[threadIdx.x] = ex_w;
+  s_start[threadIdx.x] = base_c + ex_c;
+  s_cnt[threadIdx.x] = c;
+  if (r < d.rows) {
+    d.row_ptr[r] = base_c + ex_c;
+    d.row_wptr[r] = base_w + ex_w;
+    if (c > 0) {
+      const int h = (int)(r / d.total_rows);
+      const int64_t rr = r - (int64_t)h * d.total_rows;
+      const int b = upper_index(d.req_off, d.B, rr);
+      const int p = (int)(rr - d.req_off[b]);
+      const int32_t phys = d.block_table[(int64_t)b * d.bt_stride + p];
+      // record header: KV tile row of the pool, (token count), first key
+      // position of the page, first query head of the KV head
+      s_hdr[threadIdx.x] = make_int4((phys * d.Hkv + h) * kPage, 0, p * kPage, h * d.G);
+      s_item[threadIdx.x] = make_int2(b, (h << 24) | p);
+    }
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < tw; k += kPlanTile) {
+    const int j = upper_index(s_wex, kPlanTile, k);  // last row starting at or before k
+    const int ch = k - s_wex[j];
+    const int n = min(d.C, s_cnt[j] - ch * d.C);
+    const int64_t wi = (int64_t)base_w + k;
+    reinterpret_cast<int4*>(d.work)[wi] =
+        make_int4(s_start[j] + ch * d.C, n, s_item[j].x, s_item[j].y);
+    int4 hdr = s_hdr[j];
+    hdr.y = n;
+    d.records[wi * d.rec_stride] = hdr;
   }
 }
 
@@ -364,7 +419,7 @@ cudaError_t launch_plan(const msa_plan_t& pl, const int32_t* topk,
   d.row_cnt = pl.row_cnt;
   d.row_wptr = pl.row_wptr;
   d.tile_sums = pl.tile_sums;
-  d.ntiles = (int)ceil_div(pl.rows, kPlanTile);
+  d.ntiles = (int)ceil_div(pl.rows, kCountTile);
   d.row_ptr = pl.row_ptr;
   d.q_idx = pl.q_idx;
   d.slot = pl.slot;
@@ -388,10 +443,11 @@ cudaError_t launch_plan(const msa_plan_t& pl, const int32_t* topk,
     e = launch_pdl(plan_mark_kernel, mgrid, 256, 0, stream, d);
   if (e == cudaSuccess && d.ntiles > 0)
     e = launch_pdl(plan_rows_kernel, (unsigned)d.ntiles, kPlanTile, 0, stream, d);
+  const unsigned egrid = (unsigned)ceil_div(pl.rows, kPlanTile);
   if (e == cudaSuccess)
     e = launch_pdl(plan_scan_kernel, 1u, kScanThreads, 0, stream, d);
-  if (e == cudaSuccess && d.ntiles > 0)
-    e = launch_pdl(plan_emit_kernel, (unsigned)d.ntiles, kPlanTile, 0, stream, d);
+  if (e == cudaSuccess && egrid > 0)
+    e = launch_pdl(plan_emit_kernel, egrid, kPlanTile, 0, stream, d);
   if (e == cudaSuccess && marks > 0)
     e = launch_pdl(plan_scatter_kernel, mgrid, 256, 0, stream, d);
   return e;
