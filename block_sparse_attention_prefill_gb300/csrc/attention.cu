@@ -592,10 +592,13 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
               o[e] = *reinterpret_cast<uint32_t*>(&a2);
               o[16 + e] = *reinterpret_cast<uint32_t*>(&b2);
             }
-            uint4* d4 = reinterpret_cast<uint4*>(dst + half * 64);
+            // whole 32-byte sectors: the row's half is 128 bytes at a
+            // 128-byte aligned offset of a 256-byte row
+            uint16_t* d = dst + half * 64;
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              d4[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            for (int q = 0; q < 4; ++q)
+              st_global_v8(d + 16 * q, o[8 * q], o[8 * q + 1], o[8 * q + 2], o[8 * q + 3],
+                           o[8 * q + 4], o[8 * q + 5], o[8 * q + 6], o[8 * q + 7]);
           }
         }
         if (valid) p.part_lse[mt.prow] = mt.lse;
