@@ -107,7 +107,8 @@ struct Params {
   const int4* records;
   int rec_stride;  // int4 per record
   const int32_t* counters;
-  uint16_t* part_o;
+  uint8_t* part_o;      // E4M3 partial rows, V's code units
+  float* part_vscale;   // the combine's copy of v_scale
   float* part_lse;
   uint32_t* status;
   int Hq, G;
@@ -134,6 +135,14 @@ __device__ __forceinline__ int row_rotation(int li, int G) {
 // p = 2^(x * c + off) for 32 score columns, packed to E4M3 in pairs and
 // stored as two 16-byte chunks of the 128-byte-swizzled P row; returns the
 // sum of the (unrounded) probabilities.  kMask: columns past kv_lim are 0.
+// Four floats rounded to E4M3 (nearest even, saturating) in one word, the
+// first in the low byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
 template <bool kMask>
 __device__ __forceinline__ float exp_pack32(const uint32_t (&r)[32], int col0,
                                             int kv_lim, float c, float off,
@@ -191,6 +200,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
   // one in the stream
   pdl_wait();
   pdl_trigger();
+  if (blockIdx.x == 0 && threadIdx.x == 0) *p.part_vscale = p.v_scale;
   const int num_work = p.counters[1];
   // work items are dealt round-robin: CTA b takes items b, b + grid, ...
   // Items of one heavily selected KV row are adjacent in the work list, so
@@ -538,7 +548,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       }
       RowMeta mt;
       mt.prow = prow;
-      mt.inv = l > 0.f ? p.v_scale / l : 0.f;
+      mt.inv = l > 0.f ? 1.f / l : 0.f;  // O in V's code units; the combine scales
       mt.lse = l > 0.f ? (m2 + __log2f(l) - 8.f) * 0.69314718055994530942f
                        : -INFINITY;
       meta[(li % kMetaSlots) * kTileM + row] = mt;
@@ -571,7 +581,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       tc_fence_after();
       if (warp_valid) {
         const uint32_t o_tmem = tmem + lane_off + (uint32_t)(w * 256 + 128);
-        uint16_t* dst = p.part_o + mt.prow * (int64_t)kD;
+        uint8_t* dst = p.part_o + mt.prow * (int64_t)kD;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t ra[32], rb[32];
@@ -580,25 +590,26 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
           tmem_ld32(o_tmem + half * 64 + 32, rb);
           tmem_wait_ld();
           if (valid) {
-            uint32_t o[32];
+            // the normalised row in V's code units is a convex combination
+            // of E4M3 V codes, so it stays within E4M3's range; word k holds
+            // columns 4k .. 4k+3 of this half
+            uint32_t o[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              __nv_bfloat162 a2 = __floats2bfloat162_rn(
-                  __uint_as_float(ra[2 * e]) * mt.inv,
-                  __uint_as_float(ra[2 * e + 1]) * mt.inv);
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(
-                  __uint_as_float(rb[2 * e]) * mt.inv,
-                  __uint_as_float(rb[2 * e + 1]) * mt.inv);
-              o[e] = *reinterpret_cast<uint32_t*>(&a2);
-              o[16 + e] = *reinterpret_cast<uint32_t*>(&b2);
+            for (int k = 0; k < 8; ++k) {
+              o[k] = pack_e4m3x4(__uint_as_float(ra[4 * k]) * mt.inv,
+                                 __uint_as_float(ra[4 * k + 1]) * mt.inv,
+                                 __uint_as_float(ra[4 * k + 2]) * mt.inv,
+                                 __uint_as_float(ra[4 * k + 3]) * mt.inv);
+              o[8 + k] = pack_e4m3x4(__uint_as_float(rb[4 * k]) * mt.inv,
+                                     __uint_as_float(rb[4 * k + 1]) * mt.inv,
+                                     __uint_as_float(rb[4 * k + 2]) * mt.inv,
+                                     __uint_as_float(rb[4 * k + 3]) * mt.inv);
             }
-            // whole 32-byte sectors: the row's half is 128 bytes at a
-            // 128-byte aligned offset of a 256-byte row
-            uint16_t* d = dst + half * 64;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              st_global_v8(d + 16 * q, o[8 * q], o[8 * q + 1], o[8 * q + 2], o[8 * q + 3],
-                           o[8 * q + 4], o[8 * q + 5], o[8 * q + 6], o[8 * q + 7]);
+            // whole 32-byte sectors: the row's half is 64 bytes at a
+            // 64-byte aligned offset of a 128-byte row
+            uint8_t* d = dst + half * 64;
+            st_global_v8(d, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
+            st_global_v8(d + 32, o[8], o[9], o[10], o[11], o[12], o[13], o[14], o[15]);
           }
         }
         if (valid) p.part_lse[mt.prow] = mt.lse;
@@ -680,6 +691,7 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   p.rec_stride = (int)(pl.record_bytes / 16);
   p.counters = pl.counters;
   p.part_o = a.part_o;
+  p.part_vscale = a.part_vscale;
   p.part_lse = a.part_lse;
   p.status = pl.status;
   p.Hq = (int)pl.Hq;

@@ -8,6 +8,8 @@
 // HBM-bound: one warp per row, each lane owns 4 of the 128 columns, so a
 // partial row is one coalesced 256 B (bf16) or 512 B (fp32) read.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 
@@ -88,12 +90,15 @@ combine_kernel(const TIn* __restrict__ part_o, const float* __restrict__ part_ls
 }
 
 // The attention path's combine: 16 slots per row, the slot mask of the
-// row's (token, KV head) says which slots hold a partial.  A half-warp per
-// row, each lane owning 8 of the 128 columns: one 16-byte load per slot,
-// all of a row's loads issued before any is used.
+// row's (token, KV head) says which slots hold a partial.  Partial rows are
+// E4M3 in V's code units (128 bytes); the V scale is applied here, read from
+// the device scalar the attention kernel left.  A half-warp per row, each
+// lane owning 8 of the 128 columns: one 8-byte load per slot, all of a row's
+// loads issued before any is used.
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
-combine16_kernel(const __nv_bfloat16* __restrict__ part_o,
+combine16_kernel(const uint8_t* __restrict__ part_o,
                  const float* __restrict__ part_lse,
+                 const float* __restrict__ v_scale_ptr,
                  const uint16_t* __restrict__ slot_mask, int64_t group,
                  int64_t rows, uint16_t* __restrict__ out,
                  float* __restrict__ lse_out) {
@@ -105,14 +110,14 @@ combine16_kernel(const __nv_bfloat16* __restrict__ part_o,
                     (lane >> 4);
   const bool live = r < rows;
   const uint32_t mask = live ? slot_mask[r / group] : 0u;
-  const __nv_bfloat16* base = part_o + r * (int64_t)kTopK * kD + sub * 8;
-  uint4 v[kTopK];
+  const uint8_t* base = part_o + r * (int64_t)kTopK * kD + sub * 8;
+  uint2 v[kTopK];
 #pragma unroll
   for (int j = 0; j < kTopK; ++j) {
     if ((mask >> j) & 1u)
-      v[j] = *reinterpret_cast<const uint4*>(base + j * kD);
+      v[j] = *reinterpret_cast<const uint2*>(base + j * kD);
     else
-      v[j] = make_uint4(0u, 0u, 0u, 0u);
+      v[j] = make_uint2(0u, 0u);
   }
   // lane `sub` of the half-warp holds slot sub's lse
   float l = -INFINITY;
@@ -131,24 +136,30 @@ combine16_kernel(const __nv_bfloat16* __restrict__ part_o,
     if (lse_out && sub == 0) lse_out[r] = -INFINITY;
     return;
   }
-  const float inv = 1.f / sum;
+  const float inv = *v_scale_ptr / sum;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int j = 0; j < kTopK; ++j) {
-    const float wj = __shfl_sync(0xffffffffu, wl, (lane & 16) + j) * inv;
-    const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+    const float wj = __shfl_sync(0xffffffffu, wl, (lane & 16) + j);
+    const uint32_t w2[2] = {v[j].x, v[j].y};
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float2 f = __bfloat1622float2(
-          *reinterpret_cast<const __nv_bfloat162*>(&w4[u]));
-      acc[2 * u] = fmaf(wj, f.x, acc[2 * u]);
-      acc[2 * u + 1] = fmaf(wj, f.y, acc[2 * u + 1]);
+    for (int u = 0; u < 2; ++u) {
+      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
+          (__nv_fp8x2_storage_t)(w2[u] & 0xFFFFu), __NV_E4M3);
+      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
+          (__nv_fp8x2_storage_t)(w2[u] >> 16), __NV_E4M3);
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+      acc[4 * u + 0] = fmaf(wj, a.x, acc[4 * u + 0]);
+      acc[4 * u + 1] = fmaf(wj, a.y, acc[4 * u + 1]);
+      acc[4 * u + 2] = fmaf(wj, b.x, acc[4 * u + 2]);
+      acc[4 * u + 3] = fmaf(wj, b.y, acc[4 * u + 3]);
     }
   }
   uint32_t o[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * u], acc[2 * u + 1]);
+    __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * u] * inv, acc[2 * u + 1] * inv);
     o[u] = *reinterpret_cast<uint32_t*>(&h);
   }
   *dst = make_uint4(o[0], o[1], o[2], o[3]);
@@ -200,32 +211,32 @@ decode_seqlens_kernel(const int32_t* seq_lens, int64_t B, int64_t n,
 }  // namespace
 
 cudaError_t launch_combine(const void* part_o, int part_dtype,
-                           const float* part_lse, const uint16_t* slot_mask,
-                           int64_t group, int64_t rows, int64_t splits,
+                           const float* part_lse, int64_t rows, int64_t splits,
                            uint16_t* out, float* lse, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
-  const unsigned grid = (unsigned)ceil_div(rows, kWarpsPerBlock);
-  const int S = (int)splits;
+  const dim3 grid((unsigned)ceil_div(rows, kWarpsPerBlock));
   const dim3 block(kWarpsPerBlock * 32);
   const uint16_t* no_mask = nullptr;
   const int64_t one = 1;
-  if (part_dtype == MSA_DTYPE_BF16) {
-    auto po = static_cast<const __nv_bfloat16*>(part_o);
-    if (slot_mask && S == kTopK)
-      return launch_pdl(combine16_kernel, dim3((unsigned)ceil_div(rows, 2 * kWarpsPerBlock)),
-                        block, 0, stream, po, part_lse, slot_mask, group, rows, out, lse);
-    if (slot_mask)
-      return launch_pdl(combine_kernel<__nv_bfloat16, true>, dim3(grid), block, 0, stream,
-                        po, part_lse, slot_mask, group, rows, S, out, lse);
-    return launch_pdl(combine_kernel<__nv_bfloat16, false>, dim3(grid), block, 0, stream,
-                      po, part_lse, no_mask, one, rows, S, out, lse);
-  }
-  auto po = static_cast<const float*>(part_o);
-  if (slot_mask)
-    return launch_pdl(combine_kernel<float, true>, dim3(grid), block, 0, stream, po,
-                      part_lse, slot_mask, group, rows, S, out, lse);
-  return launch_pdl(combine_kernel<float, false>, dim3(grid), block, 0, stream, po,
-                    part_lse, no_mask, one, rows, S, out, lse);
+  const int S = (int)splits;
+  if (part_dtype == MSA_DTYPE_BF16)
+    return launch_pdl(combine_kernel<__nv_bfloat16, false>, grid, block, 0, stream,
+                      static_cast<const __nv_bfloat16*>(part_o), part_lse, no_mask,
+                      one, rows, S, out, lse);
+  return launch_pdl(combine_kernel<float, false>, grid, block, 0, stream,
+                    static_cast<const float*>(part_o), part_lse, no_mask, one, rows,
+                    S, out, lse);
+}
+
+cudaError_t launch_combine_attn(const uint8_t* part_o, const float* part_lse,
+                                const float* v_scale, const uint16_t* slot_mask,
+                                int64_t group, int64_t rows, uint16_t* out,
+                                float* lse, cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  return launch_pdl(combine16_kernel,
+                    dim3((unsigned)ceil_div(rows, 2 * kWarpsPerBlock)),
+                    dim3(kWarpsPerBlock * 32), 0, stream, part_o, part_lse, v_scale,
+                    slot_mask, group, rows, out, lse);
 }
 
 cudaError_t launch_decode_seqlens(const int32_t* seq_lens, int64_t B,

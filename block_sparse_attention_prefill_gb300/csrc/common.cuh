@@ -41,18 +41,27 @@ struct AttnArgs {
   const int32_t* block_table;
   int64_t bt_stride;
   const msa_plan_t* plan;
-  uint16_t* part_o;   // [T][Hq][16][128] bf16, normalised partial outputs
+  uint8_t* part_o;    // [T][Hq][16][128] E4M3: normalised partial outputs in
+                      // V's code units (a convex combination of V codes)
   float* part_lse;    // [T][Hq][16]
+  float* part_vscale; // one float: v_scale, left here for the combine
 };
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
 
-// Combine over `splits` partials per row.  With slot_mask != nullptr, the
-// mask of row r is slot_mask[r / group] and empty slots are not read.
+// Combine over `splits` caller-given partials per row (bf16 or fp32 O,
+// [rows][splits][128], lse [rows][splits], -inf marking an empty split).
 cudaError_t launch_combine(const void* part_o, int part_dtype,
-                           const float* part_lse, const uint16_t* slot_mask,
-                           int64_t group, int64_t rows, int64_t splits,
+                           const float* part_lse, int64_t rows, int64_t splits,
                            uint16_t* out, float* lse, cudaStream_t stream);
+
+// Combine of the attention kernel's partials: 16 slots per row, E4M3 O in
+// V's code units scaled by *v_scale, the mask of row r is
+// slot_mask[r / group] and empty slots are not read.
+cudaError_t launch_combine_attn(const uint8_t* part_o, const float* part_lse,
+                                const float* v_scale, const uint16_t* slot_mask,
+                                int64_t group, int64_t rows, uint16_t* out,
+                                float* lse, cudaStream_t stream);
 
 cudaError_t launch_decode_seqlens(const int32_t* seq_lens, int64_t B,
                                   int64_t n, int32_t* cu_q, int32_t* cu_k,

@@ -117,13 +117,15 @@ size_t plan_layout(const PlanShape& s, void* base, msa_plan_t* pl) {
   return c.off;
 }
 
-size_t prefill_layout(int64_t T, int64_t Hq, void* base, uint16_t** part_o,
-                      float** part_lse) {
+size_t prefill_layout(int64_t T, int64_t Hq, void* base, uint8_t** part_o,
+                      float** part_lse, float** part_vscale) {
   Carver c(base);
-  uint16_t* po = c.take<uint16_t>(T * Hq * kTopK * kD);
+  float* vs = c.take<float>(1);
+  uint8_t* po = c.take<uint8_t>(T * Hq * kTopK * kD);
   float* pl = c.take<float>(T * Hq * kTopK);
   if (part_o) *part_o = po;
   if (part_lse) *part_lse = pl;
+  if (part_vscale) *part_vscale = vs;
   return c.off;
 }
 
@@ -192,7 +194,7 @@ int attention_impl(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
       !(softmax_scale > 0.f) || !std::isfinite(q_scale * k_scale * softmax_scale))
     return MSA_ERR_SHAPE;
   if (!aligned(q, 16) || !aligned(kv, 16)) return MSA_ERR_ALIGN;
-  const size_t need = prefill_layout(T, Hq, nullptr, nullptr, nullptr);
+  const size_t need = prefill_layout(T, Hq, nullptr, nullptr, nullptr, nullptr);
   if (!ws || ws_bytes < need) return MSA_ERR_WORKSPACE;
   if (!aligned(ws, kAlign)) return MSA_ERR_ALIGN;
   AttnArgs a;
@@ -205,7 +207,7 @@ int attention_impl(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
   a.block_table = block_table;
   a.bt_stride = bt_stride;
   a.plan = plan;
-  prefill_layout(T, Hq, ws, &a.part_o, &a.part_lse);
+  prefill_layout(T, Hq, ws, &a.part_o, &a.part_lse, &a.part_vscale);
   if (num_pages == 0) return MSA_OK;
   return cuda_rc(launch_attention(a, stream));
 }
@@ -217,15 +219,15 @@ int prefill_combine_impl(const msa_plan_t* plan, void* ws, size_t ws_bytes,
   if (T == 0) return MSA_OK;
   if (!out) return MSA_ERR_NULL;
   if (!aligned(out, 8) || !aligned(lse, 4)) return MSA_ERR_ALIGN;
-  const size_t need = prefill_layout(T, Hq, nullptr, nullptr, nullptr);
+  const size_t need = prefill_layout(T, Hq, nullptr, nullptr, nullptr, nullptr);
   if (!ws || ws_bytes < need) return MSA_ERR_WORKSPACE;
   if (!aligned(ws, kAlign)) return MSA_ERR_ALIGN;
-  uint16_t* part_o;
+  uint8_t* part_o;
   float* part_lse;
-  prefill_layout(T, Hq, ws, &part_o, &part_lse);
-  return cuda_rc(launch_combine(part_o, MSA_DTYPE_BF16, part_lse,
-                                plan->slot_mask, Hq / plan->Hkv, T * Hq, kTopK,
-                                out, lse, stream));
+  float* part_vscale;
+  prefill_layout(T, Hq, ws, &part_o, &part_lse, &part_vscale);
+  return cuda_rc(launch_combine_attn(part_o, part_lse, part_vscale, plan->slot_mask,
+                                     Hq / plan->Hkv, T * Hq, out, lse, stream));
 }
 
 int prefill_impl(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
@@ -261,7 +263,7 @@ int decode_layout(int64_t B, int64_t n, int64_t Hq, int64_t Hkv,
   if (rc) return rc;
   d->cu_bytes = align_up(2 * (size_t)(B + 1) * sizeof(int32_t));
   d->plan_bytes = plan_layout(s, nullptr, nullptr);
-  d->prefill_bytes = prefill_layout(B * n, Hq, nullptr, nullptr, nullptr);
+  d->prefill_bytes = prefill_layout(B * n, Hq, nullptr, nullptr, nullptr, nullptr);
   d->total = d->cu_bytes + d->plan_bytes + d->prefill_bytes;
   return MSA_OK;
 }
@@ -316,7 +318,7 @@ int msa_plan(const int32_t* topk, const int32_t* cu_seqlens_q,
 int msa_prefill_workspace_bytes(int64_t T, int64_t Hq, size_t* bytes) {
   if (!bytes) return MSA_ERR_NULL;
   if (T < 0 || Hq <= 0 || T * Hq >= kI32Max / kTopK) return MSA_ERR_SHAPE;
-  *bytes = prefill_layout(T, Hq, nullptr, nullptr, nullptr);
+  *bytes = prefill_layout(T, Hq, nullptr, nullptr, nullptr, nullptr);
   return MSA_OK;
 }
 
@@ -362,7 +364,7 @@ int msa_combine(const void* part_o, int part_dtype, const float* part_lse,
   if (!aligned(part_o, part_dtype == MSA_DTYPE_F32 ? 16 : 8) ||
       !aligned(part_lse, 4) || !aligned(out, 8) || !aligned(lse_out, 4))
     return MSA_ERR_ALIGN;
-  return cuda_rc(launch_combine(part_o, part_dtype, part_lse, nullptr, 1, rows,
+  return cuda_rc(launch_combine(part_o, part_dtype, part_lse, rows,
                                 splits, out, lse_out,
                                 static_cast<cudaStream_t>(stream)));
 }

@@ -178,7 +178,7 @@ MSA_API int msa_plan(const int32_t *topk, const int32_t *cu_seqlens_q,
 
 /*
  * Bytes of device workspace msa_prefill() needs: the split partials,
- * T * Hq * 16 * (128 bf16 + 1 fp32).
+ * T * Hq * 16 * (128 E4M3 bytes + 1 fp32), plus the V scale for the combine.
  */
 MSA_API int msa_prefill_workspace_bytes(int64_t T, int64_t Hq, size_t *bytes);
 
@@ -216,8 +216,10 @@ MSA_API int msa_prefill(const uint8_t *q, const uint8_t *kv, int64_t num_pages,
  * separately; msa_prefill(...) is exactly msa_prefill_attention(...)
  * followed by msa_prefill_combine(...) on the same workspace.
  *   msa_prefill_attention: the attention kernel only; writes the split
- *     partials (normalised O as bf16, lse as fp32, one per token, query head
- *     and top-k slot) into `workspace`.  Arguments as in msa_prefill.
+ *     partials into `workspace`: one per token, query head and top-k slot,
+ *     the normalised O in E4M3 in V's code units (a convex combination of
+ *     E4M3 V codes, so always in range) and the lse in fp32, plus v_scale.
+ *     Arguments as in msa_prefill.
  *   msa_prefill_combine: merges the partials that msa_prefill_attention left
  *     in `workspace` (slots the plan marked empty are skipped) into out / lse.
  */

@@ -1,0 +1,101 @@
+"""Error budget of the split partials (CPU, no GPU).
+
+The attention kernel keeps each per-page partial output, normalised by its
+own softmax sum, in E4M3 in the code units of V, and the combine applies
+v_scale.  In those units the partial is a convex combination of E4M3 V codes,
+so it stays inside E4M3's range.  This test restates the per-page arithmetic
+in float64:
+
+- P = 2^(x*c - m*c + 8) rounded to E4M3;
+- l summed unrounded;
+- O = P.V / l, rounded to E4M3;
+- lse = (m*c + log2 l - 8) * ln 2.
+
+It then merges the pages by log-sum-exp (vLLM PR 60684, Performance: the
+combine step) and checks the result against exact masked softmax attention
+over the selected keys, under the acceptance rule of vLLM PR 60684,
+Validation.  bf16 partials are run alongside as the reference point.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from tolerance import acceptance
+
+
+def _dec(x):
+    return torch.as_tensor(x).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def _e4m3(x):
+    x = np.clip(x, -448.0, 448.0)
+    return torch.as_tensor(x).to(torch.float32).to(torch.float8_e4m3fn).to(
+        torch.float64).numpy()
+
+
+def _bf16(x):
+    return torch.as_tensor(x).to(torch.float32).to(torch.bfloat16).to(
+        torch.float64).numpy()
+
+
+def _run(w, tokens):
+    q = _dec(w.q.numpy())
+    kv = _dec(w.kv.numpy())
+    topk, bt = w.topk.numpy(), w.block_table.numpy()
+    cu_q, cu_k = w.cu_q.numpy(), w.cu_k.numpy()
+    G = w.Hq // w.Hkv
+    c = w.q_scale * w.k_scale * w.softmax_scale * np.log2(np.e)
+    ref, out_e4m3, out_bf16, max_code = [], [], [], 0.0
+    for t in tokens:
+        b = int(np.searchsorted(cu_q, t, side="right") - 1)
+        ql, sl = cu_q[b + 1] - cu_q[b], cu_k[b + 1] - cu_k[b]
+        pos = sl - ql + (t - cu_q[b])
+        npg = (sl + 127) // 128
+        for hq in range(w.Hq):
+            h = hq // G
+            pages = []
+            for p in topk[t, h]:
+                if 0 <= p < npg and p <= pos // 128 and p not in pages:
+                    pages.append(int(p))
+            lse, o8, o16, s_all, v_all = [], [], [], [], []
+            for p in pages:
+                k_codes = kv[bt[b, p], h, :, :128]
+                v_codes = kv[bt[b, p], h, :, 128:]
+                nk = min(128, pos - p * 128 + 1)
+                x = k_codes[:nk] @ q[t, hq]
+                s_all.append(x * w.q_scale * w.k_scale * w.softmax_scale)
+                v_all.append(v_codes[:nk] * w.v_scale)
+                m2 = x.max() * c
+                pr = np.exp2(x * c - m2 + 8.0)
+                l = pr.sum()
+                o = (_e4m3(pr) @ v_codes[:nk]) / l
+                max_code = max(max_code, float(np.abs(o).max()))
+                lse.append((m2 + np.log2(l) - 8.0) * np.log(2.0))
+                o8.append(_e4m3(o) * w.v_scale)
+                o16.append(_bf16(o * w.v_scale))
+            s = np.concatenate(s_all)
+            e = np.exp(s - s.max())
+            ref.append((e / e.sum()) @ np.concatenate(v_all))
+            lse = np.array(lse)
+            wt = np.exp(lse - lse.max())
+            wt /= wt.sum()
+            out_e4m3.append(_bf16(wt @ np.array(o8)))
+            out_bf16.append(_bf16(wt @ np.array(o16)))
+    return np.array(ref), np.array(out_e4m3), np.array(out_bf16), max_code
+
+
+@pytest.mark.parametrize("q_len,seq_len,seed", [(256, 4096, 0), (96, 16384, 3)])
+def test_e4m3_partials_within_acceptance(q_len, seq_len, seed):
+    w = workloads.make_batch("partials", [q_len], [seq_len], 16, 2, seed)
+    tokens = np.random.default_rng(seed).choice(q_len, size=24, replace=False)
+    ref, o8, o16, max_code = _run(w, tokens)
+    # the partial in V's code units never leaves E4M3's range
+    assert max_code <= 448.0
+    s8 = acceptance(o8, ref)
+    s16 = acceptance(o16, ref)
+    assert s8["ok"] and s16["ok"], (s8, s16)
+    # E4M3 rounding of the partials costs accuracy, but far less than the
+    # rule allows: no element outside it, errors well under its 0.05 atol
+    assert s8["outside"] == 0
+    assert s8["max_abs"] < 0.03
