@@ -48,7 +48,8 @@ def test_workspace_sizes(lib):
     a = msa.plan_workspace_bytes(1, 2048, 16, 2, 8192, 2048)
     b = msa.plan_workspace_bytes(1, 4096, 16, 2, 8192, 4096)
     assert 0 < a < b
-    assert msa.prefill_workspace_bytes(2048, 16) >= 2048 * 16 * 16 * (256 + 4)
+    # per (token, query head, slot): 128 E4M3 bytes of O and a 4-byte lse
+    assert msa.prefill_workspace_bytes(2048, 16) >= 2048 * 16 * 16 * (128 + 4)
     assert msa.decode_workspace_bytes(64, 8, 16, 2, 131072) > 0
 
 
