@@ -113,6 +113,8 @@ struct Params {
   uint32_t* status;
   int Hq, G;
   int q_tma;       // 1: Q rows by TMA (G % 8 == 0), 0: by cp.async
+  int rotate;      // 1: an item's rows rotate by (item % 4) * 32 (G divides 32)
+  float inv_G;     // 1 / G, for div_G
   float score_log2;
   float v_scale;
 };
@@ -128,8 +130,15 @@ __device__ __forceinline__ void set_timeout(Barriers* bars, uint32_t* status) {
 // from one item to the next.  Only for G dividing 32: then a token's G rows
 // start at a multiple of G and never straddle the end of the tile (a TMA
 // box does not wrap around).
-__device__ __forceinline__ int row_rotation(int li, int G) {
-  return (G <= 32 && 32 % G == 0) ? (li & 3) * 32 : 0;
+__device__ __forceinline__ int row_rotation(int li, int rotate) {
+  return rotate ? (li & 3) * 32 : 0;
+}
+
+// lrow / G for 0 <= lrow < 128 and 1 <= G <= 128 by one multiply: the exact
+// quotient (lrow + 0.5) / G lies at least 0.5 / G from an integer, far more
+// than the float rounding error, so truncation gives the integer quotient.
+__device__ __forceinline__ int div_G(int lrow, float inv_G) {
+  return __float2int_rz(((float)lrow + 0.5f) * inv_G);
 }
 
 // p = 2^(x * c + off) for 32 score columns, packed to E4M3 in pairs and
@@ -324,7 +333,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
           __syncwarp();
           if (lane < hdr.y)
             tma_load_2d(smem + kOffQ + qs * kTile +
-                            ((lane * p.G + row_rotation(li, p.G)) & (kTileM - 1)) * 128,
+                            ((lane * p.G + row_rotation(li, p.rotate)) & (kTileM - 1)) * 128,
                         &q_map, &bars->q_full[qs], 0, tok * p.Hq + hdr.w);
         }
         issued = li + 1;
@@ -437,11 +446,11 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         const int4* rec = reinterpret_cast<const int4*>(smem + kOffRec + ks * kRecMax);
         const int4 hdr = rec[0];
         const int rows = hdr.y * p.G;
-        const int rot = row_rotation(li, p.G);
+        const int rot = row_rotation(li, p.rotate);
         const uint32_t dst0 = smem_u32(smem + kOffQ + qs * kTile);
         for (int e = lane; e < rows * 8; e += 32) {
           const int lrow = e >> 3, ch = e & 7;
-          const int i = lrow / p.G, g = lrow - i * p.G;
+          const int i = div_G(lrow, p.inv_G), g = lrow - i * p.G;
           const int row = (lrow + rot) & (kTileM - 1);
           const int t = rec[1 + i].x;
           const uint8_t* src =
@@ -479,8 +488,8 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       const int4* rec = reinterpret_cast<const int4*>(smem + kOffRec + ks * kRecMax);
       const int4 hdr = rec[0];
       // logical row (token i, head g) held by this lane for this item
-      const int lrow = (row - row_rotation(li, p.G)) & (kTileM - 1);
-      const int i = lrow / p.G, g = lrow - i * p.G;
+      const int lrow = (row - row_rotation(li, p.rotate)) & (kTileM - 1);
+      const int i = div_G(lrow, p.inv_G), g = lrow - i * p.G;
       const bool valid = i < hdr.y;
       const bool warp_valid = __any_sync(0xffffffffu, valid);
       int64_t prow = -1;
@@ -696,6 +705,8 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   p.status = pl.status;
   p.Hq = (int)pl.Hq;
   p.G = G;
+  p.rotate = (G <= 32 && 32 % G == 0) ? 1 : 0;
+  p.inv_G = 1.0f / (float)G;
   p.q_tma = q_tma ? 1 : 0;
   p.score_log2 = a.score_log2;
   p.v_scale = a.v_scale;
