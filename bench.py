@@ -48,8 +48,8 @@ import workloads  # noqa: E402
 
 WORKLOAD = "long_prefill_1m"
 L2_FLUSH_BYTES = 256 << 20
-KERNELS_PER_STEP = 8  # plan: prep, mark, rows, scan, emit, scatter; attention; combine
-DECODE_KERNELS_PER_STEP = 9  # msa_decode: seq-lens prefix sums, then the same 8
+KERNELS_PER_STEP = 7  # plan: prep, mark, rows, emit, scatter; attention; combine
+DECODE_KERNELS_PER_STEP = 8  # msa_decode: seq-lens prefix sums, then the same 7
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attention_kernel_traffic.json")
 ATTN_SOURCES = ["attention.cu", "ptx.cuh", "common.cuh"]
 
@@ -498,7 +498,7 @@ def main():
         if r["decode"]:
             # one msa_decode call per step: its kernels are not timed apart,
             # so the roofline covers the whole call and the step's bytes
-            roof_bytes, roof_s, roof_kernel = alg["step"], step_s, "msa_decode (9 kernels)"
+            roof_bytes, roof_s, roof_kernel = alg["step"], step_s, "msa_decode (8 kernels)"
             traffic = None
             breakdown = {"decode": r["step_ms"] * 1e3}
             launches = DECODE_KERNELS_PER_STEP * args.steps

@@ -18,10 +18,10 @@
 //   rows     a half-warp per row: row length (popcount of its words) and
 //            the running count in front of every word; per 16-row tile, the
 //            sums of the lengths and of the chunk counts
-//   scan     one CTA: exclusive scan of the tile sums
-//   emit     one thread per row: row_ptr and the row's first work item;
-//            the work items / record headers of the CTA's rows dealt over
-//            all its threads
+//   emit     each CTA adds up the tile sums in front of it; one thread per
+//            row: row_ptr and the row's first work item; the work items /
+//            record headers of the CTA's rows dealt over all its threads;
+//            the last CTA writes the totals
 //   scatter  one thread per top-k entry: each kept entry goes to
 //            row_ptr + (tokens of the same row before it), found in O(1)
 //            from the word prefix and a popcount; it also fills the token
@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(kScanThreads) plan_prep_kernel(PlanDev d,
     d.counters[0] = 0;
     d.counters[1] = 0;
     d.counters[2] = st ? 0 : 1;
+    d.row_ptr[d.rows] = 0;  // the fill kernel's last CTA writes the total
   }
 }
 
@@ -291,29 +292,8 @@ __global__ void __launch_bounds__(kPlanTile) plan_rows_kernel(PlanDev d) {
   }
 }
 
-__global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(PlanDev d) {
-  pdl_wait();
-  pdl_trigger();
-  for (int which = 0; which < 2; ++which) {
-    int32_t* a = d.tile_sums + (int64_t)which * d.ntiles;
-    int carry = 0;
-    for (int base = 0; base < d.ntiles; base += kScanThreads) {
-      const int i = base + threadIdx.x;
-      const int v = i < d.ntiles ? a[i] : 0;
-      int total;
-      const int ex = block_excl_scan<kScanThreads>(v, &total);
-      if (i < d.ntiles) a[i] = carry + ex;
-      carry += total;
-    }
-    if (threadIdx.x == 0) {
-      d.counters[which] = carry;
-      if (which == 0) d.row_ptr[d.rows] = carry;
-    }
-  }
-}
-
 // kPlanTile rows per CTA.  One thread per row finds the row's offsets (the
-// scanned sums of the count tiles in front of the CTA plus a block scan)
+// sums of the count tiles in front of the CTA plus a block scan)
 // and its page; then the CTA's chunks are dealt to all its threads, each
 // finding its row by a search over the rows' first chunks, so a row with
 // many chunks does not serialise on one thread.
@@ -332,9 +312,37 @@ __global__ void __launch_bounds__(kPlanTile) plan_emit_kernel(PlanDev d) {
   int tc, tw;
   const int ex_c = block_excl_scan<kPlanTile>(c, &tc);
   const int ex_w = block_excl_scan<kPlanTile>(chunks, &tw);
+  // the rows in front of this CTA: the sums of the count tiles before it,
+  // added up by the whole CTA (no separate scan kernel)
   const int tile0 = blockIdx.x * (kPlanTile / kCountTile);
-  const int base_c = d.tile_sums[tile0];
-  const int base_w = d.tile_sums[d.ntiles + tile0];
+  __shared__ int s_red[2][kPlanTile / 32];
+  int pc = 0, pw = 0;
+  for (int i = threadIdx.x; i < tile0; i += kPlanTile) {
+    pc += d.tile_sums[i];
+    pw += d.tile_sums[d.ntiles + i];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    pc += __shfl_xor_sync(0xffffffffu, pc, o);
+    pw += __shfl_xor_sync(0xffffffffu, pw, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    s_red[0][threadIdx.x >> 5] = pc;
+    s_red[1][threadIdx.x >> 5] = pw;
+  }
+  __syncthreads();
+  int base_c = 0, base_w = 0;
+#pragma unroll
+  for (int w = 0; w < kPlanTile / 32; ++w) {
+    base_c += s_red[0][w];
+    base_w += s_red[1][w];
+  }
+  if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) {
+    // the last CTA closes the CSR and publishes the totals
+    d.counters[0] = base_c + tc;
+    d.counters[1] = base_w + tw;
+    d.row_ptr[d.rows] = base_c + tc;
+  }
   s_wex[threadIdx.x] = ex_w;
   s_start[threadIdx.x] = base_c + ex_c;
   s_cnt[threadIdx.x] = c;
@@ -444,8 +452,6 @@ cudaError_t launch_plan(const msa_plan_t& pl, const int32_t* topk,
   if (e == cudaSuccess && d.ntiles > 0)
     e = launch_pdl(plan_rows_kernel, (unsigned)d.ntiles, kPlanTile, 0, stream, d);
   const unsigned egrid = (unsigned)ceil_div(pl.rows, kPlanTile);
-  if (e == cudaSuccess)
-    e = launch_pdl(plan_scan_kernel, 1u, kScanThreads, 0, stream, d);
   if (e == cudaSuccess && egrid > 0)
     e = launch_pdl(plan_emit_kernel, egrid, kPlanTile, 0, stream, d);
   if (e == cudaSuccess && marks > 0)
