@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the CUDA-graph replay timing")
     return ap.parse_args()
 
 
@@ -253,37 +255,37 @@ def run_ours(args, rank, world):
             w.B, n_dec, w.Hq, w.Hkv, w.max_seqlen_k), dtype=torch.uint8,
             device=dev)
 
-    def decode_step(ev=None):
+    def decode_step(ev=None, st=stream):
         if ev:
-            ev[0].record(stream)
+            ev[0].record(st)
         _, _, plan = msa.msa_decode(wd.q, wd.kv, w.q_scale, w.k_scale,
                                     w.v_scale, w.softmax_scale, wd.topk,
                                     wd.block_table, seq_lens_d, n_dec,
                                     w.max_seqlen_k, workspace=ws_dec, out=out,
-                                    lse=lse, stream=stream)
+                                    lse=lse, stream=st)
         if ev:
             for e in ev[1:]:
-                e.record(stream)
+                e.record(st)
         return plan
 
-    def step(ev=None):
+    def step(ev=None, st=stream):
         if decode:
-            return decode_step(ev)
+            return decode_step(ev, st)
         if ev:
-            ev[0].record(stream)
+            ev[0].record(st)
         plan = msa.msa_plan(wd.topk, wd.cu_q, wd.cu_k, wd.block_table,
                             w.num_pages, w.Hq, w.total_rows, w.max_seqlen_q,
-                            w.max_seqlen_k, workspace=ws_plan, stream=stream)
+                            w.max_seqlen_k, workspace=ws_plan, stream=st)
         if ev:
-            ev[1].record(stream)
+            ev[1].record(st)
         msa.msa_prefill_attention(wd.q, wd.kv, w.q_scale, w.k_scale,
                                   w.v_scale, w.softmax_scale, wd.block_table,
-                                  plan, ws_pre, stream=stream)
+                                  plan, ws_pre, stream=st)
         if ev:
-            ev[2].record(stream)
-        msa.msa_prefill_combine(plan, ws_pre, out, lse, stream=stream)
+            ev[2].record(st)
+        msa.msa_prefill_combine(plan, ws_pre, out, lse, stream=st)
         if ev:
-            ev[3].record(stream)
+            ev[3].record(st)
         return plan
 
     clocks = ClockSampler(local)
@@ -311,6 +313,26 @@ def run_ours(args, rank, world):
                     for e in evs])                       # ms
     plan_ms, attn_ms, comb_ms, step_ms = per.mean(axis=0)
     total_ms = float(per[:, 3].sum())
+
+    # ---- the same step captured once in a CUDA graph, replayed with the L2
+    # flushed before every replay (reported beside the eager figure)
+    graph_ms = None
+    if not args.no_graph:
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            step(st=cap)
+        torch.cuda.synchronize()
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, b in gev:
+            flush.zero_()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        graph_ms = float(np.mean([a.elapsed_time(b) for a, b in gev]))
 
     # ---- end to end through host buffers (pinned), copies inside the region
     e2e = None
@@ -373,10 +395,12 @@ def run_ours(args, rank, world):
         [total_ms, attn_ms, comb_ms, plan_ms, step_ms,
          e2e["ms"] if e2e else 0.0], world, dev, "max")
     (job_pairs,) = reduce_over_ranks([float(pairs)], world, dev, "sum")
+    if graph_ms is not None:
+        (graph_ms,) = reduce_over_ranks([graph_ms], world, dev, "max")
     return dict(w=w, decode=decode, pairs=pairs, upages=upages, total_ms=total_ms,
                 attn_ms=attn_ms, comb_ms=comb_ms, plan_ms=plan_ms,
                 step_ms=step_ms, e2e=e2e, e2e_ms=e2e_ms, clocks=clk,
-                job_pairs=job_pairs,
+                job_pairs=job_pairs, graph_ms=graph_ms,
                 status=status, t_wall=t_wall)
 
 
@@ -537,6 +561,12 @@ def main():
                 "fp8_peak_source": "2 x measured bf16 burst"},
             "work": {"pairs": r["pairs"], "unique_kv_pages": r["upages"]},
             "gpu_launches": launches,
+            "graph": None if r["graph_ms"] is None else {
+                "us_per_layer": r["graph_ms"] * 1e3,
+                "value": job_tflops(r["job_pairs"], r["graph_ms"]),
+                "unit": "TFLOP/s", "replays": args.steps,
+                "note": "the same step captured once in a CUDA graph; "
+                        "replayed after the timed steps, L2 flushed before each"},
             "clocks": r["clocks"], "device_status": r["status"],
         }
         if r["e2e"]:
