@@ -113,3 +113,15 @@ def test_repeatable_and_stream_ordered():
         o2, l2, _ = msa.run_workload(w)
     s.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_mixed_decode_and_prefill_batch(seed):
+    # decode / speculative-verify requests (1 to 8 tokens at the tail of a
+    # long context) and chunked prefills in one plan and one prefill call,
+    # decodes first as the serving engine orders them
+    w = workloads.make_batch("mixed", [1, 8, 4, 8, 333, 1024],
+                             [40000, 65536, 9000, 131072, 5000, 1024],
+                             16, 2, seed=40 + seed)
+    s, e, st = check_against_oracle(w, what="mixed seed %d" % seed)
+    assert st == 0
