@@ -13,29 +13,34 @@
 // causal=True, page_table=block_table).  The kernel design is this
 // library's own.
 //
-// One CTA per SM, persistent over a contiguous range of the work list.
-// Every work item has a record written by the plan: {KV row of the page in
-// the pool, token count n, first key position, first query head} and, per
-// token, {token id, query position, top-k slot}.  Warp roles (16 warps):
-//   warp 0      producer: bulk copy of the item's record, TMA loads of the
-//               K and V halves of the page (2 x 16 KB, 128-byte swizzle)
-//               and, when G is a multiple of 8, of the Q rows: one box of G
-//               rows per token, issued by one lane per token from token ids
-//               prefetched out of the record in global memory
+// One CTA per SM, persistent; work items are dealt round-robin (CTA b takes
+// items b, b + grid, ...), because the plan emits the items of one heavily
+// selected KV row next to each other.  Every work item has a record
+// written by the plan: {KV row of the page in the pool, token count n,
+// first key position, first query head} and, per token, {token id, query
+// position, top-k slot}.  Warp roles (16 warps):
+//   warp 0      producer: headers and token ids staged 8 items ahead in
+//               shared memory by cp.async; bulk copy of the item's record;
+//               TMA loads of the K and V halves of the page (2 x 16 KB,
+//               128-byte swizzle) and, when G is a multiple of 8, of the Q
+//               rows: one box of G rows per token, one lane per token
 //   warp 1      tcgen05 issuer (one thread) and TMEM owner (512 columns)
 //   warps 2-3   Q gather when G is not a multiple of 8: cp.async of 16-byte
 //               chunks into the 128-byte-swizzled K-major tile
 //   warps 4-7   softmax group 0 (even items)
 //   warps 8-11  softmax group 1 (odd items)
-//   warps 12-15 epilogue: O from TMEM, normalised, bf16 partials to HBM
+//   warps 12-15 epilogue: O from TMEM, normalised, rounded to E4M3 in V's
+//               code units (the combine applies v_scale), written as whole
+//               32-byte sectors
 // Shared memory: a 4-slot ring of {K, V} 16 KB tiles with the item's record
 // (released when PV completes), a 3-slot ring of Q tiles (released when QK
 // completes), 2 P tiles, and a 4-slot ring of per-row results handed from
 // softmax to epilogue.
 // TMEM: per group an S tile (128 columns) and an O tile (128 columns).
-// The MMA thread issues QK(n) and PV(n) as soon as each one's inputs are
-// ready, in order, so the tensor cores compute item n+1's scores while item
-// n's softmax runs and never wait on one item for the next one's data.
+// The MMA thread issues QK(n) and PV(n) in order, each as soon as its inputs
+// are ready.  QK(n) reuses the S tile of item n-2 as soon as the softmax
+// holds S(n-2) in registers, so scores for the next items are computed
+// while earlier softmaxes run.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>

@@ -5,8 +5,10 @@
 //
 // For row r with filled slots j:  M = max lse_j,  sum = sum_j e^(lse_j - M),
 // out = sum_j (e^(lse_j - M) / sum) * O_j,  lse = M + ln(sum).
-// HBM-bound: one warp per row, each lane owns 4 of the 128 columns, so a
-// partial row is one coalesced 256 B (bf16) or 512 B (fp32) read.
+// Two kernels: combine16_kernel merges the attention kernel's partials (16
+// slots, E4M3 in V's code units, a half-warp per row); combine_kernel merges
+// caller-given bf16 / fp32 partials for msa_combine (a warp per row, each
+// lane owning 4 of the 128 columns).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
