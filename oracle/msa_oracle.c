@@ -64,6 +64,77 @@ double oracle_e4m3_decode(uint8_t code) {
     return sign ? -v : v;
 }
 
+/* Nearest E4M3 value to x, ties to the even code (round to nearest even on
+ * the format's grid), magnitudes past the largest finite value 448 saturated
+ * to 448.  On [2^k, 2^(k+1)) the grid step is 2^(k-3) for k >= -6; below
+ * 2^-6 it is the subnormal step 2^-9.  x must not be NaN. */
+uint8_t oracle_e4m3_encode(double x) {
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a >= 448.0) return sign | 0x7E;
+    double q;
+    if (a < ldexp(1.0, -6)) {
+        q = ldexp(1.0, -9);
+    } else {
+        int k;
+        frexp(a, &k);               /* a = f * 2^k with f in [0.5, 1) */
+        q = ldexp(1.0, (k - 1) - 3);
+    }
+    const double n = a / q;         /* exact: q is a power of two */
+    const double f = floor(n);
+    const double r = n - f;
+    const double m = (r > 0.5 || (r == 0.5 && fmod(f, 2.0) == 1.0)) ? f + 1.0 : f;
+    const double v = m * q;         /* on the grid, <= 448 */
+    if (v < ldexp(1.0, -6))         /* subnormal: m * 2^-9, m = 0..7 */
+        return sign | (uint8_t)(v / ldexp(1.0, -9));
+    int k;
+    frexp(v, &k);
+    const int e = (k - 1) + 7;      /* v in [2^(e-7), 2^(e-6)) */
+    const int mant = (int)(ldexp(v, -(k - 1)) * 8.0) - 8;
+    return sign | (uint8_t)((e << 3) | mant);
+}
+
+/* OCP 4-bit floating point, E2M1: bit 3 sign, bits 2..1 exponent with bias
+ * 1, bit 0 mantissa.  Exponent 0 is the subnormal 0.5 * m; every other code
+ * is (1 + m/2) * 2^(e-1).  The magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double oracle_e2m1_decode(uint8_t code) {
+    const int sign = (code >> 3) & 1;
+    const int e = (code >> 1) & 0x3;
+    const int m = code & 0x1;
+    const double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -v : v;
+}
+
+/*
+ * NVFP4 page pool -> the E4M3 pool an E4M3-query kernel reads ([P2] vLLM
+ * PR 60684, Details: with an E4M3 query each NVFP4 code times its block
+ * scale is dequantised to E4M3; the K and V global scales stay outside, on
+ * the scores and in the combine).  kv4 holds, per (page, KV head), a K slot
+ * then a V slot; a slot is 128 tokens x 64 bytes of codes (element 2i in the
+ * low nibble of byte i) followed by 128 tokens x 8 E4M3 scales (scale b for
+ * elements 16b .. 16b+15).  kv8 is [page][KV head][128][256], K then V.
+ */
+void oracle_nvfp4_to_e4m3(const uint8_t *kv4, int64_t page_heads, uint8_t *kv8) {
+    const int64_t slot = ORACLE_PAGE * (ORACLE_D / 2) + ORACLE_PAGE * (ORACLE_D / 16);
+#pragma omp parallel for schedule(static)
+    for (int64_t ph = 0; ph < page_heads; ++ph) {
+        for (int s = 0; s < 2; ++s) {
+            const uint8_t *codes = kv4 + (ph * 2 + s) * slot;
+            const uint8_t *scales = codes + ORACLE_PAGE * (ORACLE_D / 2);
+            for (int t = 0; t < ORACLE_PAGE; ++t) {
+                for (int e = 0; e < ORACLE_D; ++e) {
+                    const uint8_t byte = codes[t * (ORACLE_D / 2) + e / 2];
+                    const uint8_t nib = (e & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);
+                    const double v = oracle_e2m1_decode(nib) *
+                                     oracle_e4m3_decode(scales[t * (ORACLE_D / 16) + e / 16]);
+                    kv8[(ph * ORACLE_PAGE + t) * (2 * ORACLE_D) + s * ORACLE_D + e] =
+                        oracle_e4m3_encode(v);
+                }
+            }
+        }
+    }
+}
+
 static double g_dec[256];
 static int g_dec_ready = 0;
 

@@ -60,6 +60,12 @@ def _lib_setup(lib):
     lib.oracle_combine.argtypes = [P, P, i64, i32, i32, P, P]
     lib.oracle_combine.restype = None
     lib.oracle_max_threads.restype = i32
+    lib.oracle_e4m3_encode.argtypes = [f64]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+    lib.oracle_e2m1_decode.restype = f64
+    lib.oracle_nvfp4_to_e4m3.argtypes = [P, i64, P]
+    lib.oracle_nvfp4_to_e4m3.restype = None
 
 
 def _np(x, dtype):
@@ -86,6 +92,29 @@ def e4m3_table() -> np.ndarray:
     return np.array([e4m3_decode(c) for c in range(256)], dtype=np.float64)
 
 
+def e4m3_encode(x: float) -> int:
+    """Nearest E4M3 code (ties to even, saturating at 448), from the format
+    definition."""
+    return int(_load().oracle_e4m3_encode(float(x)))
+
+
+def e2m1_decode(code: int) -> float:
+    """OCP E2M1 (FP4) decoding, from the format definition (bias 1)."""
+    return float(_load().oracle_e2m1_decode(int(code) & 0xF))
+
+
+def nvfp4_to_e4m3(kv4, lib=None) -> np.ndarray:
+    """The E4M3 pool an E4M3-query kernel reads from an NVFP4 pool ([P2]
+    vLLM PR 60684, Details: each code times its block scale, dequantised to
+    E4M3): uint8 [pages][Hkv][2][slot bytes] -> uint8 [pages][Hkv][128][256]."""
+    lib = lib or _load()
+    k4 = _np(kv4, np.uint8)
+    pages, hkv = int(k4.shape[0]), int(k4.shape[1])
+    kv8 = np.zeros((pages, hkv, PAGE, 2 * D), np.uint8)
+    lib.oracle_nvfp4_to_e4m3(_ptr(k4), pages * hkv, _ptr(kv8))
+    return kv8
+
+
 def attention(w, tokens=None, nthreads: int = 0, lib=None):
     """Masked softmax attention of ``w`` (a ``workloads.Workload``) in FP64.
 
@@ -101,7 +130,9 @@ def attention(w, tokens=None, nthreads: int = 0, lib=None):
     """
     lib = lib or _load()
     q = _np(w.q, np.uint8)
-    kv = _np(w.kv, np.uint8)
+    # an NVFP4 workload is attended over the E4M3 pool its kernel reads; its
+    # k_scale / v_scale are the global scales
+    kv = nvfp4_to_e4m3(w.kv4, lib) if w.kv is None else _np(w.kv, np.uint8)
     topk = _np(w.topk, np.int32)
     bt = _np(w.block_table, np.int32)
     cu_q = _np(w.cu_q, np.int32)

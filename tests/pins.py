@@ -15,6 +15,7 @@ seqused_k=seq_lens).
 """
 from __future__ import annotations
 
+import ctypes
 import math
 import os
 
@@ -336,6 +337,70 @@ def check_csr(lib):
         assert np.array_equal(mask, mask_ref)
 
 
+def check_e4m3_encode(lib):
+    """The E4M3 encoder (nearest, ties to even, saturating at 448) against
+    the format's own codes and against torch's float8_e4m3fn cast: every
+    finite code encodes back to itself; random values and the exact
+    midpoints between neighbouring codes round as torch rounds them; values
+    past 448 saturate."""
+    dec = [lib.oracle_e4m3_decode(c) for c in range(256)]
+    for c, v in enumerate(dec):
+        if not math.isnan(v):
+            assert lib.oracle_e4m3_encode(v) == c, hex(c)
+    pos = sorted({v for v in dec if not math.isnan(v) and v >= 0})
+    mids = [(a + b) / 2 for a, b in zip(pos[:-1], pos[1:])]
+    rng = np.random.default_rng(21)
+    xs = np.concatenate([mids, [-m for m in mids],
+                         rng.standard_normal(2000) * 40.0,
+                         rng.uniform(-0.02, 0.02, 500)])
+    xs = xs[np.abs(xs) < 448.0]
+    want = torch.as_tensor(xs.astype(np.float32)).to(torch.float8_e4m3fn).view(
+        torch.uint8).numpy()
+    got = np.array([lib.oracle_e4m3_encode(float(np.float32(x))) for x in xs])
+    assert np.array_equal(got, want)
+    for x, c in ((449.0, 0x7E), (1e6, 0x7E), (-500.0, 0xFE)):
+        assert lib.oracle_e4m3_encode(x) == c
+
+
+def check_nvfp4(lib):
+    """E2M1 decoding against the format definition
+    (tests/golden/e2m1_ocp.txt); the NVFP4 -> E4M3 conversion of a slot with
+    random codes and block scales against a restatement here: the nibble of
+    element e is byte e // 2 (low nibble first), its scale is scale e // 16
+    of its token, and the product is rounded by torch's float8_e4m3fn cast."""
+    path = os.path.join(os.path.dirname(__file__), "golden", "e2m1_ocp.txt")
+    table = {}
+    for line in open(path):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        code, val = line.split()
+        got = lib.oracle_e2m1_decode(int(code, 16))
+        assert got == float(val) and \
+            math.copysign(1, got) == math.copysign(1, float(val)), code
+        table[int(code, 16)] = float(val)
+    rng = np.random.default_rng(22)
+    slot = 128 * 64 + 128 * 8
+    kv4 = np.zeros((3, 1, 2, slot), np.uint8)
+    kv4[..., :128 * 64] = rng.integers(0, 256, size=(3, 1, 2, 128 * 64))
+    # block scales: E4M3 codes of magnitudes up to 74 (code times scale stays
+    # within 448), zero included
+    kv4[..., 128 * 64:] = rng.integers(0, 0x6A, size=(3, 1, 2, 128 * 8))
+    out = np.zeros((3, 1, 128, 256), np.uint8)
+    lib.oracle_nvfp4_to_e4m3(kv4.ctypes.data_as(ctypes.c_void_p), 3,
+                             out.ctypes.data_as(ctypes.c_void_p))
+    codes = kv4[..., :128 * 64].reshape(3, 1, 2, 128, 64)
+    nib = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(3, 1, 2, 128, 128)
+    vals = np.vectorize(table.get)(nib).astype(np.float64)
+    sc = _dec_torch(kv4[..., 128 * 64:].reshape(3, 1, 2, 128, 8))
+    prod = vals * np.repeat(sc, 16, axis=-1)
+    want = torch.as_tensor(prod.astype(np.float32)).to(torch.float8_e4m3fn).view(
+        torch.uint8).numpy()
+    want = np.concatenate([want[:, :, 0], want[:, :, 1]], axis=-1)  # K | V
+    assert np.array_equal(out, want)
+
+
 ALL_CHECKS = [check_e4m3, check_dense_equivalence, check_brute_force,
               check_block_table_permutation, check_padding_and_order,
-              check_closed_forms, check_combine_identity, check_csr]
+              check_closed_forms, check_combine_identity, check_csr,
+              check_e4m3_encode, check_nvfp4]

@@ -52,6 +52,18 @@ MUTATIONS = [
      "const double w = exp(l - L);", "const double w = exp(l - M);"),
     ("E4M3 subnormal exponent", "v = ldexp((double)m, -9);",
      "v = ldexp((double)m, -10);"),
+    ("E4M3 encoder rounds ties away from zero",
+     "(r > 0.5 || (r == 0.5 && fmod(f, 2.0) == 1.0))", "(r >= 0.5)"),
+    ("E4M3 encoder truncates", "(r > 0.5 || (r == 0.5 && fmod(f, 2.0) == 1.0))",
+     "(0)"),
+    ("E2M1 exponent bias 0", "ldexp(1.0 + 0.5 * m, e - 1)",
+     "ldexp(1.0 + 0.5 * m, e)"),
+    ("NVFP4 nibble order swapped",
+     "(e & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF)",
+     "(e & 1) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4)"),
+    ("NVFP4 block of 8 elements", "scales[t * (ORACLE_D / 16) + e / 16]",
+     "scales[t * (ORACLE_D / 16) + e / 8 % 8]"),
+    ("NVFP4 V slot written over K", "s * ORACLE_D + e] =", "0 * s + e] ="),
 ]
 
 

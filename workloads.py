@@ -35,6 +35,11 @@ HEAD_DIM = 128
 PAGE = 128
 TOPK = 16
 E4M3_MAX = 448.0
+E2M1_MAX = 6.0
+# NVFP4 page slot (one KV head's K or V of one page): 128 tokens x 64 bytes
+# of packed E2M1 codes, then 128 tokens x 8 E4M3 block scales
+NVFP4_BLOCK = 16  # elements per E4M3 block scale
+NVFP4_SLOT_BYTES = PAGE * (HEAD_DIM // 2) + PAGE * (HEAD_DIM // NVFP4_BLOCK)
 SOFTMAX_SCALE = 1.0 / math.sqrt(HEAD_DIM)
 
 
@@ -65,6 +70,10 @@ class Workload:
     v_scale: float
     softmax_scale: float = SOFTMAX_SCALE
     meta: dict = field(default_factory=dict)
+    # NVFP4 page pool (uint8 [pages][Hkv][2][NVFP4_SLOT_BYTES]), or None; an
+    # NVFP4 workload has no E4M3 pool (kv is None) and its k_scale / v_scale
+    # are the global scales
+    kv4: torch.Tensor = None
 
     @property
     def B(self) -> int:
@@ -101,8 +110,8 @@ class Workload:
 
     def to(self, device) -> "Workload":
         """Same workload with every tensor moved to ``device``."""
-        mv = {k: getattr(self, k).to(device) for k in
-              ("q", "kv", "topk", "block_table", "cu_q", "cu_k")}
+        mv = {k: (None if getattr(self, k) is None else getattr(self, k).to(device))
+              for k in ("q", "kv", "topk", "block_table", "cu_q", "cu_k", "kv4")}
         return Workload(self.name, list(self.q_lens), list(self.seq_lens),
                         self.Hq, self.Hkv, q_scale=self.q_scale,
                         k_scale=self.k_scale, v_scale=self.v_scale,
@@ -124,6 +133,28 @@ def _quantize(x: torch.Tensor, scale: float) -> torch.Tensor:
         torch.float8_e4m3fn).view(torch.uint8)
 
 
+def _normal_chunks(rng_seed: int, shape, device="cpu"):
+    """N(0,1) fp32 of ``shape`` drawn in chunks along axis 0: yields
+    (start, stop, chunk).  The same seed gives the same numbers every time."""
+    shape = tuple(int(s) for s in shape)
+    n0 = shape[0]
+    inner = int(np.prod(shape[1:])) if len(shape) > 1 else 1
+    chunk = max(1, (1 << 26) // max(inner, 1))
+    if device == "cpu":
+        rng = np.random.Generator(np.random.PCG64(rng_seed))
+        for a in range(0, n0, chunk):
+            b = min(n0, a + chunk)
+            yield a, b, torch.from_numpy(
+                rng.standard_normal((b - a,) + shape[1:], dtype=np.float32))
+    else:
+        g = torch.Generator(device=device)
+        g.manual_seed(rng_seed)
+        for a in range(0, n0, chunk):
+            b = min(n0, a + chunk)
+            yield a, b, torch.randn((b - a,) + shape[1:], generator=g,
+                                    device=device, dtype=torch.float32)
+
+
 def _normal_e4m3(rng_seed: int, shape, device="cpu", split_last=None):
     """N(0,1) fp32 of ``shape`` quantised to E4M3 with a per-tensor scale.
 
@@ -133,37 +164,70 @@ def _normal_e4m3(rng_seed: int, shape, device="cpu", split_last=None):
     never hold their fp32 copy in memory.
     """
     shape = tuple(int(s) for s in shape)
-    n0 = shape[0]
-    inner = int(np.prod(shape[1:])) if len(shape) > 1 else 1
-    chunk = max(1, (1 << 26) // max(inner, 1))
-
-    def chunks():
-        if device == "cpu":
-            rng = np.random.Generator(np.random.PCG64(rng_seed))
-            for a in range(0, n0, chunk):
-                b = min(n0, a + chunk)
-                yield a, b, torch.from_numpy(
-                    rng.standard_normal((b - a,) + shape[1:], dtype=np.float32))
-        else:
-            g = torch.Generator(device=device)
-            g.manual_seed(rng_seed)
-            for a in range(0, n0, chunk):
-                b = min(n0, a + chunk)
-                yield a, b, torch.randn((b - a,) + shape[1:], generator=g,
-                                        device=device, dtype=torch.float32)
-
     parts = [slice(None)] if split_last is None else \
         [slice(0, split_last), slice(split_last, None)]
     amax = [0.0 for _ in parts]
-    for _, _, x in chunks():
+    for _, _, x in _normal_chunks(rng_seed, shape, device):
         for i, sl in enumerate(parts):
             amax[i] = max(amax[i], float(x[..., sl].abs().max()))
     scales = [a / E4M3_MAX if a > 0 else 1.0 for a in amax]
     out = torch.empty(shape, dtype=torch.uint8, device=device)
-    for a, b, x in chunks():
+    for a, b, x in _normal_chunks(rng_seed, shape, device):
         for i, sl in enumerate(parts):
             out[a:b][..., sl] = _quantize(x[..., sl], scales[i])
     return out, scales
+
+
+_E2M1_VALUES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def _e2m1_codes(y: torch.Tensor) -> torch.Tensor:
+    """Nearest E2M1 value, ties to the even magnitude index; 4-bit codes with
+    the sign in bit 3 and the magnitude index in bits 0-2 (input
+    generation only)."""
+    grid = torch.tensor(_E2M1_VALUES, dtype=torch.float32, device=y.device)
+    a = y.abs().clamp(max=E2M1_MAX).contiguous()
+    hi = torch.searchsorted(grid, a).clamp(max=7)
+    lo = (hi - 1).clamp(min=0)
+    dlo, dhi = a - grid[lo], grid[hi] - a
+    idx = torch.where((dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0)), hi, lo)
+    sign = ((y < 0) & (idx > 0)).to(torch.uint8) << 3
+    return idx.to(torch.uint8) | sign
+
+
+def _nvfp4_slots(x: torch.Tensor, g: float) -> torch.Tensor:
+    """fp32 [..., 128 tokens, 128] -> uint8 [..., NVFP4_SLOT_BYTES]: per
+    16-element block an E4M3 scale amax / (6 g) and E2M1 codes of x / (scale
+    g), two codes per byte with the first in the low nibble."""
+    xb = x.reshape(*x.shape[:-1], HEAD_DIM // NVFP4_BLOCK, NVFP4_BLOCK)
+    sb = (xb.abs().amax(-1) / (E2M1_MAX * g)).clamp(max=E4M3_MAX).to(
+        torch.float8_e4m3fn)
+    den = (sb.to(torch.float32) * g).unsqueeze(-1)
+    y = torch.where(den > 0, xb / den.clamp(min=1e-30), torch.zeros_like(xb))
+    codes = _e2m1_codes(y).reshape(x.shape)
+    packed = codes[..., 0::2] | (codes[..., 1::2] << 4)
+    lead = x.shape[:-2]
+    return torch.cat([packed.reshape(*lead, -1),
+                      sb.view(torch.uint8).reshape(*lead, -1)], dim=-1)
+
+
+def _normal_nvfp4(rng_seed: int, num_pages: int, Hkv: int, device="cpu"):
+    """The N(0,1) K|V pool of _normal_e4m3 (same draws), quantised to NVFP4
+    instead: uint8 [pages][Hkv][2 slots: K, V][NVFP4_SLOT_BYTES] and the
+    global scales (K, V) = amax / 448, so that every code times its block
+    scale stays within E4M3's range."""
+    shape = (num_pages, Hkv, PAGE, 2 * HEAD_DIM)
+    amax = [0.0, 0.0]
+    for _, _, x in _normal_chunks(rng_seed, shape, device):
+        amax[0] = max(amax[0], float(x[..., :HEAD_DIM].abs().max()))
+        amax[1] = max(amax[1], float(x[..., HEAD_DIM:].abs().max()))
+    gs = [a / E4M3_MAX if a > 0 else 1.0 for a in amax]
+    out = torch.empty((num_pages, Hkv, 2, NVFP4_SLOT_BYTES), dtype=torch.uint8,
+                      device=device)
+    for a, b, x in _normal_chunks(rng_seed, shape, device):
+        out[a:b, :, 0] = _nvfp4_slots(x[..., :HEAD_DIM], gs[0])
+        out[a:b, :, 1] = _nvfp4_slots(x[..., HEAD_DIM:], gs[1])
+    return out, gs
 
 
 def select_pages(rng, q_len: int, seq_len: int, hkv: int) -> np.ndarray:
@@ -199,7 +263,8 @@ def select_pages(rng, q_len: int, seq_len: int, hkv: int) -> np.ndarray:
 
 
 def make_batch(name: str, q_lens, seq_lens, Hq: int, Hkv: int, seed: int,
-               device="cpu", kv_device=None, extra_pages: int = 0) -> Workload:
+               device="cpu", kv_device=None, extra_pages: int = 0,
+               kv_format: str = "e4m3") -> Workload:
     """General prefill batch: request b has ``q_lens[b]`` query tokens at the
     tail of ``seq_lens[b]`` tokens; all requests share one page pool whose
     pages are handed out by a random permutation."""
@@ -232,13 +297,18 @@ def make_batch(name: str, q_lens, seq_lens, Hq: int, Hkv: int, seed: int,
     kvseed = int(r_kv.integers(0, 2**62))
     kvdev = kv_device or device
     q, (qs,) = _normal_e4m3(qseed, (T, Hq, HEAD_DIM), device=device)
-    kv, (ks, vs) = _normal_e4m3(kvseed, (num_pages, Hkv, PAGE, 2 * HEAD_DIM),
-                                device=kvdev, split_last=HEAD_DIM)
+    kv4 = None
+    if kv_format == "nvfp4":
+        kv = None
+        kv4, (ks, vs) = _normal_nvfp4(kvseed, num_pages, Hkv, device=kvdev)
+    else:
+        kv, (ks, vs) = _normal_e4m3(kvseed, (num_pages, Hkv, PAGE, 2 * HEAD_DIM),
+                                    device=kvdev, split_last=HEAD_DIM)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
     return Workload(name, q_lens, seq_lens, Hq, Hkv, q=q, kv=kv,
                     topk=t(topk), block_table=t(bt), cu_q=t(cu_q),
                     cu_k=t(cu_k), q_scale=qs, k_scale=ks, v_scale=vs,
-                    meta={"seed": seed})
+                    meta={"seed": seed, "kv_format": kv_format}, kv4=kv4)
 
 
 # ----------------------------------------------------------------------------
@@ -283,21 +353,33 @@ CONFIGS = {
 
 
 def make_config(name: str, seed: int = 0, device="cpu", kv_device=None):
+    """A named workload; a name ending in "_nvfp4" is the same workload with
+    an NVFP4 page pool (the same normal draws) instead of the E4M3 one."""
+    if name.endswith("_nvfp4"):
+        w = _make_config(name[:-len("_nvfp4")], seed, device, kv_device, "nvfp4")
+        w.name = name
+        w.meta["description"] += "; NVFP4 K/V pages"
+        return w
+    return _make_config(name, seed, device, kv_device, "e4m3")
+
+
+def _make_config(name, seed, device, kv_device, kv_format):
+    mb = lambda *a: make_batch(*a, kv_format=kv_format)  # noqa: E731
     if name == "tiny_full_prefill":
-        w = make_batch(name, [1024], [1024], 4, 1, seed, device, kv_device)
+        w = mb(name, [1024], [1024], 4, 1, seed, device, kv_device)
     elif name == "chunked_prefill_32k":
-        w = make_batch(name, [2048], [32768], 16, 2, seed, device, kv_device)
+        w = mb(name, [2048], [32768], 16, 2, seed, device, kv_device)
     elif name == "ragged_batch_8":
         ql, sl = ragged_lengths(seed)
-        w = make_batch(name, ql, sl, 16, 2, seed, device, kv_device)
+        w = mb(name, ql, sl, 16, 2, seed, device, kv_device)
     elif name == "long_prefill_1m":
-        w = make_batch(name, [2048], [1048576], 16, 2, seed, device, kv_device)
+        w = mb(name, [2048], [1048576], 16, 2, seed, device, kv_device)
     elif name == "long_prefill_150k":
-        w = make_batch(name, [8192], [153600], 16, 2, seed, device, kv_device)
+        w = mb(name, [8192], [153600], 16, 2, seed, device, kv_device)
     elif name in ("decode_64x8", "decode_16x8"):
         n = 64 if name == "decode_64x8" else 16
         sl = decode_lengths(seed, n)
-        w = make_batch(name, [8] * n, sl, 16, 2, seed, device, kv_device)
+        w = mb(name, [8] * n, sl, 16, 2, seed, device, kv_device)
     else:
         raise KeyError(name)
     w.meta["description"] = CONFIGS[name]
