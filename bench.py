@@ -50,8 +50,11 @@ WORKLOAD = "long_prefill_1m"
 L2_FLUSH_BYTES = 256 << 20
 KERNELS_PER_STEP = 7  # plan: prep, mark, rows, emit, scatter; attention; combine
 DECODE_KERNELS_PER_STEP = 8  # msa_decode: seq-lens prefix sums, then the same 7
+# one (page, KV head) of an NVFP4 pool: K and V slots of 128 x 64 code
+# bytes and 128 x 8 E4M3 block scales
+NVFP4_PAGE_HEAD_BYTES = 2 * (128 * 64 + 128 * 8)
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attention_kernel_traffic.json")
-ATTN_SOURCES = ["attention.cu", "ptx.cuh", "common.cuh"]
+ATTN_SOURCES = ["attention.cu", "ptx.cuh", "common.cuh", "nvfp4.cuh"]
 
 
 def parse():
@@ -143,8 +146,11 @@ def pair_and_page_counts(w):
 
 
 def algorithmic_bytes(w, unique_pages):
+    """Bytes the step must move: Q once, each selected (KV head, page) once
+    (E4M3: 128 x 256 bytes; NVFP4: two slots of codes and block scales),
+    out bf16, the top-k ids."""
     q = w.T * w.Hq * 128
-    kv = unique_pages * 128 * 256
+    kv = unique_pages * (NVFP4_PAGE_HEAD_BYTES if is_nvfp4(w) else 128 * 256)
     out = w.T * w.Hq * 128 * 2
     topk = w.T * w.Hkv * 16 * 4
     return {"attention": q + kv, "step": q + kv + out + topk}
@@ -165,17 +171,24 @@ def source_hash(names):
     return h.hexdigest()[:16]
 
 
-def measured_traffic():
-    """dram bytes per attention launch from the committed ncu summary, or
-    None when the kernel source changed since it was captured."""
+def is_nvfp4(w):
+    return getattr(w, "kv4", None) is not None
+
+
+def measured_traffic(workload):
+    """dram bytes per attention launch on ``workload`` from the committed
+    ncu summaries, or None when there is none for it or the kernel source
+    changed since it was captured."""
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
     except (OSError, ValueError):
         return None
-    if t.get("source_hash") != source_hash(ATTN_SOURCES):
-        return None
-    return t.get("bytes_per_launch")
+    h = source_hash(ATTN_SOURCES)
+    for e in t if isinstance(t, list) else [t]:
+        if e.get("workload") == workload and e.get("source_hash") == h:
+            return e.get("bytes_per_launch")
+    return None
 
 
 # ---------------------------------------------------------------- clocks
@@ -252,6 +265,12 @@ def run_ours(args, rank, world):
     lse = torch.empty((w.T, w.Hq), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     decode = is_decode(w)
+    fp4 = is_nvfp4(w)
+    kv_dev = wd.kv4 if fp4 else wd.kv
+    attention_fn = msa.msa_prefill_attention_nvfp4 if fp4 else msa.msa_prefill_attention
+    prefill_fn = msa.msa_prefill_nvfp4 if fp4 else msa.msa_prefill
+    decode_fn = msa.msa_decode_nvfp4 if fp4 else msa.msa_decode
+    kv_key = "kv4" if fp4 else "kv"
     if decode:
         # decode-shaped batches go through msa_decode: n tokens at the tail
         # of every request, one call per step
@@ -264,11 +283,11 @@ def run_ours(args, rank, world):
     def decode_step(ev=None, st=stream):
         if ev:
             ev[0].record(st)
-        _, _, plan = msa.msa_decode(wd.q, wd.kv, w.q_scale, w.k_scale,
-                                    w.v_scale, w.softmax_scale, wd.topk,
-                                    wd.block_table, seq_lens_d, n_dec,
-                                    w.max_seqlen_k, workspace=ws_dec, out=out,
-                                    lse=lse, stream=st)
+        _, _, plan = decode_fn(wd.q, kv_dev, w.q_scale, w.k_scale,
+                               w.v_scale, w.softmax_scale, wd.topk,
+                               wd.block_table, seq_lens_d, n_dec,
+                               w.max_seqlen_k, workspace=ws_dec, out=out,
+                               lse=lse, stream=st)
         if ev:
             for e in ev[1:]:
                 e.record(st)
@@ -284,9 +303,8 @@ def run_ours(args, rank, world):
                             w.max_seqlen_k, workspace=ws_plan, stream=st)
         if ev:
             ev[1].record(st)
-        msa.msa_prefill_attention(wd.q, wd.kv, w.q_scale, w.k_scale,
-                                  w.v_scale, w.softmax_scale, wd.block_table,
-                                  plan, ws_pre, stream=st)
+        attention_fn(wd.q, kv_dev, w.q_scale, w.k_scale, w.v_scale,
+                     w.softmax_scale, wd.block_table, plan, ws_pre, stream=st)
         if ev:
             ev[2].record(st)
         msa.msa_prefill_combine(plan, ws_pre, out, lse, stream=st)
@@ -345,7 +363,7 @@ def run_ours(args, rank, world):
     if not args.no_e2e:
         host = {k: getattr(w, k).cpu().pin_memory() if getattr(w, k).device.type == "cpu"
                 else getattr(w, k).cpu().pin_memory()
-                for k in ("q", "kv", "topk", "block_table", "cu_q", "cu_k")}
+                for k in ("q", kv_key, "topk", "block_table", "cu_q", "cu_k")}
         dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
         out_h = torch.empty((w.T, w.Hq, 128), dtype=torch.bfloat16).pin_memory()
         lse_h = torch.empty((w.T, w.Hq), dtype=torch.float32).pin_memory()
@@ -365,11 +383,11 @@ def run_ours(args, rank, world):
                     continue
                 dev_in[k].copy_(host[k], non_blocking=True)
             if decode:
-                msa.msa_decode(dev_in["q"], dev_in["kv"], w.q_scale, w.k_scale,
-                               w.v_scale, w.softmax_scale, dev_in["topk"],
-                               dev_in["block_table"], dev_in["seq_lens"],
-                               n_dec, w.max_seqlen_k, workspace=ws_dec,
-                               out=out, lse=lse, stream=stream)
+                decode_fn(dev_in["q"], dev_in[kv_key], w.q_scale, w.k_scale,
+                          w.v_scale, w.softmax_scale, dev_in["topk"],
+                          dev_in["block_table"], dev_in["seq_lens"],
+                          n_dec, w.max_seqlen_k, workspace=ws_dec,
+                          out=out, lse=lse, stream=stream)
                 out_h.copy_(out, non_blocking=True)
                 lse_h.copy_(lse, non_blocking=True)
                 return
@@ -377,10 +395,10 @@ def run_ours(args, rank, world):
                              dev_in["block_table"], w.num_pages, w.Hq,
                              w.total_rows, w.max_seqlen_q, w.max_seqlen_k,
                              workspace=ws_plan, stream=stream)
-            msa.msa_prefill(dev_in["q"], dev_in["kv"], w.q_scale, w.k_scale,
-                            w.v_scale, w.softmax_scale, dev_in["block_table"],
-                            p, workspace=ws_pre, out=out, lse=lse,
-                            stream=stream)
+            prefill_fn(dev_in["q"], dev_in[kv_key], w.q_scale, w.k_scale,
+                       w.v_scale, w.softmax_scale, dev_in["block_table"],
+                       p, workspace=ws_pre, out=out, lse=lse,
+                       stream=stream)
             out_h.copy_(out, non_blocking=True)
             lse_h.copy_(lse, non_blocking=True)
 
@@ -500,6 +518,7 @@ def config_of(w, args):
     return {"workload": "%s: %s" % (w.name, w.meta.get("description", "")),
             "T": w.T, "seq_lens": w.seq_lens if w.B <= 8 else "%d requests" % w.B,
             "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": 128, "page": 128, "topk": 16,
+            "kv_cache": "nvfp4" if is_nvfp4(w) else "e4m3",
             "l2": "flushed before every timed step (256 MiB write)",
             "parallelism": "independent batch per GPU" if args.gpus > 1
             else "single GPU"}
@@ -534,7 +553,7 @@ def main():
             launches = DECODE_KERNELS_PER_STEP * args.steps
         else:
             roof_bytes, roof_s, roof_kernel = alg["attention"], r["attn_ms"] / 1e3, "attention_kernel"
-            traffic = measured_traffic()
+            traffic = measured_traffic(w.name)
             breakdown = {"plan": r["plan_ms"] * 1e3, "attention": r["attn_ms"] * 1e3,
                          "combine": r["comb_ms"] * 1e3}
             launches = KERNELS_PER_STEP * args.steps
@@ -548,7 +567,9 @@ def main():
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": r["step_ms"], "us_per_layer": r["step_ms"] * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
+            "dtype": ("nvfp4 K/V dequantised to e4m3, e4m3 Q (fp32 accumulate)"
+                      if is_nvfp4(w) else "e4m3 (fp32 accumulate)"),
+            "data": "synthetic",
             "config": config_of(w, args),
             "breakdown_us": breakdown,
             "roofline": {"bound": "hbm", "achieved": achieved,

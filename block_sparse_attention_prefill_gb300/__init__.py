@@ -11,6 +11,8 @@ Calls (same names as the C ABI, without the ``msa_`` prefix where noted):
   msa_prefill   sparse attention + log-sum-exp combine -> bf16 out, fp32 lse
   msa_decode    1..8 query tokens per request (decode / speculative verify)
   msa_combine   merge split partials by log-sum-exp
+  msa_prefill_nvfp4, msa_decode_nvfp4   the same over NVFP4 K/V pages
+  msa_nvfp4_to_e4m3   NVFP4 pages -> the E4M3 pages those calls read
 """
 from __future__ import annotations
 
@@ -23,6 +25,7 @@ from . import build as _build
 
 HEAD_DIM = 128
 PAGE_SIZE = 128
+NVFP4_SLOT_BYTES = 9216      # 128 x 64 code bytes + 128 x 8 block scales
 TOPK = 16
 
 DTYPE_F32 = 0
@@ -88,6 +91,14 @@ def load():
                         i64, i64, i64, P, ctypes.c_size_t, P, P, PL, P], i32),
         "msa_decode_noalloc": ([P, P, i64, f32, f32, f32, f32, P, P, i64, P,
                                 i64, i64, i64, i64, i64, P, P, P], i32),
+        "msa_prefill_nvfp4": ([P, P, i64, f32, f32, f32, f32, P, i64, PL, P,
+                               ctypes.c_size_t, P, P, P], i32),
+        "msa_decode_nvfp4": ([P, P, i64, f32, f32, f32, f32, P, P, i64, P, i64,
+                              i64, i64, i64, i64, P, ctypes.c_size_t, P, P, PL,
+                              P], i32),
+        "msa_nvfp4_to_e4m3": ([P, i64, P, P], i32),
+        "msa_prefill_attention_nvfp4": ([P, P, i64, f32, f32, f32, f32, P, i64,
+                                         PL, P, ctypes.c_size_t, P], i32),
         "msa_read_status": ([PL, ctypes.POINTER(ctypes.c_uint32)], i32),
         "msa_read_counters": ([PL, ctypes.POINTER(ctypes.c_int64),
                                ctypes.POINTER(ctypes.c_int64)], i32),
@@ -250,21 +261,67 @@ def msa_plan(topk, cu_seqlens_q, cu_seqlens_k, block_table, num_pages, Hq,
     return Plan(st, ws, (topk, cu_seqlens_q, cu_seqlens_k, block_table))
 
 
+def _need_kv(kv, Hkv, fp4):
+    if fp4:
+        _need(kv, "kv4", (torch.uint8,))
+        if kv.dim() != 4 or tuple(kv.shape[1:]) != (Hkv, 2, NVFP4_SLOT_BYTES):
+            raise MsaError("kv4 must be uint8 [num_pages, Hkv, 2, %d]"
+                           % NVFP4_SLOT_BYTES)
+    else:
+        _need(kv, "kv", _E4M3)
+        if kv.dim() != 4 or tuple(kv.shape[1:]) != (Hkv, PAGE_SIZE, 2 * HEAD_DIM):
+            raise MsaError("kv must be [num_pages, Hkv, 128, 256]")
+
+
 def msa_prefill(q, kv, q_scale, k_scale, v_scale, softmax_scale, block_table,
                 plan: Plan, workspace=None, out=None, lse=None,
                 want_lse=True, stream=None):
     """Sparse attention + combine.  q E4M3 [T, Hq, 128]; kv E4M3
     [num_pages, Hkv, 128, 256].  Returns (out bf16 [T, Hq, 128],
     lse fp32 [T, Hq] or None)."""
+    return _prefill("msa_prefill", q, kv, q_scale, k_scale, v_scale,
+                    softmax_scale, block_table, plan, workspace, out, lse,
+                    want_lse, stream)
+
+
+def msa_prefill_nvfp4(q, kv4, q_scale, k_scale, v_scale, softmax_scale,
+                      block_table, plan: Plan, workspace=None, out=None,
+                      lse=None, want_lse=True, stream=None):
+    """msa_prefill over an NVFP4 pool: kv4 uint8 [num_pages, Hkv, 2, 9216]
+    (per KV head a K slot then a V slot: 128 x 64 code bytes, then 128 x 8
+    E4M3 block scales); k_scale / v_scale are the global scales."""
+    return _prefill("msa_prefill_nvfp4", q, kv4, q_scale, k_scale, v_scale,
+                    softmax_scale, block_table, plan, workspace, out, lse,
+                    want_lse, stream)
+
+
+def msa_nvfp4_to_e4m3(kv4, out=None, stream=None):
+    """NVFP4 pool -> the E4M3 pool [num_pages, Hkv, 128, 256] that the
+    NVFP4 attention reads (each code times its block scale, rounded to
+    E4M3)."""
+    _need(kv4, "kv4", (torch.uint8,))
+    if kv4.dim() != 4 or tuple(kv4.shape[2:]) != (2, NVFP4_SLOT_BYTES):
+        raise MsaError("kv4 must be uint8 [num_pages, Hkv, 2, %d]"
+                       % NVFP4_SLOT_BYTES)
+    P, Hkv = int(kv4.shape[0]), int(kv4.shape[1])
+    if out is None:
+        out = torch.empty((P, Hkv, PAGE_SIZE, 2 * HEAD_DIM),
+                          dtype=torch.float8_e4m3fn, device=kv4.device)
+    _need(out, "out", _E4M3)
+    _check(load().msa_nvfp4_to_e4m3(_ptr(kv4), P * Hkv, _ptr(_bytes(out)),
+                                    _stream(stream)), "msa_nvfp4_to_e4m3")
+    return out
+
+
+def _prefill(name, q, kv, q_scale, k_scale, v_scale, softmax_scale,
+             block_table, plan, workspace, out, lse, want_lse, stream):
     _need(q, "q", _E4M3)
-    _need(kv, "kv", _E4M3)
     _need(block_table, "block_table", (torch.int32,))
     s = plan.struct
     T, Hq = int(s.T), int(s.Hq)
     if tuple(q.shape) != (T, Hq, HEAD_DIM):
         raise MsaError("q must be [T, Hq, 128] = %s" % ((T, Hq, HEAD_DIM),))
-    if kv.dim() != 4 or tuple(kv.shape[1:]) != (s.Hkv, PAGE_SIZE, 2 * HEAD_DIM):
-        raise MsaError("kv must be [num_pages, Hkv, 128, 256]")
+    _need_kv(kv, int(s.Hkv), name.endswith("nvfp4"))
     need = prefill_workspace_bytes(T, Hq)
     ws = _workspace(need, q.device, workspace)
     if out is None:
@@ -275,12 +332,12 @@ def msa_prefill(q, kv, q_scale, k_scale, v_scale, softmax_scale, block_table,
     if lse is not None:
         _need(lse, "lse", (torch.float32,))
     bt_stride = int(block_table.shape[1]) if block_table.dim() == 2 else 1
-    _check(load().msa_prefill(_ptr(_bytes(q)), _ptr(_bytes(kv)),
-                              int(kv.shape[0]), float(q_scale), float(k_scale),
-                              float(v_scale), float(softmax_scale),
-                              _ptr(block_table), bt_stride,
-                              ctypes.byref(s), _ptr(ws), need, _ptr(out),
-                              _ptr(lse), _stream(stream)), "msa_prefill")
+    _check(getattr(load(), name)(_ptr(_bytes(q)), _ptr(_bytes(kv)),
+                                 int(kv.shape[0]), float(q_scale),
+                                 float(k_scale), float(v_scale),
+                                 float(softmax_scale), _ptr(block_table),
+                                 bt_stride, ctypes.byref(s), _ptr(ws), need,
+                                 _ptr(out), _ptr(lse), _stream(stream)), name)
     return out, lse
 
 
@@ -288,15 +345,33 @@ def msa_prefill_attention(q, kv, q_scale, k_scale, v_scale, softmax_scale,
                           block_table, plan: Plan, workspace, stream=None):
     """First half of msa_prefill: the attention kernel, partials into
     ``workspace`` (a uint8 CUDA tensor of prefill_workspace_bytes())."""
+    return _attention("msa_prefill_attention", q, kv, q_scale, k_scale,
+                      v_scale, softmax_scale, block_table, plan, workspace,
+                      stream)
+
+
+def msa_prefill_attention_nvfp4(q, kv4, q_scale, k_scale, v_scale,
+                                softmax_scale, block_table, plan: Plan,
+                                workspace, stream=None):
+    """The attention half of msa_prefill_nvfp4."""
+    return _attention("msa_prefill_attention_nvfp4", q, kv4, q_scale, k_scale,
+                      v_scale, softmax_scale, block_table, plan, workspace,
+                      stream)
+
+
+def _attention(name, q, kv, q_scale, k_scale, v_scale, softmax_scale,
+               block_table, plan, workspace, stream):
     s = plan.struct
+    _need(q, "q", _E4M3)
+    _need_kv(kv, int(s.Hkv), name.endswith("nvfp4"))
     need = prefill_workspace_bytes(int(s.T), int(s.Hq))
     ws = _workspace(need, q.device, workspace)
     bt_stride = int(block_table.shape[1]) if block_table.dim() == 2 else 1
-    _check(load().msa_prefill_attention(
+    _check(getattr(load(), name)(
         _ptr(_bytes(q)), _ptr(_bytes(kv)), int(kv.shape[0]), float(q_scale),
         float(k_scale), float(v_scale), float(softmax_scale),
         _ptr(block_table), bt_stride, ctypes.byref(s), _ptr(ws), need,
-        _stream(stream)), "msa_prefill_attention")
+        _stream(stream)), name)
     return ws
 
 
@@ -338,13 +413,31 @@ def msa_decode(q, kv, q_scale, k_scale, v_scale, softmax_scale, topk,
     """Decode / speculative verify: n query tokens per request at the tail.
     q E4M3 [B*n, Hq, 128]; topk int32 [B*n, Hkv, 16]; seq_lens int32 [B].
     Returns (out, lse, plan)."""
+    return _decode("msa_decode", q, kv, q_scale, k_scale, v_scale,
+                   softmax_scale, topk, block_table, seq_lens, n,
+                   max_seqlen_k, workspace, out, lse, want_lse, stream)
+
+
+def msa_decode_nvfp4(q, kv4, q_scale, k_scale, v_scale, softmax_scale, topk,
+                     block_table, seq_lens, n, max_seqlen_k, workspace=None,
+                     out=None, lse=None, want_lse=True, stream=None):
+    """msa_decode over an NVFP4 pool (kv4 as in msa_prefill_nvfp4; k_scale /
+    v_scale the global scales).  Returns (out, lse, plan)."""
+    return _decode("msa_decode_nvfp4", q, kv4, q_scale, k_scale, v_scale,
+                   softmax_scale, topk, block_table, seq_lens, n,
+                   max_seqlen_k, workspace, out, lse, want_lse, stream)
+
+
+def _decode(name, q, kv, q_scale, k_scale, v_scale, softmax_scale, topk,
+            block_table, seq_lens, n, max_seqlen_k, workspace, out, lse,
+            want_lse, stream):
     _need(q, "q", _E4M3)
-    _need(kv, "kv", _E4M3)
     _need(topk, "topk", (torch.int32,))
     _need(block_table, "block_table", (torch.int32,))
     _need(seq_lens, "seq_lens", (torch.int32,))
     B = int(seq_lens.numel())
     Hq, Hkv = int(q.shape[1]), int(topk.shape[1])
+    _need_kv(kv, Hkv, name.endswith("nvfp4"))
     if q.shape[0] != B * n or topk.shape[0] != B * n:
         raise MsaError("q and topk need B*n rows")
     need = decode_workspace_bytes(B, n, Hq, Hkv, max_seqlen_k)
@@ -356,13 +449,14 @@ def msa_decode(q, kv, q_scale, k_scale, v_scale, softmax_scale, topk,
         lse = torch.empty((B * n, Hq), dtype=torch.float32, device=q.device)
     bt_stride = int(block_table.shape[1]) if block_table.dim() == 2 else 1
     st = MsaPlanStruct()
-    _check(load().msa_decode(_ptr(_bytes(q)), _ptr(_bytes(kv)),
-                             int(kv.shape[0]), float(q_scale), float(k_scale),
-                             float(v_scale), float(softmax_scale), _ptr(topk),
-                             _ptr(block_table), bt_stride, _ptr(seq_lens), B,
-                             int(n), Hq, Hkv, int(max_seqlen_k), _ptr(ws),
-                             need, _ptr(out), _ptr(lse), ctypes.byref(st),
-                             _stream(stream)), "msa_decode")
+    _check(getattr(load(), name)(_ptr(_bytes(q)), _ptr(_bytes(kv)),
+                                 int(kv.shape[0]), float(q_scale),
+                                 float(k_scale), float(v_scale),
+                                 float(softmax_scale), _ptr(topk),
+                                 _ptr(block_table), bt_stride, _ptr(seq_lens),
+                                 B, int(n), Hq, Hkv, int(max_seqlen_k),
+                                 _ptr(ws), need, _ptr(out), _ptr(lse),
+                                 ctypes.byref(st), _stream(stream)), name)
     return out, lse, Plan(st, ws, (topk, seq_lens, block_table))
 
 
@@ -397,6 +491,12 @@ def run_workload(w, stream=None):
     plan = msa_plan(w.topk, w.cu_q, w.cu_k, w.block_table, w.num_pages, w.Hq,
                     w.total_rows, w.max_seqlen_q, w.max_seqlen_k,
                     stream=stream)
-    out, lse = msa_prefill(w.q, w.kv, w.q_scale, w.k_scale, w.v_scale,
-                           w.softmax_scale, w.block_table, plan, stream=stream)
+    if getattr(w, "kv4", None) is not None:
+        out, lse = msa_prefill_nvfp4(w.q, w.kv4, w.q_scale, w.k_scale,
+                                     w.v_scale, w.softmax_scale,
+                                     w.block_table, plan, stream=stream)
+    else:
+        out, lse = msa_prefill(w.q, w.kv, w.q_scale, w.k_scale, w.v_scale,
+                               w.softmax_scale, w.block_table, plan,
+                               stream=stream)
     return out, lse, plan

@@ -6,12 +6,13 @@
 // head, top-k slot).
 //
 // What it computes follows vLLM PR 60684 (Details / "Kernel capability":
-// E4M3 query over E4M3 K/V with E4M3 QK and PV MMAs; Details / "Numerics":
-// softmax probabilities rounded to E4M3; Details / "Scales": q scale folded
-// into the softmax scale) and the vLLM docs for sparse_attention_msa
-// (MiniMaxM3SparseMSAImpl.forward: sparse_atten_func over the k2q CSR,
-// causal=True, page_table=block_table).  The kernel design is this
-// library's own.
+// E4M3 query over E4M3 K/V with E4M3 QK and PV MMAs, and over NVFP4 K/V
+// with each code times its block scale dequantised to E4M3; Details /
+// "Numerics": softmax probabilities rounded to E4M3; Details / "Scales":
+// q scale folded into the softmax scale) and the vLLM docs for
+// sparse_attention_msa (MiniMaxM3SparseMSAImpl.forward: sparse_atten_func
+// over the k2q CSR, causal=True, page_table=block_table).  The kernel design
+// is this library's own.
 //
 // One CTA per SM, persistent; work items are dealt round-robin (CTA b takes
 // items b, b + grid, ...), because the plan emits the items of one heavily
@@ -21,56 +22,54 @@
 // position, top-k slot}.  Warp roles (16 warps):
 //   warp 0      producer: headers and token ids staged 8 items ahead in
 //               shared memory by cp.async; bulk copy of the item's record;
-//               TMA loads of the K and V halves of the page (2 x 16 KB,
-//               128-byte swizzle) and, when G is a multiple of 8, of the Q
-//               rows: one box of G rows per token, one lane per token
+//               E4M3 pool: TMA loads of the K and V halves of the page
+//               (2 x 16 KB, 128-byte swizzle); NVFP4 pool: bulk copies of
+//               the page-head's K and V slots (2 x 9 KB); and, when G is a
+//               multiple of 8, TMA loads of the Q rows: one box of G rows
+//               per token, one lane per token
 //   warp 1      tcgen05 issuer (one thread) and TMEM owner (512 columns)
 //   warps 2-3   Q gather when G is not a multiple of 8: cp.async of 16-byte
-//               chunks into the 128-byte-swizzled K-major tile
+//               chunks into the 128-byte-swizzled K-major tile; NVFP4: also
+//               the dequantisation of each item's V slot
 //   warps 4-7   softmax group 0 (even items)
-//   warps 8-11  softmax group 1 (odd items)
+//   warps 8-11  softmax group 1 (odd items); NVFP4: each group also
+//               dequantises the K slot of its next item after writing P
 //   warps 12-15 epilogue: O from TMEM, normalised, rounded to E4M3 in V's
 //               code units (the combine applies v_scale), written as whole
 //               32-byte sectors
-// Shared memory: a 4-slot ring of {K, V} 16 KB tiles with the item's record
-// (released when PV completes), a 3-slot ring of Q tiles (released when QK
-// completes), 2 P tiles, and a 4-slot ring of per-row results handed from
-// softmax to epilogue.
+// Shared memory (E4M3 pool): a 4-slot ring of {K, V} 16 KB tiles with the
+// item's record (released when PV completes), a 3-slot ring of Q tiles
+// (released when QK completes), 2 P tiles, and a 4-slot ring of per-row
+// results handed from softmax to epilogue.  The NVFP4 layout is described
+// at Ring below.
 // TMEM: per group an S tile (128 columns) and an O tile (128 columns).
 // The MMA thread issues QK(n) and PV(n) in order, each as soon as its inputs
 // are ready.  QK(n) reuses the S tile of item n-2 as soon as the softmax
 // holds S(n-2) in registers, so scores for the next items are computed
 // while earlier softmaxes run.
 #include <cuda.h>
+#include <cstring>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
+#include "nvfp4.cuh"
 #include "ptx.cuh"
 
 namespace msa {
 namespace {
 
-constexpr int kKvStages = 4;
-constexpr int kQStages = 3;
 constexpr int kTile = 128 * 128;  // one 128 x 128 E4M3 tile, bytes
 constexpr int kThreads = 512;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kTmemCols = 512;
-constexpr int kRegsControl = 48;
+constexpr int kRegsControl = 64;
 constexpr int kRegsSoftmax = 176;
-constexpr int kRegsEpilogue = 104;
+constexpr int kRegsEpilogue = 88;
 static_assert(4 * 32 * kRegsControl + 8 * 32 * kRegsSoftmax +
                   4 * 32 * kRegsEpilogue <= 65536,
               "register split must equal the launch allocation");
 constexpr int kRecMax = 16 * (1 + kTileM);  // header + up to 128 tokens
-
-// offsets from the 1024-byte aligned base
-constexpr int kOffK = 0;
-constexpr int kOffV = kOffK + kKvStages * kTile;
-constexpr int kOffQ = kOffV + kKvStages * kTile;
-constexpr int kOffP = kOffQ + kQStages * kTile;
-constexpr int kOffRec = kOffP + 2 * kTile;
 constexpr int kMetaSlots = 4;
 // per row: partial row index (int64, -1 = none), lse, 1/l * v_scale
 struct RowMeta {
@@ -78,21 +77,25 @@ struct RowMeta {
   float lse;
   float inv;
 };
-constexpr int kOffMeta = kOffRec + kKvStages * kRecMax;
 // producer staging of prefetched record headers and token ids: two halves
 // of kBatch items each
 constexpr int kBatch = 8;
-constexpr int kOffStage = kOffMeta + kMetaSlots * kTileM * (int)sizeof(RowMeta);
 constexpr int kStageHdr = 2 * kBatch * 16;                   // int4 per item
 constexpr int kStageTok = 2 * kBatch * 16 * 4;               // 16 ids per item
-constexpr int kOffBar = kOffStage + kStageHdr + kStageTok;
 
+constexpr int kMaxRing = 6;
 struct Barriers {
-  uint64_t rec_full[kKvStages];
-  uint64_t kv_full[kKvStages];
-  uint64_t kv_empty[kKvStages];
-  uint64_t q_full[kQStages];
-  uint64_t q_empty[kQStages];
+  uint64_t rec_full[kMaxRing];
+  uint64_t kraw_full[kMaxRing];  // NVFP4: K slot of the page-head landed
+  uint64_t kraw_empty[kMaxRing]; // NVFP4: K slot converted
+  uint64_t vraw_full[kMaxRing];  // NVFP4: V slot landed
+  uint64_t vraw_empty[kMaxRing]; // NVFP4: V slot converted
+  uint64_t k_full[kMaxRing];     // K tile ready (E4M3: K and V landed)
+  uint64_t v_full[kMaxRing];     // NVFP4: V tile converted
+  uint64_t kv_empty[kMaxRing];   // PV done (E4M3: the whole {K, V} slot)
+  uint64_t k_empty[kMaxRing];    // NVFP4: QK done, the K tile is free
+  uint64_t q_full[kMaxRing];
+  uint64_t q_empty[kMaxRing];
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full[2];
@@ -104,11 +107,48 @@ struct Barriers {
   int abort;
 };
 
-constexpr int kSmemBytes = kOffBar + (int)sizeof(Barriers) + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory above the 227 KB limit");
+// Shared-memory rings and offsets from the 1024-byte aligned base.
+//   E4M3 pool: 4 {K, V} tile slots filled by TMA; the record ring follows
+//   the tile ring.
+//   NVFP4 pool: the K and V slots of a page-head (9 KB each) land in
+//   rings of 3 each; the softmax group of item j - 2 converts K slot j once
+//   it has written P(j - 2), warps 2-3 convert V slot j once PV(j - 2) is
+//   done; then the 2 KB code x scale lookup table and 2 K and 2 V E4M3
+//   tiles.  A record is read until its softmax starts, which precedes the
+//   conversion of the K and V slots two items later, so a ring of
+//   min(K slots, V slots) + 2 records never overwrites one in use.
+template <bool kFp4>
+struct Ring {
+  static constexpr int kv = kFp4 ? 2 : 4;
+  static constexpr int kraw = kFp4 ? 3 : 0;
+  static constexpr int vraw = kFp4 ? 3 : 0;
+  static constexpr int q = 3;
+  static constexpr int rec = kFp4 ? (kraw < vraw ? kraw : vraw) + 2 : kv;
+  static constexpr int off_k = 0;
+  static constexpr int off_v = off_k + kv * kTile;
+  static constexpr int off_q = off_v + kv * kTile;
+  static constexpr int off_p = off_q + q * kTile;
+  static constexpr int off_kraw = off_p + 2 * kTile;
+  static constexpr int off_vraw = off_kraw + kraw * kFp4Slot;
+  static constexpr int off_lut = off_vraw + vraw * kFp4Slot;
+  static constexpr int off_rec = off_lut + (kFp4 ? kFp4LutBytes : 0);
+  static constexpr int off_meta = off_rec + rec * kRecMax;
+  static constexpr int off_stage =
+      off_meta + kMetaSlots * kTileM * (int)sizeof(RowMeta);
+  static constexpr int off_bar = off_stage + kStageHdr + kStageTok;
+  static constexpr int bytes = off_bar + (int)sizeof(Barriers) + 1024;
+  static_assert(rec <= kMaxRing && q <= kMaxRing && kv <= kMaxRing &&
+                    kraw <= kMaxRing && vraw <= kMaxRing,
+                "ring deeper than the barrier arrays");
+  static_assert(off_rec % 16 == 0 && off_kraw % 16 == 0 && off_vraw % 16 == 0 &&
+                    kFp4Slot % 16 == 0 && off_meta % 8 == 0,
+                "bulk-copy destinations must be 16-byte aligned");
+  static_assert(bytes <= 232448, "shared memory above the 227 KB limit");
+};
 
 struct Params {
   const uint8_t* q;
+  const uint8_t* kv4;   // NVFP4 pool (page-heads of kFp4PageHead bytes)
   const int4* records;
   int rec_stride;  // int4 per record
   const int32_t* counters;
@@ -198,13 +238,51 @@ __device__ __forceinline__ float max32(const uint32_t (&r)[32], int col0,
   return m;
 }
 
+// One 128-token slot (K or V) of an NVFP4 page-head, dequantised into a
+// 128 x 128 E4M3 tile in the 128-byte-swizzled layout a TMA box would have
+// written: 1024 blocks of 16 elements, thread c of kN threads taking blocks
+// c, c + kN, ...  Code loads are 8 contiguous bytes per thread and the
+// 16-byte stores of a warp cover 4 whole rows, so neither has bank
+// conflicts.
+// Blocks go in batches of four whose loads are all issued before any of
+// their stores, so the shared-memory latencies of a batch overlap (the
+// compiler cannot move a load above a store to the same array itself).
+template <int kN>
+__device__ __forceinline__ void convert_slot(const uint8_t* raw, uint8_t* tile,
+                                             const uint8_t* lut, int c) {
+  constexpr int kBatchBlocks = 4;
+  static_assert((1024 / kN) % kBatchBlocks == 0, "whole batches per thread");
+#pragma unroll 1
+  for (int j = 0; j < 1024 / kN; j += kBatchBlocks) {
+    uint2 codes[kBatchBlocks];
+    uint32_t scale[kBatchBlocks];
+#pragma unroll
+    for (int u = 0; u < kBatchBlocks; ++u) {
+      const int blk = (j + u) * kN + c;
+      codes[u] = *reinterpret_cast<const uint2*>(raw + blk * 8);
+      scale[u] = raw[kFp4Codes + blk];
+    }
+    uint4 out[kBatchBlocks];
+#pragma unroll
+    for (int u = 0; u < kBatchBlocks; ++u)
+      out[u] = nvfp4_block_to_e4m3(codes[u], scale[u], lut);
+#pragma unroll
+    for (int u = 0; u < kBatchBlocks; ++u) {
+      const int blk = (j + u) * kN + c, t = blk >> 3, b = blk & 7;
+      *reinterpret_cast<uint4*>(tile + t * 128 + ((b ^ (t & 7)) << 4)) = out[u];
+    }
+  }
+}
+
+template <bool kFp4>
 __global__ void __launch_bounds__(kThreads, 1)
 attention_kernel(const __grid_constant__ CUtensorMap kv_map,
                  const __grid_constant__ CUtensorMap q_map, const Params p) {
+  using L = Ring<kFp4>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Barriers* bars = reinterpret_cast<Barriers*>(smem + kOffBar);
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + L::off_bar);
   const volatile int* abort = &bars->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -225,13 +303,26 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
   const int64_t rec_step = (int64_t)gridDim.x * p.rec_stride;  // int4s between own items
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kKvStages; ++s) {
-      mbar_init(&bars->rec_full[s], 1);
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+    // NVFP4: each converting warp arrives once (lane 0, after a
+    // __syncwarp): the four warps of a softmax group on k_full and
+    // kraw_empty; warps 2-3 on v_full, vraw_empty and, gathering Q, q_full
+    for (int s = 0; s < L::rec; ++s) mbar_init(&bars->rec_full[s], 1);
+    for (int s = 0; s < L::kraw; ++s) {
+      mbar_init(&bars->kraw_full[s], 1);
+      mbar_init(&bars->kraw_empty[s], 4);
     }
-    for (int s = 0; s < kQStages; ++s) {
-      mbar_init(&bars->q_full[s], p.q_tma ? 1 : 32);
+    for (int s = 0; s < L::vraw; ++s) {
+      mbar_init(&bars->vraw_full[s], 1);
+      mbar_init(&bars->vraw_empty[s], 2);
+    }
+    for (int s = 0; s < L::kv; ++s) {
+      mbar_init(&bars->k_full[s], kFp4 ? 4 : 1);
+      mbar_init(&bars->v_full[s], 2);
+      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < L::q; ++s) {
+      mbar_init(&bars->q_full[s], p.q_tma ? 1 : (kFp4 ? 2 : 32));
       mbar_init(&bars->q_empty[s], 1);
     }
     for (int w = 0; w < 2; ++w) {
@@ -252,14 +343,15 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  if constexpr (kFp4) nvfp4_build_lut(smem + L::off_lut, threadIdx.x, kThreads);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
   // Launched with 128 registers per thread (512 threads); each role's
-  // warpgroup then resizes: softmax 176, epilogue 104, control warps 48
-  // (4*32*48 + 8*32*176 + 4*32*104 = 64512 <= 65536).
+  // warpgroup then resizes: softmax 176, epilogue 88, control warps 64
+  // (4*32*64 + 8*32*176 + 4*32*88 = 64512 <= 65536).
 
   if (warp < 4) {
   setmaxnreg_dec<kRegsControl>();
@@ -275,8 +367,8 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     // waited for when it ends, so the producer never stalls on a global
     // load.  Lane j < kBatch copies the header of item j; lane l copies the
     // token ids at flat entries l, l+32, l+64, l+96 of the kBatch x 16 ids.
-    int4* shdr = reinterpret_cast<int4*>(smem + kOffStage);
-    int* stok = reinterpret_cast<int*>(smem + kOffStage + kStageHdr);
+    int4* shdr = reinterpret_cast<int4*>(smem + L::off_stage);
+    int* stok = reinterpret_cast<int*>(smem + L::off_stage + kStageHdr);
     auto load_batch = [&](int base, int half) {
       if (lane < kBatch && base + lane < cnt)
         cp_async_16(smem_u32(shdr + half * kBatch + lane),
@@ -305,16 +397,27 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       if (base + kBatch < cnt) load_batch(base + kBatch, half ^ 1);
       for (int j = 0; j < kBatch && base + j < cnt; ++j) {
         const int li = base + j;
-        const int ks = li % kKvStages, qs = li % kQStages;
+        const int ks = li % L::kv, qs = li % L::q, rs = li % L::rec;
         const int4 hdr = shdr[half * kBatch + j];
         const int tok = (lane < 16) ? stok[(half * kBatch + j) * 16 + lane] : 0;
         int ok = 1;
         if (lane == 0) {
-          if (li >= kKvStages)
-            ok = bounded_wait(&bars->kv_empty[ks], ((li / kKvStages) - 1) & 1,
-                              abort, kWaitLimitNs);
-          if (ok && li >= kQStages)
-            ok = bounded_wait(&bars->q_empty[qs], ((li / kQStages) - 1) & 1,
+          // NVFP4: the K and V slots of item li - kraw / li - vraw are
+          // converted, which also frees record slot li - rec
+          if constexpr (kFp4) {
+            if (li >= L::kraw)
+              ok = bounded_wait(&bars->kraw_empty[li % L::kraw],
+                                ((li / L::kraw) - 1) & 1, abort, kWaitLimitNs);
+            if (ok && li >= L::vraw)
+              ok = bounded_wait(&bars->vraw_empty[li % L::vraw],
+                                ((li / L::vraw) - 1) & 1, abort, kWaitLimitNs);
+          } else {
+            if (li >= L::kv)
+              ok = bounded_wait(&bars->kv_empty[ks], ((li / L::kv) - 1) & 1,
+                                abort, kWaitLimitNs);
+          }
+          if (ok && li >= L::q)
+            ok = bounded_wait(&bars->q_empty[qs], ((li / L::q) - 1) & 1,
                               abort, kWaitLimitNs);
           if (!ok && !*abort) set_timeout(bars, p.status);
         }
@@ -324,20 +427,31 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         }
         if (lane == 0) {
           const uint32_t rec_bytes = 16u * (1u + (uint32_t)hdr.y);
-          mbar_arrive_expect_tx(&bars->rec_full[ks], rec_bytes);
-          bulk_load(smem + kOffRec + ks * kRecMax,
+          mbar_arrive_expect_tx(&bars->rec_full[rs], rec_bytes);
+          bulk_load(smem + L::off_rec + rs * kRecMax,
                     grec + li * rec_step, rec_bytes,
-                    &bars->rec_full[ks]);
-          mbar_arrive_expect_tx(&bars->kv_full[ks], 2 * kTile);
-          tma_load_2d(smem + kOffK + ks * kTile, &kv_map, &bars->kv_full[ks], 0, hdr.x);
-          tma_load_2d(smem + kOffV + ks * kTile, &kv_map, &bars->kv_full[ks], kD, hdr.x);
+                    &bars->rec_full[rs]);
+          if constexpr (kFp4) {
+            const uint8_t* ph = p.kv4 + (int64_t)(hdr.x >> 7) * kFp4PageHead;
+            const int kr = li % L::kraw, vr = li % L::vraw;
+            mbar_arrive_expect_tx(&bars->kraw_full[kr], kFp4Slot);
+            bulk_load(smem + L::off_kraw + kr * kFp4Slot, ph, kFp4Slot,
+                      &bars->kraw_full[kr]);
+            mbar_arrive_expect_tx(&bars->vraw_full[vr], kFp4Slot);
+            bulk_load(smem + L::off_vraw + vr * kFp4Slot, ph + kFp4Slot, kFp4Slot,
+                      &bars->vraw_full[vr]);
+          } else {
+            mbar_arrive_expect_tx(&bars->k_full[ks], 2 * kTile);
+            tma_load_2d(smem + L::off_k + ks * kTile, &kv_map, &bars->k_full[ks], 0, hdr.x);
+            tma_load_2d(smem + L::off_v + ks * kTile, &kv_map, &bars->k_full[ks], kD, hdr.x);
+          }
           if (p.q_tma)
             mbar_arrive_expect_tx(&bars->q_full[qs], (uint32_t)(hdr.y * p.G * 128));
         }
         if (p.q_tma) {
           __syncwarp();
           if (lane < hdr.y)
-            tma_load_2d(smem + kOffQ + qs * kTile +
+            tma_load_2d(smem + L::off_q + qs * kTile +
                             ((lane * p.G + row_rotation(li, p.rotate)) & (kTileM - 1)) * 128,
                         &q_map, &bars->q_full[qs], 0, tok * p.Hq + hdr.w);
         }
@@ -350,15 +464,24 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     cp_async_wait<0>();
     // every copy this warp started must land before the CTA exits
     if (lane == 0) {
-      for (int li = issued > kKvStages ? issued - kKvStages : 0; li < issued; ++li) {
-        bounded_wait(&bars->rec_full[li % kKvStages], (li / kKvStages) & 1,
+      for (int li = issued > L::rec ? issued - L::rec : 0; li < issued; ++li)
+        bounded_wait(&bars->rec_full[li % L::rec], (li / L::rec) & 1,
                      nullptr, kWaitLimitNs);
-        bounded_wait(&bars->kv_full[li % kKvStages], (li / kKvStages) & 1,
-                     nullptr, kWaitLimitNs);
+      if constexpr (kFp4) {
+        for (int li = issued > L::kraw ? issued - L::kraw : 0; li < issued; ++li)
+          bounded_wait(&bars->kraw_full[li % L::kraw], (li / L::kraw) & 1,
+                       nullptr, kWaitLimitNs);
+        for (int li = issued > L::vraw ? issued - L::vraw : 0; li < issued; ++li)
+          bounded_wait(&bars->vraw_full[li % L::vraw], (li / L::vraw) & 1,
+                       nullptr, kWaitLimitNs);
+      } else {
+        for (int li = issued > L::kv ? issued - L::kv : 0; li < issued; ++li)
+          bounded_wait(&bars->k_full[li % L::kv], (li / L::kv) & 1,
+                       nullptr, kWaitLimitNs);
       }
       if (p.q_tma)
-        for (int li = issued > kQStages ? issued - kQStages : 0; li < issued; ++li)
-          bounded_wait(&bars->q_full[li % kQStages], (li / kQStages) & 1,
+        for (int li = issued > L::q ? issued - L::q : 0; li < issued; ++li)
+          bounded_wait(&bars->q_full[li % L::q], (li / L::q) & 1,
                        nullptr, kWaitLimitNs);
     }
     __syncwarp();
@@ -369,10 +492,10 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       constexpr uint32_t idesc_pv = idesc_e4m3_f32(128, 128, true);
       bool ok = true;
       auto issue_qk = [&](int li) {
-        const int ks = li % kKvStages, qs = li % kQStages, w = li & 1;
+        const int ks = li % L::kv, qs = li % L::q, w = li & 1;
         tc_fence_after();
-        const uint64_t a = smem_desc_sw128(smem_u32(smem + kOffQ + qs * kTile), 16, 1024);
-        const uint64_t b = smem_desc_sw128(smem_u32(smem + kOffK + ks * kTile), 16, 1024);
+        const uint64_t a = smem_desc_sw128(smem_u32(smem + L::off_q + qs * kTile), 16, 1024);
+        const uint64_t b = smem_desc_sw128(smem_u32(smem + L::off_k + ks * kTile), 16, 1024);
         const uint32_t d = tmem + (uint32_t)(w * 256);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // K = 128 bytes = 4 x 32
@@ -380,12 +503,13 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
                      kk > 0);
         mma_commit(&bars->s_full[w]);
         mma_commit(&bars->q_empty[qs]);
+        if constexpr (kFp4) mma_commit(&bars->k_empty[ks]);
       };
       auto issue_pv = [&](int li) {
-        const int ks = li % kKvStages, w = li & 1;
+        const int ks = li % L::kv, w = li & 1;
         tc_fence_after();
-        const uint64_t a = smem_desc_sw128(smem_u32(smem + kOffP + w * kTile), 16, 1024);
-        const uint64_t b = smem_desc_sw128(smem_u32(smem + kOffV + ks * kTile), 1024, 1024);
+        const uint64_t a = smem_desc_sw128(smem_u32(smem + L::off_p + w * kTile), 16, 1024);
+        const uint64_t b = smem_desc_sw128(smem_u32(smem + L::off_v + ks * kTile), 1024, 1024);
         const uint32_t d = tmem + (uint32_t)(w * 256 + 128);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // 128 keys = 4 x 32; V rows advance 4 KB
@@ -404,8 +528,8 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         if (qk < cnt) {
           const int k = qk >> 1;
           if ((k == 0 || mbar_test(&bars->s_free[qk & 1], (k - 1) & 1)) &&
-              mbar_test(&bars->kv_full[qk % kKvStages], (qk / kKvStages) & 1) &&
-              mbar_test(&bars->q_full[qk % kQStages], (qk / kQStages) & 1)) {
+              mbar_test(&bars->k_full[qk % L::kv], (qk / L::kv) & 1) &&
+              mbar_test(&bars->q_full[qk % L::q], (qk / L::q) & 1)) {
             issue_qk(qk);
             ++qk;
             progressed = true;
@@ -414,7 +538,8 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         if (pv < qk) {
           const int w = pv & 1, k = pv >> 1;
           if (mbar_test(&bars->p_full[w], k & 1) &&
-              (k == 0 || mbar_test(&bars->o_free[w], (k - 1) & 1))) {
+              (k == 0 || mbar_test(&bars->o_free[w], (k - 1) & 1)) &&
+              (!kFp4 || mbar_test(&bars->v_full[pv % L::kv], (pv / L::kv) & 1))) {
             issue_pv(pv);
             ++pv;
             progressed = true;
@@ -432,40 +557,78 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       bounded_wait(&bars->mma_done, 0, nullptr, kWaitLimitNs);
     }
   } else if (warp < 4) {
-    // ------------------------------------------------------------ Q gather
-    // (cp.async mode only) two warps take alternate items; 16-byte chunks
-    // into the swizzled layout, then a proxy fence so the tensor cores see
-    // the rows.
-    if (!p.q_tma) {
+    // Q rows of item li (cp.async mode): 16-byte chunks into the
+    // 128-byte-swizzled K-major tile, `nthr` threads from thread `tid`
+    auto gather_q = [&](int li, int tid, int nthr) {
+      const int4* rec =
+          reinterpret_cast<const int4*>(smem + L::off_rec + (li % L::rec) * kRecMax);
+      const int4 hdr = rec[0];
+      const int rows = hdr.y * p.G;
+      const int rot = row_rotation(li, p.rotate);
+      const uint32_t dst0 = smem_u32(smem + L::off_q + (li % L::q) * kTile);
+      for (int e = tid; e < rows * 8; e += nthr) {
+        const int lrow = e >> 3, ch = e & 7;
+        const int i = div_G(lrow, p.inv_G), g = lrow - i * p.G;
+        const int row = (lrow + rot) & (kTileM - 1);
+        const int t = rec[1 + i].x;
+        const uint8_t* src = p.q + ((int64_t)t * p.Hq + hdr.w + g) * kD + ch * 16;
+        cp_async_16(dst0 + row * 128 + ((ch ^ (row & 7)) << 4), src);
+      }
+      cp_async_commit();
+    };
+    auto wait_rec_q = [&](int li) {
+      return bounded_wait(&bars->rec_full[li % L::rec], (li / L::rec) & 1, abort,
+                          kWaitLimitNs) &&
+             (li < L::q || bounded_wait(&bars->q_empty[li % L::q],
+                                        ((li / L::q) - 1) & 1, abort, kWaitLimitNs));
+    };
+    if constexpr (kFp4) {
+      // ---------------------------------------------------------- V converter
+      // both warps on every item: the Q gather first (cp.async mode), then
+      // the V slot once PV of item li - 2 has freed its tile, followed by a
+      // proxy fence so the tensor cores see the generic-proxy stores
+      const int c = threadIdx.x - 64;
       bool ok = true;
-      for (int li = warp - 2; li < cnt; li += 2) {
-        const int ks = li % kKvStages, qs = li % kQStages;
-        if (!bounded_wait(&bars->rec_full[ks], (li / kKvStages) & 1, abort,
-                          kWaitLimitNs) ||
-            (li >= kQStages &&
-             !bounded_wait(&bars->q_empty[qs], ((li / kQStages) - 1) & 1, abort,
-                           kWaitLimitNs))) {
+      for (int li = 0; li < cnt; ++li) {
+        const int ks = li % L::kv, r = li % L::vraw;
+        if (!p.q_tma) {
+          if (!wait_rec_q(li)) { ok = false; break; }
+          gather_q(li, c, 64);
+          cp_async_wait<0>();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->q_full[li % L::q]);
+        }
+        if (!bounded_wait(&bars->vraw_full[r], (li / L::vraw) & 1, abort, kWaitLimitNs) ||
+            (li >= L::kv && !bounded_wait(&bars->kv_empty[ks], ((li / L::kv) - 1) & 1,
+                                          abort, kWaitLimitNs))) {
           ok = false;
           break;
         }
-        const int4* rec = reinterpret_cast<const int4*>(smem + kOffRec + ks * kRecMax);
-        const int4 hdr = rec[0];
-        const int rows = hdr.y * p.G;
-        const int rot = row_rotation(li, p.rotate);
-        const uint32_t dst0 = smem_u32(smem + kOffQ + qs * kTile);
-        for (int e = lane; e < rows * 8; e += 32) {
-          const int lrow = e >> 3, ch = e & 7;
-          const int i = div_G(lrow, p.inv_G), g = lrow - i * p.G;
-          const int row = (lrow + rot) & (kTileM - 1);
-          const int t = rec[1 + i].x;
-          const uint8_t* src =
-              p.q + ((int64_t)t * p.Hq + hdr.w + g) * kD + ch * 16;
-          cp_async_16(dst0 + row * 128 + ((ch ^ (row & 7)) << 4), src);
+        convert_slot<64>(smem + L::off_vraw + r * kFp4Slot,
+                         smem + L::off_v + ks * kTile, smem + L::off_lut, c);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars->v_full[ks]);
+          mbar_arrive(&bars->vraw_empty[r]);
         }
-        cp_async_commit();
+      }
+      cp_async_wait<0>();
+      if (!ok && lane == 0 && !*abort) set_timeout(bars, p.status);
+    } else if (!p.q_tma) {
+      // ---------------------------------------------------------- Q gather
+      // two warps take alternate items; every lane arrives on q_full
+      bool ok = true;
+      for (int li = warp - 2; li < cnt; li += 2) {
+        if (!wait_rec_q(li)) {
+          ok = false;
+          break;
+        }
+        gather_q(li, lane, 32);
         cp_async_wait<0>();
         fence_proxy_async_smem();
-        mbar_arrive(&bars->q_full[qs]);
+        mbar_arrive(&bars->q_full[li % L::q]);
       }
       cp_async_wait<0>();
       if (!ok && lane == 0 && !*abort) set_timeout(bars, p.status);
@@ -479,18 +642,41 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     const int row = quad * 32 + lane;    // tile row = TMEM lane
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t s_tmem = tmem + lane_off + (uint32_t)(w * 256);
-    uint8_t* prow_s = smem + kOffP + w * kTile + row * 128;
-    RowMeta* meta = reinterpret_cast<RowMeta*>(smem + kOffMeta);
-    for (int k = 0;; ++k) {
+    uint8_t* prow_s = smem + L::off_p + w * kTile + row * 128;
+    RowMeta* meta = reinterpret_cast<RowMeta*>(smem + L::off_meta);
+    // NVFP4: the group dequantises the K slot of each of its items; item j
+    // (j >= 2) right after P(j - 2), whose QK has freed the K tile
+    auto convert_k = [&](int j) {
+      constexpr int R = kFp4 ? L::kraw : 1;  // (E4M3: never called)
+      const int ks = j % L::kv, r = j % R;
+      if (!bounded_wait(&bars->kraw_full[r], (j / R) & 1, abort, kWaitLimitNs) ||
+          (j >= L::kv && !bounded_wait(&bars->k_empty[ks], ((j / L::kv) - 1) & 1,
+                                       abort, kWaitLimitNs))) {
+        if (lane == 0 && !*abort) set_timeout(bars, p.status);
+        return false;
+      }
+      convert_slot<128>(smem + L::off_kraw + r * kFp4Slot, smem + L::off_k + ks * kTile,
+                        smem + L::off_lut, threadIdx.x - 128 - 128 * w);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars->k_full[ks]);
+        mbar_arrive(&bars->kraw_empty[r]);
+      }
+      return true;
+    };
+    bool ok_k = true;
+    if constexpr (kFp4) ok_k = w >= cnt || convert_k(w);
+    for (int k = 0; ok_k; ++k) {
       const int li = 2 * k + w;
       if (li >= cnt) break;
-      const int ks = li % kKvStages;
-      if (!bounded_wait(&bars->rec_full[ks], (li / kKvStages) & 1, abort,
+      const int rs = li % L::rec;
+      if (!bounded_wait(&bars->rec_full[rs], (li / L::rec) & 1, abort,
                         kWaitLimitNs)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
-      const int4* rec = reinterpret_cast<const int4*>(smem + kOffRec + ks * kRecMax);
+      const int4* rec = reinterpret_cast<const int4*>(smem + L::off_rec + rs * kRecMax);
       const int4 hdr = rec[0];
       // logical row (token i, head g) held by this lane for this item
       const int lrow = (row - row_rotation(li, p.rotate)) & (kTileM - 1);
@@ -570,6 +756,9 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       tc_fence_before();
       mbar_arrive(&bars->p_full[w]);
       mbar_arrive(&bars->meta_full[li % kMetaSlots]);
+      if constexpr (kFp4) {
+        if (li + 2 < cnt && !convert_k(li + 2)) break;
+      }
     }
   } else {
     setmaxnreg_dec<kRegsEpilogue>();
@@ -577,7 +766,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const RowMeta* meta = reinterpret_cast<const RowMeta*>(smem + kOffMeta);
+    const RowMeta* meta = reinterpret_cast<const RowMeta*>(smem + L::off_meta);
     for (int li = 0; li < cnt; ++li) {
       const int w = li & 1, k = li >> 1;
       if (!bounded_wait(&bars->meta_full[li % kMetaSlots],
@@ -676,6 +865,21 @@ bool encode_rows(EncodeTiledFn enc, CUtensorMap* map, const void* base,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <bool kFp4>
+cudaError_t launch_kernel(const CUtensorMap& kv_map, const CUtensorMap& q_map,
+                          const Params& p, int64_t grid, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attention_kernel<kFp4>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Ring<kFp4>::bytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_pdl(attention_kernel<kFp4>, dim3((unsigned)grid), dim3(kThreads),
+                    Ring<kFp4>::bytes, stream, kv_map, q_map, p);
+}
+
 }  // namespace
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
@@ -684,10 +888,14 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const int G = (int)(pl.Hq / pl.Hkv);
-  // page pool: rows = (page, KV head, token), 256 bytes each (K then V)
+  const bool fp4 = a.kv_format == MSA_KV_NVFP4;
+  // E4M3 page pool: rows = (page, KV head, token), 256 bytes each (K then
+  // V).  An NVFP4 pool is read by plain bulk copies, with no tensor map.
   CUtensorMap kv_map, q_map;
-  if (!encode_rows(enc, &kv_map, a.kv, 2 * kD,
-                   (uint64_t)a.num_pages * pl.Hkv * kPage, 128))
+  memset(&kv_map, 0, sizeof(kv_map));
+  memset(&q_map, 0, sizeof(q_map));
+  if (!fp4 && !encode_rows(enc, &kv_map, a.kv, 2 * kD,
+                           (uint64_t)a.num_pages * pl.Hkv * kPage, 128))
     return cudaErrorInvalidValue;
   // queries: rows = (token, query head), 128 bytes each; one box = the G
   // heads of one KV head of one token
@@ -695,12 +903,11 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   if (q_tma) {
     if (!encode_rows(enc, &q_map, a.q, kD, (uint64_t)pl.T * pl.Hq, (uint32_t)G))
       return cudaErrorInvalidValue;
-  } else {
-    q_map = kv_map;  // unused
   }
 
   Params p;
   p.q = a.q;
+  p.kv4 = fp4 ? a.kv : nullptr;
   p.records = reinterpret_cast<const int4*>(pl.records);
   p.rec_stride = (int)(pl.record_bytes / 16);
   p.counters = pl.counters;
@@ -716,16 +923,9 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   p.score_log2 = a.score_log2;
   p.v_scale = a.v_scale;
 
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(
-        attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
   const int64_t grid = std::min<int64_t>(num_sms(), pl.max_work);
-  return launch_pdl(attention_kernel, dim3((unsigned)grid), dim3(kThreads), kSmemBytes,
-                    stream, kv_map, q_map, p);
+  return fp4 ? launch_kernel<true>(kv_map, q_map, p, grid, stream)
+             : launch_kernel<false>(kv_map, q_map, p, grid, stream);
 }
 
 }  // namespace msa

@@ -45,6 +45,9 @@ struct AttnArgs {
                       // V's code units (a convex combination of V codes)
   float* part_lse;    // [T][Hq][16]
   float* part_vscale; // one float: v_scale, left here for the combine
+  int kv_format;      // MSA_KV_E4M3: kv is the E4M3 pool; MSA_KV_NVFP4: kv
+                      // holds NVFP4 page-heads (nvfp4.cuh), dequantised to
+                      // E4M3 in shared memory
 };
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
@@ -66,6 +69,10 @@ cudaError_t launch_combine_attn(const uint8_t* part_o, const float* part_lse,
 cudaError_t launch_decode_seqlens(const int32_t* seq_lens, int64_t B,
                                   int64_t n, int32_t* cu_q, int32_t* cu_k,
                                   cudaStream_t stream);
+
+// NVFP4 page-heads -> E4M3 pool [page_heads][128][256].
+cudaError_t launch_nvfp4_to_e4m3(const uint8_t* kv4, int64_t page_heads,
+                                 uint8_t* kv8, cudaStream_t stream);
 
 int num_sms();
 

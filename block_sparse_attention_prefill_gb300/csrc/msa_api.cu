@@ -29,6 +29,7 @@ namespace {
 
 constexpr size_t kAlign = 256;
 constexpr int64_t kI32Max = 2147483647;
+constexpr int64_t kFp4PageBytes = MSA_NVFP4_PAGE_HEAD_BYTES;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -182,7 +183,8 @@ int attention_impl(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
                    float q_scale, float k_scale, float v_scale,
                    float softmax_scale, const int32_t* block_table,
                    int64_t bt_stride, const msa_plan_t* plan, void* ws,
-                   size_t ws_bytes, cudaStream_t stream) {
+                   size_t ws_bytes, cudaStream_t stream,
+                   int kv_format = MSA_KV_E4M3) {
   if (!plan) return MSA_ERR_NULL;
   const int64_t T = plan->T, Hq = plan->Hq;
   if (T == 0) return MSA_OK;
@@ -207,6 +209,7 @@ int attention_impl(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
   a.block_table = block_table;
   a.bt_stride = bt_stride;
   a.plan = plan;
+  a.kv_format = kv_format;
   prefill_layout(T, Hq, ws, &a.part_o, &a.part_lse, &a.part_vscale);
   if (num_pages == 0) return MSA_OK;
   return cuda_rc(launch_attention(a, stream));
@@ -235,14 +238,14 @@ int prefill_impl(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
                  float softmax_scale, const int32_t* block_table,
                  int64_t bt_stride, const msa_plan_t* plan, void* ws,
                  size_t ws_bytes, uint16_t* out, float* lse,
-                 cudaStream_t stream) {
+                 cudaStream_t stream, int kv_format = MSA_KV_E4M3) {
   if (!plan) return MSA_ERR_NULL;
   if (plan->T == 0) return MSA_OK;
   if (!out) return MSA_ERR_NULL;
   if (!aligned(out, 8) || !aligned(lse, 4)) return MSA_ERR_ALIGN;
   int rc = attention_impl(q, kv, num_pages, q_scale, k_scale, v_scale,
                           softmax_scale, block_table, bt_stride, plan, ws,
-                          ws_bytes, stream);
+                          ws_bytes, stream, kv_format);
   if (rc) return rc;
   return prefill_combine_impl(plan, ws, ws_bytes, out, lse, stream);
 }
@@ -266,6 +269,53 @@ int decode_layout(int64_t B, int64_t n, int64_t Hq, int64_t Hkv,
   d->prefill_bytes = prefill_layout(B * n, Hq, nullptr, nullptr, nullptr, nullptr);
   d->total = d->cu_bytes + d->plan_bytes + d->prefill_bytes;
   return MSA_OK;
+}
+
+int decode_impl(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
+                float q_scale, float k_scale, float v_scale,
+                float softmax_scale, const int32_t* topk,
+                const int32_t* block_table, int64_t bt_stride,
+                const int32_t* seq_lens, int64_t B, int64_t n, int64_t Hq,
+                int64_t Hkv, int64_t max_seqlen_k, void* workspace,
+                size_t workspace_bytes, uint16_t* out, float* lse,
+                msa_plan_t* plan_out, cudaStream_t st, int kv_format) {
+  DecodeLayout d;
+  int rc = decode_layout(B, n, Hq, Hkv, max_seqlen_k, &d);
+  if (rc) return rc;
+  if (B == 0) return MSA_OK;
+  if (!seq_lens) return MSA_ERR_NULL;
+  if (!workspace || workspace_bytes < d.total) return MSA_ERR_WORKSPACE;
+  if (!aligned(workspace, kAlign)) return MSA_ERR_ALIGN;
+  char* ws = static_cast<char*>(workspace);
+  int32_t* cu_q = reinterpret_cast<int32_t*>(ws);
+  int32_t* cu_k = cu_q + (B + 1);
+  msa_plan_t local;
+  msa_plan_t* plan = plan_out ? plan_out : &local;
+  // validate everything the plan checks before launching anything
+  PlanShape s;
+  rc = plan_shape(B, B * n, Hq, Hkv, d.R, n, &s);
+  if (rc) return rc;
+  if (!q || !kv || !out || !topk || !block_table) return MSA_ERR_NULL;
+  if (bt_stride < 1 || num_pages < 0 ||
+      num_pages * Hkv * kPage >= kI32Max)
+    return MSA_ERR_SHAPE;
+  if (!(q_scale > 0.f) || !(k_scale > 0.f) || !(v_scale > 0.f) ||
+      !(softmax_scale > 0.f))
+    return MSA_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 8) ||
+      !aligned(lse, 4) || !aligned(topk, 4) || !aligned(block_table, 4) ||
+      !aligned(seq_lens, 4))
+    return MSA_ERR_ALIGN;
+  if (launch_decode_seqlens(seq_lens, B, n, cu_q, cu_k, st) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  rc = plan_impl(topk, cu_q, cu_k, block_table, bt_stride, num_pages, B, B * n,
+                 Hq, Hkv, d.R, n, max_seqlen_k, ws + d.cu_bytes, d.plan_bytes,
+                 plan, st);
+  if (rc) return rc;
+  return prefill_impl(q, kv, num_pages, q_scale, k_scale, v_scale,
+                      softmax_scale, block_table, bt_stride, plan,
+                      ws + d.cu_bytes + d.plan_bytes, d.prefill_bytes, out,
+                      lse, st, kv_format);
 }
 
 }  // namespace
@@ -334,6 +384,29 @@ int msa_prefill(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
                       static_cast<cudaStream_t>(stream));
 }
 
+int msa_prefill_nvfp4(const uint8_t* q, const uint8_t* kv4, int64_t num_pages,
+                      float q_scale, float k_scale, float v_scale,
+                      float softmax_scale, const int32_t* block_table,
+                      int64_t bt_stride, const msa_plan_t* plan,
+                      void* workspace, size_t workspace_bytes, uint16_t* out,
+                      float* lse, void* stream) {
+  return prefill_impl(q, kv4, num_pages, q_scale, k_scale, v_scale,
+                      softmax_scale, block_table, bt_stride, plan, workspace,
+                      workspace_bytes, out, lse,
+                      static_cast<cudaStream_t>(stream), MSA_KV_NVFP4);
+}
+
+int msa_nvfp4_to_e4m3(const uint8_t* kv4, int64_t page_heads, uint8_t* kv8,
+                      void* stream) {
+  if (page_heads < 0 || page_heads > (int64_t(1) << 40) / kFp4PageBytes)
+    return MSA_ERR_SHAPE;
+  if (page_heads == 0) return MSA_OK;
+  if (!kv4 || !kv8) return MSA_ERR_NULL;
+  if (!aligned(kv4, 16) || !aligned(kv8, 16)) return MSA_ERR_ALIGN;
+  return cuda_rc(launch_nvfp4_to_e4m3(kv4, page_heads, kv8,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
 int msa_prefill_attention(const uint8_t* q, const uint8_t* kv,
                           int64_t num_pages, float q_scale, float k_scale,
                           float v_scale, float softmax_scale,
@@ -343,6 +416,18 @@ int msa_prefill_attention(const uint8_t* q, const uint8_t* kv,
   return attention_impl(q, kv, num_pages, q_scale, k_scale, v_scale,
                         softmax_scale, block_table, bt_stride, plan, workspace,
                         workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int msa_prefill_attention_nvfp4(const uint8_t* q, const uint8_t* kv4,
+                                int64_t num_pages, float q_scale, float k_scale,
+                                float v_scale, float softmax_scale,
+                                const int32_t* block_table, int64_t bt_stride,
+                                const msa_plan_t* plan, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  return attention_impl(q, kv4, num_pages, q_scale, k_scale, v_scale,
+                        softmax_scale, block_table, bt_stride, plan, workspace,
+                        workspace_bytes, static_cast<cudaStream_t>(stream),
+                        MSA_KV_NVFP4);
 }
 
 int msa_prefill_combine(const msa_plan_t* plan, void* workspace,
@@ -387,44 +472,26 @@ int msa_decode(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
                int64_t Hkv, int64_t max_seqlen_k, void* workspace,
                size_t workspace_bytes, uint16_t* out, float* lse,
                msa_plan_t* plan_out, void* stream) {
-  DecodeLayout d;
-  int rc = decode_layout(B, n, Hq, Hkv, max_seqlen_k, &d);
-  if (rc) return rc;
-  if (B == 0) return MSA_OK;
-  if (!seq_lens) return MSA_ERR_NULL;
-  if (!workspace || workspace_bytes < d.total) return MSA_ERR_WORKSPACE;
-  if (!aligned(workspace, kAlign)) return MSA_ERR_ALIGN;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  char* ws = static_cast<char*>(workspace);
-  int32_t* cu_q = reinterpret_cast<int32_t*>(ws);
-  int32_t* cu_k = cu_q + (B + 1);
-  msa_plan_t local;
-  msa_plan_t* plan = plan_out ? plan_out : &local;
-  // validate everything the plan checks before launching anything
-  PlanShape s;
-  rc = plan_shape(B, B * n, Hq, Hkv, d.R, n, &s);
-  if (rc) return rc;
-  if (!q || !kv || !out || !topk || !block_table) return MSA_ERR_NULL;
-  if (bt_stride < 1 || num_pages < 0 ||
-      num_pages * Hkv * kPage >= kI32Max)
-    return MSA_ERR_SHAPE;
-  if (!(q_scale > 0.f) || !(k_scale > 0.f) || !(v_scale > 0.f) ||
-      !(softmax_scale > 0.f))
-    return MSA_ERR_SHAPE;
-  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 8) ||
-      !aligned(lse, 4) || !aligned(topk, 4) || !aligned(block_table, 4) ||
-      !aligned(seq_lens, 4))
-    return MSA_ERR_ALIGN;
-  if (launch_decode_seqlens(seq_lens, B, n, cu_q, cu_k, st) != cudaSuccess)
-    return MSA_ERR_CUDA;
-  rc = plan_impl(topk, cu_q, cu_k, block_table, bt_stride, num_pages, B, B * n,
-                 Hq, Hkv, d.R, n, max_seqlen_k, ws + d.cu_bytes, d.plan_bytes,
-                 plan, st);
-  if (rc) return rc;
-  return prefill_impl(q, kv, num_pages, q_scale, k_scale, v_scale,
-                      softmax_scale, block_table, bt_stride, plan,
-                      ws + d.cu_bytes + d.plan_bytes, d.prefill_bytes, out,
-                      lse, st);
+  return decode_impl(q, kv, num_pages, q_scale, k_scale, v_scale,
+                     softmax_scale, topk, block_table, bt_stride, seq_lens, B,
+                     n, Hq, Hkv, max_seqlen_k, workspace, workspace_bytes, out,
+                     lse, plan_out, static_cast<cudaStream_t>(stream),
+                     MSA_KV_E4M3);
+}
+
+int msa_decode_nvfp4(const uint8_t* q, const uint8_t* kv4, int64_t num_pages,
+                     float q_scale, float k_scale, float v_scale,
+                     float softmax_scale, const int32_t* topk,
+                     const int32_t* block_table, int64_t bt_stride,
+                     const int32_t* seq_lens, int64_t B, int64_t n, int64_t Hq,
+                     int64_t Hkv, int64_t max_seqlen_k, void* workspace,
+                     size_t workspace_bytes, uint16_t* out, float* lse,
+                     msa_plan_t* plan_out, void* stream) {
+  return decode_impl(q, kv4, num_pages, q_scale, k_scale, v_scale,
+                     softmax_scale, topk, block_table, bt_stride, seq_lens, B,
+                     n, Hq, Hkv, max_seqlen_k, workspace, workspace_bytes, out,
+                     lse, plan_out, static_cast<cudaStream_t>(stream),
+                     MSA_KV_NVFP4);
 }
 
 }  // extern "C"

@@ -84,6 +84,31 @@ extern "C" {
 #define MSA_DTYPE_BF16 1
 
 /*
+ * NVFP4 K/V pages ([P2] Details / "Kernel capability": with an E4M3 query,
+ * each NVFP4 code times its block scale is dequantised to E4M3, the K global
+ * scale is applied to the scores and the V global scale in the combine;
+ * Details / "Numerics": K and V are rounded to E4M3.  [P4]
+ * MiniMaxM3SparseMSANvfp4Backend: each KV head's K and V are two slots of
+ * packed data plus block scales.)  The pages name the parts, not their byte
+ * order; this library's layout, per (page, KV head), is the K slot then the
+ * V slot, MSA_NVFP4_SLOT_BYTES each:
+ *   codes   128 tokens x 64 bytes of E2M1 (OCP FP4: sign in bit 3, 2-bit
+ *           exponent with bias 1, one mantissa bit); element 2i of a token
+ *           in the low nibble of byte i, element 2i+1 in the high nibble
+ *   scales  128 tokens x 8 E4M3 block scales, finite; scale b covers
+ *           elements 16b .. 16b+15 of its token
+ * so a pool is [num_pages][Hkv][MSA_NVFP4_PAGE_HEAD_BYTES] bytes.  Element
+ * e of token t reads as E4M3(code x scale), rounded to nearest even and
+ * saturated at 448; its real value is that times the K (or V) global scale.
+ */
+#define MSA_NVFP4_SLOT_BYTES 9216
+#define MSA_NVFP4_PAGE_HEAD_BYTES 18432
+
+/* KV page formats (AttnArgs::kv_format inside the library) */
+#define MSA_KV_E4M3 0
+#define MSA_KV_NVFP4 1
+
+/*
  * The page-to-query plan.  msa_plan() fills this host struct; its pointers
  * point into the caller's plan workspace and at the caller's cu_seqlens
  * arrays, which must stay alive and unchanged until the last msa_prefill()
@@ -236,6 +261,46 @@ MSA_API int msa_prefill_combine(const msa_plan_t *plan, void *workspace,
                                 float *lse, void *stream);
 
 /*
+ * NVFP4 page-heads -> E4M3 pool: the cache exactly as the NVFP4 attention
+ * reads it (layout and rounding above).  kv8[ph][t][0..127] is token t's K,
+ * kv8[ph][t][128..255] its V; page-head ph = page * Hkv + KV head.
+ *   kv4   [page_heads][MSA_NVFP4_PAGE_HEAD_BYTES], 16-byte aligned
+ *   kv8   E4M3 [page_heads][128][256], 16-byte aligned, not overlapping kv4
+ * One HBM-bound kernel on `stream`.
+ */
+MSA_API int msa_nvfp4_to_e4m3(const uint8_t *kv4, int64_t page_heads,
+                              uint8_t *kv8, void *stream);
+
+/*
+ * msa_prefill over an NVFP4 pool: the same arguments, with kv4 in place of
+ * kv ([num_pages][Hkv][MSA_NVFP4_PAGE_HEAD_BYTES], 16-byte aligned) and
+ * k_scale / v_scale the K and V global scales.  Each selected (page, KV
+ * head) is read in its NVFP4 form (18 KB instead of 32 KB) and dequantised
+ * to E4M3 in shared memory; the result is the one msa_prefill gives on the
+ * E4M3 pool that msa_nvfp4_to_e4m3() writes, with the same scales.
+ * Workspace: msa_prefill_workspace_bytes().
+ */
+MSA_API int msa_prefill_nvfp4(const uint8_t *q, const uint8_t *kv4,
+                              int64_t num_pages, float q_scale, float k_scale,
+                              float v_scale, float softmax_scale,
+                              const int32_t *block_table, int64_t bt_stride,
+                              const msa_plan_t *plan, void *workspace,
+                              size_t workspace_bytes, uint16_t *out,
+                              float *lse, void *stream);
+
+/* The attention half of msa_prefill_nvfp4 (see msa_prefill_attention);
+ * msa_prefill_combine() finishes it. */
+MSA_API int msa_prefill_attention_nvfp4(const uint8_t *q, const uint8_t *kv4,
+                                        int64_t num_pages, float q_scale,
+                                        float k_scale, float v_scale,
+                                        float softmax_scale,
+                                        const int32_t *block_table,
+                                        int64_t bt_stride,
+                                        const msa_plan_t *plan,
+                                        void *workspace,
+                                        size_t workspace_bytes, void *stream);
+
+/*
  * Merge split partials by log-sum-exp ([P2] Performance: "combine" is the
  * third step of the per-layer call; Validation: probabilities are rounded
  * per split).  For each row r:
@@ -283,6 +348,20 @@ MSA_API int msa_decode(const uint8_t *q, const uint8_t *kv, int64_t num_pages,
                int64_t Hkv, int64_t max_seqlen_k, void *workspace,
                size_t workspace_bytes, uint16_t *out, float *lse,
                msa_plan_t *plan_out, void *stream);
+
+/*
+ * msa_decode over an NVFP4 pool: kv4 as in msa_prefill_nvfp4, k_scale /
+ * v_scale the global scales, everything else as in msa_decode.
+ */
+MSA_API int msa_decode_nvfp4(const uint8_t *q, const uint8_t *kv4,
+                             int64_t num_pages, float q_scale, float k_scale,
+                             float v_scale, float softmax_scale,
+                             const int32_t *topk, const int32_t *block_table,
+                             int64_t bt_stride, const int32_t *seq_lens,
+                             int64_t B, int64_t n, int64_t Hq, int64_t Hkv,
+                             int64_t max_seqlen_k, void *workspace,
+                             size_t workspace_bytes, uint16_t *out, float *lse,
+                             msa_plan_t *plan_out, void *stream);
 
 /*
  * msa_decode for callers that cannot allocate device memory -- for example

@@ -180,7 +180,7 @@ def k2q_csr(w, total_rows=None, lib=None):
     mask = np.zeros((max(T, 1), w.Hkv), np.uint16)
     bt_stride = bt.shape[1] if bt.ndim == 2 else 1
     nnz = lib.oracle_k2q_csr(_ptr(topk), _ptr(bt), bt_stride,
-                             int(w.kv.shape[0]), _ptr(cu_q), _ptr(cu_k), w.B,
+                             int(w.num_pages), _ptr(cu_q), _ptr(cu_k), w.B,
                              w.Hkv, R, _ptr(row_ptr), _ptr(q_idx), _ptr(slot),
                              cap, _ptr(mask))
     if nnz < 0:

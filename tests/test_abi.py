@@ -97,3 +97,23 @@ def test_host_validation_before_launch(lib):
     assert lib.msa_decode(fake, fake, 4, 1.0, 1.0, 1.0, 0.1, fake, fake, 4,
                           fake, 2, 9, 16, 2, 1000, fake, 1 << 30, fake, None,
                           None, None) == 1
+    # NVFP4 prefill: NULL plan; decode: n out of range
+    assert lib.msa_prefill_nvfp4(fake, fake, 4, 1.0, 1.0, 1.0, 0.1, fake, 4,
+                                 None, fake, 1 << 20, fake, None, None) == 6
+    assert lib.msa_decode_nvfp4(fake, fake, 4, 1.0, 1.0, 1.0, 0.1, fake, fake,
+                                4, fake, 2, 9, 16, 2, 1000, fake, 1 << 30,
+                                fake, None, None, None) == 1
+    # NVFP4 -> E4M3 staging: negative count, NULL, misaligned; zero is a no-op
+    assert lib.msa_nvfp4_to_e4m3(fake, -1, fake, None) == 1
+    assert lib.msa_nvfp4_to_e4m3(None, 4, fake, None) == 6
+    assert lib.msa_nvfp4_to_e4m3(P(4096 + 8), 4, fake, None) == 3
+    assert lib.msa_nvfp4_to_e4m3(fake, 0, fake, None) == 0
+
+
+def test_nvfp4_layout_constants():
+    text = open(HEADER).read()
+    slot = int(re.search(r"#define MSA_NVFP4_SLOT_BYTES (\d+)", text).group(1))
+    ph = int(re.search(r"#define MSA_NVFP4_PAGE_HEAD_BYTES (\d+)", text).group(1))
+    # 128 tokens x (64 code bytes + 8 block scales); K slot + V slot
+    assert slot == 128 * 64 + 128 * 8 == msa.NVFP4_SLOT_BYTES
+    assert ph == 2 * slot

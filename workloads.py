@@ -89,7 +89,7 @@ class Workload:
 
     @property
     def num_pages(self) -> int:
-        return int(self.kv.shape[0])
+        return int((self.kv if self.kv is not None else self.kv4).shape[0])
 
     @property
     def pages_per_request(self) -> list:
