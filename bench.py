@@ -153,7 +153,8 @@ def algorithmic_bytes(w, unique_pages):
     kv = unique_pages * (NVFP4_PAGE_HEAD_BYTES if is_nvfp4(w) else 128 * 256)
     out = w.T * w.Hq * 128 * 2
     topk = w.T * w.Hkv * 16 * 4
-    return {"attention": q + kv, "step": q + kv + out + topk}
+    return {"attention": q + kv, "prefill": q + kv + out,
+            "step": q + kv + out + topk}
 
 
 def source_hash(names):
@@ -588,6 +589,15 @@ def main():
                 "fp8_peak_source": "2 x measured bf16 burst"},
             "work": {"pairs": r["pairs"], "unique_kv_pages": r["upages"]},
             "gpu_launches": launches,
+            "roofline_prefill": None if r["decode"] else {
+                "note": "msa_prefill alone (attention + combine, the plan "
+                        "excluded): Q, the selected pages and out",
+                "bound": "hbm" if alg["prefill"] / (peaks["hbm_gbs"] * 1e9) >= t_fp8
+                         else "tensor",
+                "roofline_us": max(alg["prefill"] / (peaks["hbm_gbs"] * 1e9), t_fp8) * 1e6,
+                "frac": max(alg["prefill"] / (peaks["hbm_gbs"] * 1e9), t_fp8)
+                        / ((r["attn_ms"] + r["comb_ms"]) / 1e3),
+                "algorithmic_bytes": alg["prefill"]},
             "graph": None if r["graph_ms"] is None else {
                 "us_per_layer": r["graph_ms"] * 1e3,
                 "value": job_tflops(r["job_pairs"], r["graph_ms"]),

@@ -37,7 +37,7 @@ def _dec_torch(codes) -> np.ndarray:
 
 def _replace(w, **kw):
     d = dict(q=w.q, kv=w.kv, topk=w.topk, block_table=w.block_table,
-             cu_q=w.cu_q, cu_k=w.cu_k)
+             cu_q=w.cu_q, cu_k=w.cu_k, kv4=getattr(w, "kv4", None))
     d.update(kw)
     return workloads.Workload(w.name, list(w.q_lens), list(w.seq_lens), w.Hq,
                               w.Hkv, q_scale=w.q_scale, k_scale=w.k_scale,

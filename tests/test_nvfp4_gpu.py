@@ -16,6 +16,7 @@ import torch
 
 import block_sparse_attention_prefill_gb300 as msa
 import oracle
+import pins
 import workloads
 from gpu_cases import check_against_oracle, run_gpu, sample_tokens
 from tolerance import assert_acceptance, assert_lse
@@ -112,3 +113,68 @@ def test_decode_nvfp4_matches_oracle():
     # the same kernels through the prefill entry points: identical bits
     o2, l2, _ = msa.run_workload(wd)
     assert torch.equal(out, o2) and torch.equal(lse, l2)
+
+
+def test_nvfp4_invalid_entries_are_skipped():
+    # planted bad ids, repeats, future pages and a bad block-table entry, as
+    # in the E4M3 test, over an NVFP4 pool
+    w = workloads.make_batch("tiny_sparse4", [5, 3, 4], [2400, 300, 130], 4, 2,
+                             seed=3, kv_format="nvfp4")
+    tk = w.topk.clone()
+    tk[0, 0, 5] = 10**6
+    tk[1, 1, 3] = -7
+    tk[2, 0, 7] = tk[2, 0, 1]
+    tk[8, 0, 3] = 1
+    bt = w.block_table.clone()
+    bt[0, 3] = -1
+    w = pins._replace(w, topk=tk, block_table=bt)
+    s, e, st = check_against_oracle(w, what="nvfp4 invalid")
+    assert st & msa.STATUS_BAD_PAGE_ID and st & msa.STATUS_BAD_BLOCK
+
+
+def test_nvfp4_graph_replay_matches_eager():
+    w = workloads.make_config("chunked_prefill_32k_nvfp4", seed=7).to("cuda")
+    ws_plan = torch.empty(msa.plan_workspace_bytes(
+        w.B, w.T, w.Hq, w.Hkv, w.total_rows, w.max_seqlen_q),
+        dtype=torch.uint8, device="cuda")
+    ws_pre = torch.empty(msa.prefill_workspace_bytes(w.T, w.Hq),
+                         dtype=torch.uint8, device="cuda")
+    out = torch.empty((w.T, w.Hq, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.T, w.Hq), dtype=torch.float32, device="cuda")
+
+    def step():
+        plan = msa.msa_plan(w.topk, w.cu_q, w.cu_k, w.block_table, w.num_pages,
+                            w.Hq, w.total_rows, w.max_seqlen_q, w.max_seqlen_k,
+                            workspace=ws_plan)
+        msa.msa_prefill_nvfp4(w.q, w.kv4, w.q_scale, w.k_scale, w.v_scale,
+                              w.softmax_scale, w.block_table, plan,
+                              workspace=ws_pre, out=out, lse=lse)
+        return plan
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        plan = step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    ref = [out.clone(), lse.clone()]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(2):
+        out.zero_()
+        lse.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref[0]) and torch.equal(lse, ref[1])
+
+
+def test_nvfp4_binding_rejects_wrong_pool_shape():
+    w = workloads.make_config("tiny_full_prefill_nvfp4", seed=0).to("cuda")
+    plan = msa.msa_plan(w.topk, w.cu_q, w.cu_k, w.block_table, w.num_pages,
+                        w.Hq, w.total_rows, w.max_seqlen_q, w.max_seqlen_k)
+    with pytest.raises(msa.MsaError):
+        msa.msa_prefill_nvfp4(w.q, w.kv4.view(w.num_pages, w.Hkv, -1),
+                              w.q_scale, w.k_scale, w.v_scale,
+                              w.softmax_scale, w.block_table, plan)
