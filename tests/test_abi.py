@@ -117,3 +117,16 @@ def test_nvfp4_layout_constants():
     # 128 tokens x (64 code bytes + 8 block scales); K slot + V slot
     assert slot == 128 * 64 + 128 * 8 == msa.NVFP4_SLOT_BYTES
     assert ph == 2 * slot
+
+
+def test_binding_rejects_host_tensors_and_wrong_pools():
+    # argument checks in the Python binding run before any library call
+    import torch
+    kv4 = torch.zeros((2, 1, 2, msa.NVFP4_SLOT_BYTES), dtype=torch.uint8)
+    assert "CUDA" in _err(msa.msa_nvfp4_to_e4m3, kv4)
+    assert "dtype" in _err(msa._need, kv4.to(torch.int16), "kv4", (torch.uint8,),
+                           False)
+    # the NVFP4 pool check names the expected layout
+    with pytest.raises(msa.MsaError) as e:
+        msa._need_kv(kv4.view(2, 1, -1), 1, True)
+    assert str(msa.NVFP4_SLOT_BYTES) in str(e.value)
