@@ -51,12 +51,13 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 
 // Four E2M1 codes in the low 16 bits of `codes` (the first in the low
 // nibble; `mags` = the same with the sign bits cleared) -> four E4M3 bytes,
-// the first in the low byte.  t0/t1: the block's eight magnitude codes.  A byte permute looks up the magnitude index (bits 0-2
-// of each nibble); a second permute, whose nibbles keep their sign bit,
-// gives 0xFF for a negative code (the sign-replicate mode of prmt on a 0x80
-// byte) and 0x80 otherwise, and bit 0 of that byte, moved to bit 7, flips
-// the sign of the looked-up code.  Flipping (rather than setting) the sign
-// also gives the right sign of zero and of a negative scale.
+// the first in the low byte.  t0/t1: the block's eight magnitude codes.
+// A byte permute looks up the magnitude index (bits 0-2 of each nibble); a
+// second permute, whose nibbles keep their sign bit, gives 0xFF for a
+// negative code (the sign-replicate mode of prmt on a 0x80 byte) and 0x80
+// otherwise, and bit 0 of that byte, moved to bit 7, flips the sign of the
+// looked-up code.  Flipping (rather than setting) the sign also gives the
+// right sign of zero and of a negative scale.
 __device__ __forceinline__ uint32_t fp4x4_lut(uint32_t codes, uint32_t mags,
                                               uint32_t t0, uint32_t t1) {
   const uint32_t mag = prmt(t0, t1, mags);
