@@ -287,12 +287,12 @@ def check_combine_identity(lib):
     assert (e_o == 0).all() and np.isneginf(e_l).all()
 
 
-def python_loop_inversion(w):
+def python_loop_inversion(w, total_rows=None):
     """The CSR as a plain dict of lists: walk tokens in ascending order and
     append each valid, first-seen, not-future page to its row."""
     tk = w.topk.numpy()
     bt = w.block_table.numpy()
-    R = w.total_rows
+    R = w.total_rows if total_rows is None else total_rows
     rows = {}
     mask = np.zeros((w.T, w.Hkv), np.uint16)
     off = 0
@@ -398,6 +398,65 @@ def check_nvfp4(lib):
         torch.uint8).numpy()
     want = np.concatenate([want[:, :, 0], want[:, :, 1]], axis=-1)  # K | V
     assert np.array_equal(out, want)
+
+
+def schedule_cases():
+    """(workload, total_rows) pairs for the work-list pins: GQA groups from
+    1 to 128 (chunks of 128 down to 1 token), ragged batches with two KV
+    heads, spare rows past the requests' pages, invalid entries, and rows
+    selected by hundreds of tokens (many chunks per row)."""
+    cases = []
+    for hq, hkv, seed in ((16, 2, 31), (3, 1, 32), (12, 4, 33), (128, 1, 34),
+                          (4, 4, 35)):
+        w = workloads.make_batch("sched", [300, 40, 7], [2000, 900, 7], hq,
+                                 hkv, seed=seed)
+        cases.append((w, w.total_rows))
+    w = workloads.make_batch("sched_long", [1500], [1500], 16, 2, seed=36)
+    cases.append((w, w.total_rows + 5))
+    w = tiny_sparse_workload(3)
+    cases.append((w, w.total_rows))
+    return cases
+
+
+def check_schedule(schedule=None):
+    """The work list against what its rule fixes, from a CSR built by the
+    plain Python inversion (not the oracle's): every item's token count n
+    satisfies 1 <= n and n * G <= 128 (one 128-row MMA tile of n tokens x G
+    query heads); the items' CSR ranges lie inside their own row
+    (h * R + request offset + p) and, taken in order, tile [0, nnz) exactly
+    once, so rows come in ascending order; every item of a row but its last
+    is full (floor(128 / G) tokens); a row of c entries gives
+    ceil(c / floor(128 / G)) items."""
+    schedule = schedule or orc.schedule
+    for w, R in schedule_cases():
+        rows, _ = python_loop_inversion(w, total_rows=R)
+        nrows = w.Hkv * R
+        cnt = np.zeros(nrows, np.int64)
+        for r, v in rows.items():
+            cnt[r] = len(v)
+        row_ptr = np.zeros(nrows + 1, np.int64)
+        row_ptr[1:] = np.cumsum(cnt)
+        off = np.zeros(w.B + 1, np.int64)
+        off[1:] = np.cumsum(w.pages_per_request)
+        full = 128 // w.G
+        items = schedule(row_ptr, w, total_rows=R)
+        at, last_row = 0, -1
+        per_row = {}
+        for start, n, b, h, p in items:
+            assert 1 <= n and n * w.G <= 128, (n, w.G)
+            assert 0 <= b < w.B and 0 <= h < w.Hkv and \
+                0 <= p < w.pages_per_request[b]
+            r = h * R + int(off[b]) + p
+            assert row_ptr[r] <= start and start + n <= row_ptr[r + 1], (r, start)
+            assert start == at, "items do not tile the CSR in order"
+            assert r >= last_row, "rows out of order"
+            at, last_row = start + n, r
+            per_row.setdefault(r, []).append(n)
+        assert at == row_ptr[-1]
+        assert len(items) == sum(-(-int(c) // full) for c in cnt)
+        for r, ns in per_row.items():
+            assert all(n == full for n in ns[:-1]), r
+            assert sum(ns) == cnt[r]
 
 
 ALL_CHECKS = [check_e4m3, check_dense_equivalence, check_brute_force,

@@ -1,8 +1,11 @@
 """The oracle against facts outside itself (see tests/pins.py), and proof
 that the pins have teeth: copies of the oracle with a planted mistake each
 fail at least one pin."""
+import inspect
 import os
 import shutil
+
+import numpy as np
 
 import pytest
 
@@ -85,3 +88,31 @@ def test_planted_mistake_is_caught(name, old, new, tmp_path):
         except (ValueError, IndexError):
             caught.append(check.__name__)
     assert caught, "no pin caught: %s" % name
+
+
+def test_schedule_pins():
+    pins.check_schedule()
+
+
+# (what goes wrong, text in oracle.schedule, replacement)
+SCHEDULE_MUTATIONS = [
+    ("chunk one token too long", "C = 128 // w.G", "C = 128 // w.G + 1"),
+    ("chunks sized by query heads", "C = 128 // w.G", "C = 128 // w.Hq"),
+    ("requests outer, KV heads inner",
+     "for h in range(w.Hkv):\n        for b in range(w.B):",
+     "for b in range(w.B):\n        for h in range(w.Hkv):"),
+    ("last short chunk dropped", "for c in range(a, e, C):",
+     "for c in range(a, e - C + 1, C):"),
+    ("count not clipped at the row end", "min(C, e - c)", "C"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", SCHEDULE_MUTATIONS,
+                         ids=[m[0] for m in SCHEDULE_MUTATIONS])
+def test_schedule_planted_mistake_is_caught(name, old, new):
+    src = inspect.getsource(orc.schedule)
+    assert src.count(old) == 1, "mutation anchor not unique: %s" % name
+    ns = {"np": np}
+    exec(src.replace(old, new), ns)
+    with pytest.raises(AssertionError):
+        pins.check_schedule(ns["schedule"])
