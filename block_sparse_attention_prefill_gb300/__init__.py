@@ -42,7 +42,7 @@ _I64 = ("B", "T", "Hq", "Hkv", "total_rows", "max_seqlen_q", "max_seqlen_k",
         "num_pages", "bt_stride", "bitmap_words", "chunk_tokens", "max_nnz",
         "max_work", "rows", "record_bytes")
 _PTR = ("cu_seqlens_q", "cu_seqlens_k", "req_off", "bitmap", "word_pre",
-        "row_cnt", "row_wptr", "tile_sums", "row_ptr", "q_idx", "slot", "work",
+        "row_cnt", "row_wptr", "tile_state", "row_ptr", "q_idx", "slot", "work",
         "records", "counters", "slot_mask", "status")
 
 
@@ -99,6 +99,7 @@ def load():
         "msa_nvfp4_to_e4m3": ([P, i64, P, P], i32),
         "msa_prefill_attention_nvfp4": ([P, P, i64, f32, f32, f32, f32, P, i64,
                                          PL, P, ctypes.c_size_t, P], i32),
+        "msa_test_set_wait_limit_ns": ([ctypes.c_uint64], i32),
         "msa_read_status": ([PL, ctypes.POINTER(ctypes.c_uint32)], i32),
         "msa_read_counters": ([PL, ctypes.POINTER(ctypes.c_int64),
                                ctypes.POINTER(ctypes.c_int64)], i32),
@@ -261,16 +262,44 @@ def msa_plan(topk, cu_seqlens_q, cu_seqlens_k, block_table, num_pages, Hq,
     return Plan(st, ws, (topk, cu_seqlens_q, cu_seqlens_k, block_table))
 
 
-def _need_kv(kv, Hkv, fp4):
+def _kv_shape(kv, Hkv, fp4):
+    if kv is None:
+        raise MsaError("%s is required" % ("kv4" if fp4 else "kv"))
     if fp4:
-        _need(kv, "kv4", (torch.uint8,))
         if kv.dim() != 4 or tuple(kv.shape[1:]) != (Hkv, 2, NVFP4_SLOT_BYTES):
             raise MsaError("kv4 must be uint8 [num_pages, Hkv, 2, %d]"
                            % NVFP4_SLOT_BYTES)
-    else:
-        _need(kv, "kv", _E4M3)
-        if kv.dim() != 4 or tuple(kv.shape[1:]) != (Hkv, PAGE_SIZE, 2 * HEAD_DIM):
-            raise MsaError("kv must be [num_pages, Hkv, 128, 256]")
+    elif kv.dim() != 4 or tuple(kv.shape[1:]) != (Hkv, PAGE_SIZE, 2 * HEAD_DIM):
+        raise MsaError("kv must be [num_pages, Hkv, 128, 256]")
+
+
+def _need_kv(kv, Hkv, fp4):
+    _kv_shape(kv, Hkv, fp4)
+    _need(kv, "kv4" if fp4 else "kv", (torch.uint8,) if fp4 else _E4M3)
+
+
+def _decode_shapes(q, kv, topk, seq_lens, n, fp4, out=None, lse=None):
+    """Shape checks of the decode calls, made before any tensor reaches the
+    library (which sees only pointers): q [B*n, Hq, 128], topk
+    [B*n, Hkv, 16], the pool for Hkv KV heads, and, when given, out
+    [B*n, Hq, 128] and lse [B*n, Hq].  Returns (B, Hq, Hkv)."""
+    for t, name in ((q, "q"), (topk, "topk"), (seq_lens, "seq_lens")):
+        if t is None:
+            raise MsaError("%s is required" % name)
+    if q.dim() != 3 or q.shape[2] != HEAD_DIM:
+        raise MsaError("q must be [B*n, Hq, 128]")
+    if topk.dim() != 3 or topk.shape[2] != TOPK:
+        raise MsaError("topk must be [B*n, Hkv, 16]")
+    B = int(seq_lens.numel())
+    Hq, Hkv = int(q.shape[1]), int(topk.shape[1])
+    if q.shape[0] != B * n or topk.shape[0] != B * n:
+        raise MsaError("q and topk need B*n rows")
+    _kv_shape(kv, Hkv, fp4)
+    if out is not None and tuple(out.shape) != (B * n, Hq, HEAD_DIM):
+        raise MsaError("out must be [B*n, Hq, 128] = %s" % ((B * n, Hq, HEAD_DIM),))
+    if lse is not None and tuple(lse.shape) != (B * n, Hq):
+        raise MsaError("lse must be [B*n, Hq] = %s" % ((B * n, Hq),))
+    return B, Hq, Hkv
 
 
 def msa_prefill(q, kv, q_scale, k_scale, v_scale, softmax_scale, block_table,
@@ -431,15 +460,13 @@ def msa_decode_nvfp4(q, kv4, q_scale, k_scale, v_scale, softmax_scale, topk,
 def _decode(name, q, kv, q_scale, k_scale, v_scale, softmax_scale, topk,
             block_table, seq_lens, n, max_seqlen_k, workspace, out, lse,
             want_lse, stream):
+    fp4 = name.endswith("nvfp4")
+    B, Hq, Hkv = _decode_shapes(q, kv, topk, seq_lens, n, fp4, out, lse)
     _need(q, "q", _E4M3)
     _need(topk, "topk", (torch.int32,))
     _need(block_table, "block_table", (torch.int32,))
     _need(seq_lens, "seq_lens", (torch.int32,))
-    B = int(seq_lens.numel())
-    Hq, Hkv = int(q.shape[1]), int(topk.shape[1])
-    _need_kv(kv, Hkv, name.endswith("nvfp4"))
-    if q.shape[0] != B * n or topk.shape[0] != B * n:
-        raise MsaError("q and topk need B*n rows")
+    _need_kv(kv, Hkv, fp4)
     need = decode_workspace_bytes(B, n, Hq, Hkv, max_seqlen_k)
     ws = _workspace(need, q.device, workspace)
     if out is None:
@@ -447,6 +474,9 @@ def _decode(name, q, kv, q_scale, k_scale, v_scale, softmax_scale, topk,
                           device=q.device)
     if lse is None and want_lse:
         lse = torch.empty((B * n, Hq), dtype=torch.float32, device=q.device)
+    _need(out, "out", (torch.bfloat16,))
+    if lse is not None:
+        _need(lse, "lse", (torch.float32,))
     bt_stride = int(block_table.shape[1]) if block_table.dim() == 2 else 1
     st = MsaPlanStruct()
     _check(getattr(load(), name)(_ptr(_bytes(q)), _ptr(_bytes(kv)),
@@ -465,7 +495,12 @@ def msa_decode_noalloc(q, kv, q_scale, k_scale, v_scale, softmax_scale,
                        stream=None):
     """msa_decode with the library's fixed device scratch instead of a
     workspace: for callers that cannot allocate device memory.  out and lse
-    are the caller's; nothing is allocated here or in the library call."""
+    are the caller's; nothing is allocated here or in the library call.  The
+    same shape checks as msa_decode run first, since the library sees only
+    pointers and could not catch a mis-shaped pool or output."""
+    if out is None:
+        raise MsaError("out is required")
+    B, Hq, Hkv = _decode_shapes(q, kv, topk, seq_lens, n, False, out, lse)
     _need(q, "q", _E4M3)
     _need(kv, "kv", _E4M3)
     _need(topk, "topk", (torch.int32,))
@@ -474,14 +509,13 @@ def msa_decode_noalloc(q, kv, q_scale, k_scale, v_scale, softmax_scale,
     _need(out, "out", (torch.bfloat16,))
     if lse is not None:
         _need(lse, "lse", (torch.float32,))
-    B = int(seq_lens.numel())
     bt_stride = int(block_table.shape[1]) if block_table.dim() == 2 else 1
     _check(load().msa_decode_noalloc(
         _ptr(_bytes(q)), _ptr(_bytes(kv)), int(kv.shape[0]), float(q_scale),
         float(k_scale), float(v_scale), float(softmax_scale), _ptr(topk),
-        _ptr(block_table), bt_stride, _ptr(seq_lens), B, int(n),
-        int(q.shape[1]), int(topk.shape[1]), int(max_seqlen_k), _ptr(out),
-        _ptr(lse), _stream(stream)), "msa_decode_noalloc")
+        _ptr(block_table), bt_stride, _ptr(seq_lens), B, int(n), Hq, Hkv,
+        int(max_seqlen_k), _ptr(out), _ptr(lse), _stream(stream)),
+        "msa_decode_noalloc")
     return out, lse
 
 

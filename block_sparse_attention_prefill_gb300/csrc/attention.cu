@@ -37,17 +37,24 @@
 //   warps 12-15 epilogue: O from TMEM, normalised, rounded to E4M3 in V's
 //               code units (the combine applies v_scale), written as whole
 //               32-byte sectors
-// Shared memory (E4M3 pool): a 4-slot ring of {K, V} 16 KB tiles with the
-// item's record (released when PV completes), a 3-slot ring of Q tiles
-// (released when QK completes), 2 P tiles, and a 4-slot ring of per-row
-// results handed from softmax to epilogue.  The NVFP4 layout is described
-// at Ring below.
+// Shared memory (E4M3 pool): a 3-slot ring of K tiles (16 KB, released when
+// QK completes), a 5-slot ring of V tiles with the item's record (released
+// when PV completes), a 5-slot ring of Q/P tiles -- the item's Q rows,
+// which its softmax overwrites with P once QK has completed (released when
+// PV completes) -- and a ring of per-row results handed from softmax to
+// epilogue.  K leaves shared memory as soon as the scores are computed, so
+// more V and Q/P tiles fit, and those are the ones held through the
+// softmax.  The NVFP4 layout is described at Ring below.
 // TMEM: per group an S tile (128 columns) and an O tile (128 columns).
 // The MMA thread issues QK(n) and PV(n) in order, each as soon as its inputs
 // are ready.  QK(n) reuses the S tile of item n-2 as soon as the softmax
 // holds S(n-2) in registers, so scores for the next items are computed
-// while earlier softmaxes run.
+// while earlier softmaxes run.  Because every item writes P into its own
+// slot, the softmax of item n never waits for PV of item n-2: the items of
+// one group, whose rows sit in different TMEM lane quadrants, are worked on
+// by different warps at the same time.
 #include <cuda.h>
+#include <atomic>
 #include <cstring>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -65,15 +72,16 @@ constexpr int kSoftmaxThreads = 128;
 constexpr int kTmemCols = 512;
 constexpr int kRegsControl = 64;
 constexpr int kRegsSoftmax = 176;
-constexpr int kRegsEpilogue = 88;
+constexpr int kRegsEpilogue = 96;
 static_assert(4 * 32 * kRegsControl + 8 * 32 * kRegsSoftmax +
                   4 * 32 * kRegsEpilogue <= 65536,
               "register split must equal the launch allocation");
 constexpr int kRecMax = 16 * (1 + kTileM);  // header + up to 128 tokens
-constexpr int kMetaSlots = 4;
-// per row: partial row index (int64, -1 = none), lse, 1/l * v_scale
+constexpr int kMetaSlots = 3;
+// per row: partial row index (-1 = none; below 2^31, the host checks
+// T * Hq * 16 against it), lse, 1/l
 struct RowMeta {
-  int64_t prow;
+  int32_t prow;
   float lse;
   float inv;
 };
@@ -82,6 +90,10 @@ struct RowMeta {
 constexpr int kBatch = 8;
 constexpr int kStageHdr = 2 * kBatch * 16;                   // int4 per item
 constexpr int kStageTok = 2 * kBatch * 16 * 4;               // 16 ids per item
+// L2 policy hints: K/V pages are read once (evict first); Q rows are read by
+// every item of their tokens and the partials by the combine (evict last).
+// (Prefetching the next items' pages into L2 with bulk prefetches was
+// measured slower: the prefetches queue in the same TMA unit as the loads.)
 
 constexpr int kMaxRing = 6;
 struct Barriers {
@@ -90,45 +102,46 @@ struct Barriers {
   uint64_t kraw_empty[kMaxRing]; // NVFP4: K slot converted
   uint64_t vraw_full[kMaxRing];  // NVFP4: V slot landed
   uint64_t vraw_empty[kMaxRing]; // NVFP4: V slot converted
-  uint64_t k_full[kMaxRing];     // K tile ready (E4M3: K and V landed)
-  uint64_t v_full[kMaxRing];     // NVFP4: V tile converted
-  uint64_t kv_empty[kMaxRing];   // PV done (E4M3: the whole {K, V} slot)
-  uint64_t k_empty[kMaxRing];    // NVFP4: QK done, the K tile is free
+  uint64_t k_full[kMaxRing];     // K tile ready (landed, or converted)
+  uint64_t v_full[kMaxRing];     // V tile ready (landed, or converted)
+  uint64_t v_empty[kMaxRing];    // PV done, the V tile is free
+  uint64_t k_empty[kMaxRing];    // QK done, the K tile is free
   uint64_t q_full[kMaxRing];
-  uint64_t q_empty[kMaxRing];
+  uint64_t q_empty[kMaxRing];    // PV done: the Q/P slot is free
+  uint64_t p_full[kMaxRing];     // P of the slot's item written
   uint64_t s_full[2];
   uint64_t s_free[2];
-  uint64_t p_full[2];
   uint64_t o_full[2];
   uint64_t o_free[2];
   uint64_t meta_full[kMetaSlots];
+  uint64_t meta_free[kMetaSlots];
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
 };
 
 // Shared-memory rings and offsets from the 1024-byte aligned base.
-//   E4M3 pool: 4 {K, V} tile slots filled by TMA; the record ring follows
-//   the tile ring.
-//   NVFP4 pool: the K and V slots of a page-head (9 KB each) land in
-//   rings of 3 each; the softmax group of item j - 2 converts K slot j once
-//   it has written P(j - 2), warps 2-3 convert V slot j once PV(j - 2) is
-//   done; then the 2 KB code x scale lookup table and 2 K and 2 V E4M3
-//   tiles.  A record is read until its softmax starts, which precedes the
-//   conversion of the K and V slots two items later, so a ring of
-//   min(K slots, V slots) + 2 records never overwrites one in use.
+//   E4M3 pool: 3 K tiles and 5 V tiles filled by TMA, then 5 Q/P slots;
+//   the record ring (one record per V slot) follows the tile rings.
+//   NVFP4 pool: the K and V slots of a page-head (9 KB each) land in rings
+//   of 3 each; the softmax group of item j - 2 converts K slot j once it has
+//   written P(j - 2), warps 2-3 convert V slot j once PV(j - 2) is done;
+//   then 2 K and 2 V E4M3 tiles, 4 Q/P slots and the 2 KB code x scale
+//   lookup table.  A record is read until its softmax starts, which
+//   precedes the conversion of the K and V slots two items later, so a ring
+//   of min(K slots, V slots) + 2 records never overwrites one in use.
 template <bool kFp4>
 struct Ring {
-  static constexpr int kv = kFp4 ? 2 : 4;
+  static constexpr int k = kFp4 ? 2 : 3;  // K tiles (free once QK is done)
+  static constexpr int v = kFp4 ? 2 : 5;  // V tiles (free once PV is done)
   static constexpr int kraw = kFp4 ? 3 : 0;
   static constexpr int vraw = kFp4 ? 3 : 0;
-  static constexpr int q = 3;
-  static constexpr int rec = kFp4 ? (kraw < vraw ? kraw : vraw) + 2 : kv;
+  static constexpr int q = kFp4 ? 4 : 5;  // Q/P slots: P(n) overwrites Q(n)
+  static constexpr int rec = kFp4 ? (kraw < vraw ? kraw : vraw) + 2 : v;
   static constexpr int off_k = 0;
-  static constexpr int off_v = off_k + kv * kTile;
-  static constexpr int off_q = off_v + kv * kTile;
-  static constexpr int off_p = off_q + q * kTile;
-  static constexpr int off_kraw = off_p + 2 * kTile;
+  static constexpr int off_v = off_k + k * kTile;
+  static constexpr int off_q = off_v + v * kTile;
+  static constexpr int off_kraw = off_q + q * kTile;
   static constexpr int off_vraw = off_kraw + kraw * kFp4Slot;
   static constexpr int off_lut = off_vraw + vraw * kFp4Slot;
   static constexpr int off_rec = off_lut + (kFp4 ? kFp4LutBytes : 0);
@@ -137,11 +150,11 @@ struct Ring {
       off_meta + kMetaSlots * kTileM * (int)sizeof(RowMeta);
   static constexpr int off_bar = off_stage + kStageHdr + kStageTok;
   static constexpr int bytes = off_bar + (int)sizeof(Barriers) + 1024;
-  static_assert(rec <= kMaxRing && q <= kMaxRing && kv <= kMaxRing &&
+  static_assert(rec <= kMaxRing && q <= kMaxRing && k <= kMaxRing && v <= kMaxRing &&
                     kraw <= kMaxRing && vraw <= kMaxRing,
                 "ring deeper than the barrier arrays");
   static_assert(off_rec % 16 == 0 && off_kraw % 16 == 0 && off_vraw % 16 == 0 &&
-                    kFp4Slot % 16 == 0 && off_meta % 8 == 0,
+                    kFp4Slot % 16 == 0 && off_meta % 4 == 0 && off_stage % 16 == 0,
                 "bulk-copy destinations must be 16-byte aligned");
   static_assert(bytes <= 232448, "shared memory above the 227 KB limit");
 };
@@ -152,9 +165,11 @@ struct Params {
   const int4* records;
   int rec_stride;  // int4 per record
   const int32_t* counters;
-  uint8_t* part_o;      // E4M3 partial rows, V's code units
+  uint8_t* part_o;      // E4M3 partial rows, V's code units, 128 bytes each
+  uint8_t* part_big;    // bf16 overflow rows, 256 bytes each
   float* part_vscale;   // the combine's copy of v_scale
   float* part_lse;
+  float e4m3_limit;     // largest |O| (code units) a half keeps in E4M3
   uint32_t* status;
   int Hq, G;
   int q_tma;       // 1: Q rows by TMA (G % 8 == 0), 0: by cp.async
@@ -162,6 +177,9 @@ struct Params {
   float inv_G;     // 1 / G, for div_G
   float score_log2;
   float v_scale;
+  // wall-time limit of the pipeline waits, in ns (the drains of copies and
+  // MMAs in flight before a CTA exits always keep kWaitLimitNs)
+  uint32_t wait_ns;
 };
 
 __device__ __forceinline__ void set_timeout(Barriers* bars, uint32_t* status) {
@@ -187,8 +205,17 @@ __device__ __forceinline__ int div_G(int lrow, float inv_G) {
 }
 
 // p = 2^(x * c + off) for 32 score columns, packed to E4M3 in pairs and
-// stored as two 16-byte chunks of the 128-byte-swizzled P row; returns the
-// sum of the (unrounded) probabilities.  kMask: columns past kv_lim are 0.
+// stored as two 16-byte chunks of the 128-byte-swizzled P row; adds the
+// (unrounded) probabilities to four independent partial sums (column
+// e % 4 to l[e % 4]), so the additions form four short chains instead of
+// one long one.  kMask: columns past kv_lim are 0.
+// Two floats rounded to bf16 (nearest even) in one word, the first in the
+// low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // Four floats rounded to E4M3 (nearest even, saturating) in one word, the
 // first in the low byte.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
@@ -198,11 +225,10 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 }
 
 template <bool kMask>
-__device__ __forceinline__ float exp_pack32(const uint32_t (&r)[32], int col0,
-                                            int kv_lim, float c, float off,
-                                            uint8_t* prow, int row) {
+__device__ __forceinline__ void exp_pack32(const uint32_t (&r)[32], int col0,
+                                           int kv_lim, float c, float off,
+                                           uint8_t* prow, int row, float (&l)[4]) {
   uint32_t packed[8];
-  float l = 0.f;
 #pragma unroll
   for (int e = 0; e < 32; e += 4) {
     float pv[4];
@@ -211,7 +237,7 @@ __device__ __forceinline__ float exp_pack32(const uint32_t (&r)[32], int col0,
       const float x = __uint_as_float(r[e + u]);
       pv[u] = ex2_approx(fmaf(x, c, off));
       if (kMask && col0 + e + u > kv_lim) pv[u] = 0.f;
-      l += pv[u];
+      l[u] += pv[u];
     }
     const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(pv[0], pv[1]),
                                                  __NV_SATFINITE, __NV_E4M3);
@@ -224,18 +250,18 @@ __device__ __forceinline__ float exp_pack32(const uint32_t (&r)[32], int col0,
       make_uint4(packed[0], packed[1], packed[2], packed[3]);
   *reinterpret_cast<uint4*>(prow + ((c1 ^ (row & 7)) << 4)) =
       make_uint4(packed[4], packed[5], packed[6], packed[7]);
-  return l;
 }
 
+// Row maximum over 32 score columns into four independent partial maxima
+// (column e % 4 to m[e % 4]): four short dependency chains.
 template <bool kMask>
-__device__ __forceinline__ float max32(const uint32_t (&r)[32], int col0,
-                                       int kv_lim, float m) {
+__device__ __forceinline__ void max32(const uint32_t (&r)[32], int col0,
+                                      int kv_lim, float (&m)[4]) {
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
     const float x = __uint_as_float(r[e]);
-    if (!kMask || col0 + e <= kv_lim) m = fmaxf(m, x);
+    if (!kMask || col0 + e <= kv_lim) m[e & 3] = fmaxf(m[e & 3], x);
   }
-  return m;
 }
 
 // One 128-token slot (K or V) of an NVFP4 page-head, dequantised into a
@@ -293,7 +319,8 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
   pdl_wait();
   pdl_trigger();
   if (blockIdx.x == 0 && threadIdx.x == 0) *p.part_vscale = p.v_scale;
-  const int num_work = p.counters[1];
+  // a plan whose construction timed out is incomplete: no work
+  const int num_work = (*p.status & MSA_STATUS_TIMEOUT) ? 0 : p.counters[1];
   // work items are dealt round-robin: CTA b takes items b, b + grid, ...
   // Items of one heavily selected KV row are adjacent in the work list, so
   // contiguous ranges would give a few CTAs all of the full 128-row items.
@@ -315,25 +342,29 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       mbar_init(&bars->vraw_full[s], 1);
       mbar_init(&bars->vraw_empty[s], 2);
     }
-    for (int s = 0; s < L::kv; ++s) {
+    for (int s = 0; s < L::k; ++s) {
       mbar_init(&bars->k_full[s], kFp4 ? 4 : 1);
-      mbar_init(&bars->v_full[s], 2);
-      mbar_init(&bars->kv_empty[s], 1);
       mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < L::v; ++s) {
+      mbar_init(&bars->v_full[s], kFp4 ? 2 : 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     for (int s = 0; s < L::q; ++s) {
       mbar_init(&bars->q_full[s], p.q_tma ? 1 : (kFp4 ? 2 : 32));
       mbar_init(&bars->q_empty[s], 1);
+      mbar_init(&bars->p_full[s], kSoftmaxThreads);
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(&bars->s_full[w], 1);
       mbar_init(&bars->s_free[w], kSoftmaxThreads);
-      mbar_init(&bars->p_full[w], kSoftmaxThreads);
       mbar_init(&bars->o_full[w], 1);
       mbar_init(&bars->o_free[w], kSoftmaxThreads);
     }
-    for (int m = 0; m < kMetaSlots; ++m)
+    for (int m = 0; m < kMetaSlots; ++m) {
       mbar_init(&bars->meta_full[m], kSoftmaxThreads);
+      mbar_init(&bars->meta_free[m], kSoftmaxThreads);
+    }
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -350,8 +381,10 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
   const uint32_t tmem = bars->tmem_base;
 
   // Launched with 128 registers per thread (512 threads); each role's
-  // warpgroup then resizes: softmax 176, epilogue 88, control warps 64
-  // (4*32*64 + 8*32*176 + 4*32*88 = 64512 <= 65536).
+  // warpgroup then resizes: softmax 176, epilogue 96, control warps 64
+  // (4*32*64 + 8*32*176 + 4*32*96 = 65536).  The softmax needs its 176: at
+  // 168 the compiler fits the same code without spills but schedules the
+  // exponentials with far less overlap, and the softmax takes twice as long.
 
   if (warp < 4) {
   setmaxnreg_dec<kRegsControl>();
@@ -369,6 +402,8 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     // token ids at flat entries l, l+32, l+64, l+96 of the kBatch x 16 ids.
     int4* shdr = reinterpret_cast<int4*>(smem + L::off_stage);
     int* stok = reinterpret_cast<int*>(smem + L::off_stage + kStageHdr);
+    const uint64_t pol_stream = l2_policy_evict_first();
+    const uint64_t pol_keep = l2_policy_evict_last();
     auto load_batch = [&](int base, int half) {
       if (lane < kBatch && base + lane < cnt)
         cp_async_16(smem_u32(shdr + half * kBatch + lane),
@@ -393,13 +428,13 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     int issued = 0;
     bool ok_all = true;
     for (int base = 0; ok_all && base < cnt; base += kBatch) {
-      const int half = (base / kBatch) & 1;
-      if (base + kBatch < cnt) load_batch(base + kBatch, half ^ 1);
+      const int buf = (base / kBatch) & 1;
+      if (base + kBatch < cnt) load_batch(base + kBatch, buf ^ 1);
       for (int j = 0; j < kBatch && base + j < cnt; ++j) {
         const int li = base + j;
-        const int ks = li % L::kv, qs = li % L::q, rs = li % L::rec;
-        const int4 hdr = shdr[half * kBatch + j];
-        const int tok = (lane < 16) ? stok[(half * kBatch + j) * 16 + lane] : 0;
+        const int ks = li % L::k, vs = li % L::v, qs = li % L::q, rs = li % L::rec;
+        const int4 hdr = shdr[buf * kBatch + j];
+        const int tok = (lane < 16) ? stok[(buf * kBatch + j) * 16 + lane] : 0;
         int ok = 1;
         if (lane == 0) {
           // NVFP4: the K and V slots of item li - kraw / li - vraw are
@@ -407,18 +442,24 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
           if constexpr (kFp4) {
             if (li >= L::kraw)
               ok = bounded_wait(&bars->kraw_empty[li % L::kraw],
-                                ((li / L::kraw) - 1) & 1, abort, kWaitLimitNs);
+                                ((li / L::kraw) - 1) & 1, abort, p.wait_ns);
             if (ok && li >= L::vraw)
               ok = bounded_wait(&bars->vraw_empty[li % L::vraw],
-                                ((li / L::vraw) - 1) & 1, abort, kWaitLimitNs);
+                                ((li / L::vraw) - 1) & 1, abort, p.wait_ns);
           } else {
-            if (li >= L::kv)
-              ok = bounded_wait(&bars->kv_empty[ks], ((li / L::kv) - 1) & 1,
-                                abort, kWaitLimitNs);
+            // the K tile of item li - k is free once its QK is done, the V
+            // tile (and the record slot, rec == v) of item li - v once its PV
+            // is done
+            if (li >= L::k)
+              ok = bounded_wait(&bars->k_empty[ks], ((li / L::k) - 1) & 1,
+                                abort, p.wait_ns);
+            if (ok && li >= L::v)
+              ok = bounded_wait(&bars->v_empty[vs], ((li / L::v) - 1) & 1,
+                                abort, p.wait_ns);
           }
           if (ok && li >= L::q)
             ok = bounded_wait(&bars->q_empty[qs], ((li / L::q) - 1) & 1,
-                              abort, kWaitLimitNs);
+                              abort, p.wait_ns);
           if (!ok && !*abort) set_timeout(bars, p.status);
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
@@ -441,19 +482,24 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
             bulk_load(smem + L::off_vraw + vr * kFp4Slot, ph + kFp4Slot, kFp4Slot,
                       &bars->vraw_full[vr]);
           } else {
-            mbar_arrive_expect_tx(&bars->k_full[ks], 2 * kTile);
-            tma_load_2d(smem + L::off_k + ks * kTile, &kv_map, &bars->k_full[ks], 0, hdr.x);
-            tma_load_2d(smem + L::off_v + ks * kTile, &kv_map, &bars->k_full[ks], kD, hdr.x);
+            mbar_arrive_expect_tx(&bars->k_full[ks], kTile);
+            tma_load_2d_hint(smem + L::off_k + ks * kTile, &kv_map, &bars->k_full[ks],
+                             0, hdr.x, pol_stream);
+            mbar_arrive_expect_tx(&bars->v_full[vs], kTile);
+            tma_load_2d_hint(smem + L::off_v + vs * kTile, &kv_map, &bars->v_full[vs],
+                             kD, hdr.x, pol_stream);
           }
           if (p.q_tma)
             mbar_arrive_expect_tx(&bars->q_full[qs], (uint32_t)(hdr.y * p.G * 128));
         }
         if (p.q_tma) {
           __syncwarp();
-          if (lane < hdr.y)
-            tma_load_2d(smem + L::off_q + qs * kTile +
-                            ((lane * p.G + row_rotation(li, p.rotate)) & (kTileM - 1)) * 128,
-                        &q_map, &bars->q_full[qs], 0, tok * p.Hq + hdr.w);
+          if (lane < hdr.y) {
+            void* qdst = smem + L::off_q + qs * kTile +
+                         ((lane * p.G + row_rotation(li, p.rotate)) & (kTileM - 1)) * 128;
+            tma_load_2d_hint(qdst, &q_map, &bars->q_full[qs], 0, tok * p.Hq + hdr.w,
+                             pol_keep);
+          }
         }
         issued = li + 1;
       }
@@ -475,8 +521,11 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
           bounded_wait(&bars->vraw_full[li % L::vraw], (li / L::vraw) & 1,
                        nullptr, kWaitLimitNs);
       } else {
-        for (int li = issued > L::kv ? issued - L::kv : 0; li < issued; ++li)
-          bounded_wait(&bars->k_full[li % L::kv], (li / L::kv) & 1,
+        for (int li = issued > L::k ? issued - L::k : 0; li < issued; ++li)
+          bounded_wait(&bars->k_full[li % L::k], (li / L::k) & 1,
+                       nullptr, kWaitLimitNs);
+        for (int li = issued > L::v ? issued - L::v : 0; li < issued; ++li)
+          bounded_wait(&bars->v_full[li % L::v], (li / L::v) & 1,
                        nullptr, kWaitLimitNs);
       }
       if (p.q_tma)
@@ -492,7 +541,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       constexpr uint32_t idesc_pv = idesc_e4m3_f32(128, 128, true);
       bool ok = true;
       auto issue_qk = [&](int li) {
-        const int ks = li % L::kv, qs = li % L::q, w = li & 1;
+        const int ks = li % L::k, qs = li % L::q, w = li & 1;
         tc_fence_after();
         const uint64_t a = smem_desc_sw128(smem_u32(smem + L::off_q + qs * kTile), 16, 1024);
         const uint64_t b = smem_desc_sw128(smem_u32(smem + L::off_k + ks * kTile), 16, 1024);
@@ -502,33 +551,33 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
           mma_f8f6f4(d, a + (uint64_t)(kk * 2), b + (uint64_t)(kk * 2), idesc_qk,
                      kk > 0);
         mma_commit(&bars->s_full[w]);
-        mma_commit(&bars->q_empty[qs]);
-        if constexpr (kFp4) mma_commit(&bars->k_empty[ks]);
+        mma_commit(&bars->k_empty[ks]);
       };
       auto issue_pv = [&](int li) {
-        const int ks = li % L::kv, w = li & 1;
+        const int vs = li % L::v, qs = li % L::q, w = li & 1;
         tc_fence_after();
-        const uint64_t a = smem_desc_sw128(smem_u32(smem + L::off_p + w * kTile), 16, 1024);
-        const uint64_t b = smem_desc_sw128(smem_u32(smem + L::off_v + ks * kTile), 1024, 1024);
+        const uint64_t a = smem_desc_sw128(smem_u32(smem + L::off_q + qs * kTile), 16, 1024);
+        const uint64_t b = smem_desc_sw128(smem_u32(smem + L::off_v + vs * kTile), 1024, 1024);
         const uint32_t d = tmem + (uint32_t)(w * 256 + 128);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // 128 keys = 4 x 32; V rows advance 4 KB
           mma_f8f6f4(d, a + (uint64_t)(kk * 2), b + (uint64_t)(kk * 256),
                      idesc_pv, kk > 0);
         mma_commit(&bars->o_full[w]);
-        mma_commit(&bars->kv_empty[ks]);
+        mma_commit(&bars->v_empty[vs]);
+        mma_commit(&bars->q_empty[qs]);
       };
       // in-order issue of QK(qk) and PV(pv), each as soon as it is ready;
       // QK(n) reuses the S tile of item n-2, free once the softmax has
       // loaded S(n-2) into registers
       int qk = 0, pv = 0;
-      uint64_t idle_since = global_timer_ns();
+      uint32_t idle_since = (uint32_t)global_timer_ns();
       while (pv < cnt) {
         bool progressed = false;
         if (qk < cnt) {
           const int k = qk >> 1;
           if ((k == 0 || mbar_test(&bars->s_free[qk & 1], (k - 1) & 1)) &&
-              mbar_test(&bars->k_full[qk % L::kv], (qk / L::kv) & 1) &&
+              mbar_test(&bars->k_full[qk % L::k], (qk / L::k) & 1) &&
               mbar_test(&bars->q_full[qk % L::q], (qk / L::q) & 1)) {
             issue_qk(qk);
             ++qk;
@@ -537,17 +586,17 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         }
         if (pv < qk) {
           const int w = pv & 1, k = pv >> 1;
-          if (mbar_test(&bars->p_full[w], k & 1) &&
+          if (mbar_test(&bars->p_full[pv % L::q], (pv / L::q) & 1) &&
               (k == 0 || mbar_test(&bars->o_free[w], (k - 1) & 1)) &&
-              (!kFp4 || mbar_test(&bars->v_full[pv % L::kv], (pv / L::kv) & 1))) {
+              mbar_test(&bars->v_full[pv % L::v], (pv / L::v) & 1)) {
             issue_pv(pv);
             ++pv;
             progressed = true;
           }
         }
         if (progressed) {
-          idle_since = global_timer_ns();
-        } else if (*abort || global_timer_ns() - idle_since > kWaitLimitNs) {
+          idle_since = (uint32_t)global_timer_ns();
+        } else if (*abort || (uint32_t)global_timer_ns() - idle_since > p.wait_ns) {
           ok = false;
           break;
         }
@@ -578,9 +627,9 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     };
     auto wait_rec_q = [&](int li) {
       return bounded_wait(&bars->rec_full[li % L::rec], (li / L::rec) & 1, abort,
-                          kWaitLimitNs) &&
+                          p.wait_ns) &&
              (li < L::q || bounded_wait(&bars->q_empty[li % L::q],
-                                        ((li / L::q) - 1) & 1, abort, kWaitLimitNs));
+                                        ((li / L::q) - 1) & 1, abort, p.wait_ns));
     };
     if constexpr (kFp4) {
       // ---------------------------------------------------------- V converter
@@ -590,7 +639,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       const int c = threadIdx.x - 64;
       bool ok = true;
       for (int li = 0; li < cnt; ++li) {
-        const int ks = li % L::kv, r = li % L::vraw;
+        const int vs = li % L::v, r = li % L::vraw;
         if (!p.q_tma) {
           if (!wait_rec_q(li)) { ok = false; break; }
           gather_q(li, c, 64);
@@ -599,18 +648,18 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->q_full[li % L::q]);
         }
-        if (!bounded_wait(&bars->vraw_full[r], (li / L::vraw) & 1, abort, kWaitLimitNs) ||
-            (li >= L::kv && !bounded_wait(&bars->kv_empty[ks], ((li / L::kv) - 1) & 1,
-                                          abort, kWaitLimitNs))) {
+        if (!bounded_wait(&bars->vraw_full[r], (li / L::vraw) & 1, abort, p.wait_ns) ||
+            (li >= L::v && !bounded_wait(&bars->v_empty[vs], ((li / L::v) - 1) & 1,
+                                          abort, p.wait_ns))) {
           ok = false;
           break;
         }
         convert_slot<64>(smem + L::off_vraw + r * kFp4Slot,
-                         smem + L::off_v + ks * kTile, smem + L::off_lut, c);
+                         smem + L::off_v + vs * kTile, smem + L::off_lut, c);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&bars->v_full[ks]);
+          mbar_arrive(&bars->v_full[vs]);
           mbar_arrive(&bars->vraw_empty[r]);
         }
       }
@@ -642,16 +691,15 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     const int row = quad * 32 + lane;    // tile row = TMEM lane
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t s_tmem = tmem + lane_off + (uint32_t)(w * 256);
-    uint8_t* prow_s = smem + L::off_p + w * kTile + row * 128;
     RowMeta* meta = reinterpret_cast<RowMeta*>(smem + L::off_meta);
     // NVFP4: the group dequantises the K slot of each of its items; item j
     // (j >= 2) right after P(j - 2), whose QK has freed the K tile
     auto convert_k = [&](int j) {
       constexpr int R = kFp4 ? L::kraw : 1;  // (E4M3: never called)
-      const int ks = j % L::kv, r = j % R;
-      if (!bounded_wait(&bars->kraw_full[r], (j / R) & 1, abort, kWaitLimitNs) ||
-          (j >= L::kv && !bounded_wait(&bars->k_empty[ks], ((j / L::kv) - 1) & 1,
-                                       abort, kWaitLimitNs))) {
+      const int ks = j % L::k, r = j % R;
+      if (!bounded_wait(&bars->kraw_full[r], (j / R) & 1, abort, p.wait_ns) ||
+          (j >= L::k && !bounded_wait(&bars->k_empty[ks], ((j / L::k) - 1) & 1,
+                                       abort, p.wait_ns))) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         return false;
       }
@@ -672,7 +720,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       if (li >= cnt) break;
       const int rs = li % L::rec;
       if (!bounded_wait(&bars->rec_full[rs], (li / L::rec) & 1, abort,
-                        kWaitLimitNs)) {
+                        p.wait_ns)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
@@ -683,15 +731,15 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       const int i = div_G(lrow, p.inv_G), g = lrow - i * p.G;
       const bool valid = i < hdr.y;
       const bool warp_valid = __any_sync(0xffffffffu, valid);
-      int64_t prow = -1;
+      int32_t prow = -1;
       int kv_lim = 127;
       if (valid) {
         const int4 tok = rec[1 + i];
-        prow = ((int64_t)tok.x * p.Hq + hdr.w + g) * kTopK + tok.z;
+        prow = (tok.x * p.Hq + hdr.w + g) * kTopK + tok.z;
         kv_lim = min(tok.y - hdr.z, 127);
       }
       const bool need_mask = __any_sync(0xffffffffu, valid && kv_lim < 127);
-      if (!bounded_wait(&bars->s_full[w], k & 1, abort, kWaitLimitNs)) {
+      if (!bounded_wait(&bars->s_full[w], k & 1, abort, p.wait_ns)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
@@ -708,43 +756,50 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       // S is in registers: QK of this group's next item may overwrite it
       tc_fence_before();
       mbar_arrive(&bars->s_free[w]);
-      // the P tile is free once PV of this group's previous item is done
-      if (k > 0 &&
-          !bounded_wait(&bars->o_full[w], (k - 1) & 1, abort, kWaitLimitNs)) {
-        if (lane == 0 && !*abort) set_timeout(bars, p.status);
-        break;
-      }
+      // P goes into the item's own Q/P slot: Q is dead once QK has completed
+      // (s_full), so nothing here waits for an earlier item's PV
+      uint8_t* prow_s = smem + L::off_q + (li % L::q) * kTile + row * 128;
       float m2 = -INFINITY, l = 0.f;
       if (warp_valid) {
-        float m = -INFINITY;
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (need_mask) {
-          m = max32<true>(r0, 0, kv_lim, m);
-          m = max32<true>(r1, 32, kv_lim, m);
-          m = max32<true>(r2, 64, kv_lim, m);
-          m = max32<true>(r3, 96, kv_lim, m);
+          max32<true>(r0, 0, kv_lim, mq);
+          max32<true>(r1, 32, kv_lim, mq);
+          max32<true>(r2, 64, kv_lim, mq);
+          max32<true>(r3, 96, kv_lim, mq);
         } else {
-          m = max32<false>(r0, 0, kv_lim, m);
-          m = max32<false>(r1, 32, kv_lim, m);
-          m = max32<false>(r2, 64, kv_lim, m);
-          m = max32<false>(r3, 96, kv_lim, m);
+          max32<false>(r0, 0, kv_lim, mq);
+          max32<false>(r1, 32, kv_lim, mq);
+          max32<false>(r2, 64, kv_lim, mq);
+          max32<false>(r3, 96, kv_lim, mq);
         }
+        const float m = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
         m2 = m * p.score_log2;
         // p = 2^(x * c - m2 + 8): probabilities scaled by 256 so that small
         // ones stay out of E4M3's subnormal range; l and O carry the same
         // factor, which cancels.
         const float off = (m2 == -INFINITY) ? 0.f : 8.f - m2;
         const float c = p.score_log2;
+        float lq[4] = {0.f, 0.f, 0.f, 0.f};
         if (need_mask) {
-          l += exp_pack32<true>(r0, 0, kv_lim, c, off, prow_s, row);
-          l += exp_pack32<true>(r1, 32, kv_lim, c, off, prow_s, row);
-          l += exp_pack32<true>(r2, 64, kv_lim, c, off, prow_s, row);
-          l += exp_pack32<true>(r3, 96, kv_lim, c, off, prow_s, row);
+          exp_pack32<true>(r0, 0, kv_lim, c, off, prow_s, row, lq);
+          exp_pack32<true>(r1, 32, kv_lim, c, off, prow_s, row, lq);
+          exp_pack32<true>(r2, 64, kv_lim, c, off, prow_s, row, lq);
+          exp_pack32<true>(r3, 96, kv_lim, c, off, prow_s, row, lq);
         } else {
-          l += exp_pack32<false>(r0, 0, kv_lim, c, off, prow_s, row);
-          l += exp_pack32<false>(r1, 32, kv_lim, c, off, prow_s, row);
-          l += exp_pack32<false>(r2, 64, kv_lim, c, off, prow_s, row);
-          l += exp_pack32<false>(r3, 96, kv_lim, c, off, prow_s, row);
+          exp_pack32<false>(r0, 0, kv_lim, c, off, prow_s, row, lq);
+          exp_pack32<false>(r1, 32, kv_lim, c, off, prow_s, row, lq);
+          exp_pack32<false>(r2, 64, kv_lim, c, off, prow_s, row, lq);
+          exp_pack32<false>(r3, 96, kv_lim, c, off, prow_s, row, lq);
         }
+        l = (lq[0] + lq[1]) + (lq[2] + lq[3]);
+      }
+      // the row-meta slot is free once the epilogue has read item li - 4's
+      if (li >= kMetaSlots &&
+          !bounded_wait(&bars->meta_free[li % kMetaSlots], ((li / kMetaSlots) - 1) & 1,
+                        abort, p.wait_ns)) {
+        if (lane == 0 && !*abort) set_timeout(bars, p.status);
+        break;
       }
       RowMeta mt;
       mt.prow = prow;
@@ -754,7 +809,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       meta[(li % kMetaSlots) * kTileM + row] = mt;
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars->p_full[w]);
+      mbar_arrive(&bars->p_full[li % L::q]);
       mbar_arrive(&bars->meta_full[li % kMetaSlots]);
       if constexpr (kFp4) {
         if (li + 2 < cnt && !convert_k(li + 2)) break;
@@ -767,17 +822,19 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     const int row = quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const RowMeta* meta = reinterpret_cast<const RowMeta*>(smem + L::off_meta);
+    const uint64_t pol_keep = l2_policy_evict_last();
     for (int li = 0; li < cnt; ++li) {
       const int w = li & 1, k = li >> 1;
       if (!bounded_wait(&bars->meta_full[li % kMetaSlots],
-                        (li / kMetaSlots) & 1, abort, kWaitLimitNs)) {
+                        (li / kMetaSlots) & 1, abort, p.wait_ns)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
       const RowMeta mt = meta[(li % kMetaSlots) * kTileM + row];
+      mbar_arrive(&bars->meta_free[li % kMetaSlots]);
       const bool valid = mt.prow >= 0;
       const bool warp_valid = __any_sync(0xffffffffu, valid);
-      if (!bounded_wait(&bars->o_full[w], k & 1, abort, kWaitLimitNs)) {
+      if (!bounded_wait(&bars->o_full[w], k & 1, abort, p.wait_ns)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
@@ -793,29 +850,72 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
           tmem_ld32(o_tmem + half * 64 + 32, rb);
           tmem_wait_ld();
           if (valid) {
-            // the normalised row in V's code units is a convex combination
-            // of E4M3 V codes, so it stays within E4M3's range; word k holds
-            // columns 4k .. 4k+3 of this half
-            uint32_t o[16];
+            // The normalised row in V's code units is a convex combination
+            // of E4M3 V codes, so it stays within E4M3's range.  A half whose
+            // largest magnitude is at most p.e4m3_limit (0.5 in real units)
+            // is kept in E4M3 (rounding error at most 2^-4 of that, 0.031).
+            // A larger one goes to the bf16 overflow rows (error at most
+            // 2^-9 of the value), and its E4M3 half is filled with the NaN
+            // code, which no partial produces (the conversion saturates), as
+            // the marker the combine looks for.  So the partials never cost
+            // more than a small fraction of the acceptance rule however large
+            // the output, and the common case moves 64 bytes per half.
+            float mx[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              o[k] = pack_e4m3x4(__uint_as_float(ra[4 * k]) * mt.inv,
-                                 __uint_as_float(ra[4 * k + 1]) * mt.inv,
-                                 __uint_as_float(ra[4 * k + 2]) * mt.inv,
-                                 __uint_as_float(ra[4 * k + 3]) * mt.inv);
-              o[8 + k] = pack_e4m3x4(__uint_as_float(rb[4 * k]) * mt.inv,
-                                     __uint_as_float(rb[4 * k + 1]) * mt.inv,
-                                     __uint_as_float(rb[4 * k + 2]) * mt.inv,
-                                     __uint_as_float(rb[4 * k + 3]) * mt.inv);
+            for (int k = 0; k < 32; ++k) {
+              mx[k & 3] = fmaxf(mx[k & 3], fabsf(__uint_as_float(ra[k])));
+              mx[k & 3] = fmaxf(mx[k & 3], fabsf(__uint_as_float(rb[k])));
             }
-            // whole 32-byte sectors: the row's half is 64 bytes at a
-            // 64-byte aligned offset of a 128-byte row
+            const float amax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * mt.inv;
             uint8_t* d = dst + half * 64;
-            st_global_v8(d, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
-            st_global_v8(d + 32, o[8], o[9], o[10], o[11], o[12], o[13], o[14], o[15]);
+            if (amax <= p.e4m3_limit) {
+              // word k holds columns 4k .. 4k+3 of this half; 64 bytes as
+              // two whole 32-byte sectors
+              uint32_t o[16];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                o[k] = pack_e4m3x4(__uint_as_float(ra[4 * k]) * mt.inv,
+                                   __uint_as_float(ra[4 * k + 1]) * mt.inv,
+                                   __uint_as_float(ra[4 * k + 2]) * mt.inv,
+                                   __uint_as_float(ra[4 * k + 3]) * mt.inv);
+                o[8 + k] = pack_e4m3x4(__uint_as_float(rb[4 * k]) * mt.inv,
+                                       __uint_as_float(rb[4 * k + 1]) * mt.inv,
+                                       __uint_as_float(rb[4 * k + 2]) * mt.inv,
+                                       __uint_as_float(rb[4 * k + 3]) * mt.inv);
+              }
+              st_global_v8_hint(d, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7],
+                                pol_keep);
+              st_global_v8_hint(d + 32, o[8], o[9], o[10], o[11], o[12], o[13], o[14],
+                                o[15], pol_keep);
+            } else {
+              constexpr uint32_t kNaN4 = 0x7F7F7F7Fu;
+              st_global_v8_hint(d, kNaN4, kNaN4, kNaN4, kNaN4, kNaN4, kNaN4, kNaN4, kNaN4,
+                                pol_keep);
+              st_global_v8_hint(d + 32, kNaN4, kNaN4, kNaN4, kNaN4, kNaN4, kNaN4, kNaN4,
+                                kNaN4, pol_keep);
+              // word k holds columns 2k, 2k+1; 128 bytes as four sectors
+              uint8_t* g = p.part_big + mt.prow * (int64_t)(2 * kD) + half * 128;
+              uint32_t o[16];
+#pragma unroll
+              for (int k = 0; k < 16; ++k)
+                o[k] = pack_bf16x2(__uint_as_float(ra[2 * k]) * mt.inv,
+                                   __uint_as_float(ra[2 * k + 1]) * mt.inv);
+              st_global_v8_hint(g, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7],
+                                pol_keep);
+              st_global_v8_hint(g + 32, o[8], o[9], o[10], o[11], o[12], o[13], o[14],
+                                o[15], pol_keep);
+#pragma unroll
+              for (int k = 0; k < 16; ++k)
+                o[k] = pack_bf16x2(__uint_as_float(rb[2 * k]) * mt.inv,
+                                   __uint_as_float(rb[2 * k + 1]) * mt.inv);
+              st_global_v8_hint(g + 64, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7],
+                                pol_keep);
+              st_global_v8_hint(g + 96, o[8], o[9], o[10], o[11], o[12], o[13], o[14],
+                                o[15], pol_keep);
+            }
           }
         }
-        if (valid) p.part_lse[mt.prow] = mt.lse;
+        if (valid) st_global_f32_hint(p.part_lse + mt.prow, mt.lse, pol_keep);
       }
       tc_fence_before();
       mbar_arrive(&bars->o_free[w]);
@@ -865,16 +965,22 @@ bool encode_rows(EncodeTiledFn enc, CUtensorMap* map, const void* base,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The dynamic shared-memory limit is a per-device function attribute: set
+// it once for every device the kernel is launched on.
 template <bool kFp4>
 cudaError_t launch_kernel(const CUtensorMap& kv_map, const CUtensorMap& q_map,
                           const Params& p, int64_t grid, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attention_kernel<kFp4>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Ring<kFp4>::bytes);
+  constexpr int kMaxDevices = 64;
+  static std::atomic<bool> attr_set[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices || !attr_set[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(attention_kernel<kFp4>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Ring<kFp4>::bytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    if (dev >= 0 && dev < kMaxDevices) attr_set[dev].store(true, std::memory_order_release);
   }
   return launch_pdl(attention_kernel<kFp4>, dim3((unsigned)grid), dim3(kThreads),
                     Ring<kFp4>::bytes, stream, kv_map, q_map, p);
@@ -914,6 +1020,8 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   p.part_o = a.part_o;
   p.part_vscale = a.part_vscale;
   p.part_lse = a.part_lse;
+  p.part_big = a.part_big;
+  p.e4m3_limit = kE4M3PartialLimit / a.v_scale;
   p.status = pl.status;
   p.Hq = (int)pl.Hq;
   p.G = G;
@@ -922,6 +1030,7 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   p.q_tma = q_tma ? 1 : 0;
   p.score_log2 = a.score_log2;
   p.v_scale = a.v_scale;
+  p.wait_ns = (uint32_t)std::min<uint64_t>(pipeline_wait_limit_ns(), kWaitLimitNs);
 
   const int64_t grid = std::min<int64_t>(num_sms(), pl.max_work);
   return fp4 ? launch_kernel<true>(kv_map, q_map, p, grid, stream)

@@ -14,6 +14,7 @@
 #include <cuda_fp8.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace msa {
 namespace {
@@ -93,12 +94,17 @@ combine_kernel(const TIn* __restrict__ part_o, const float* __restrict__ part_ls
 
 // The attention path's combine: 16 slots per row, the slot mask of the
 // row's (token, KV head) says which slots hold a partial.  Partial rows are
-// E4M3 in V's code units (128 bytes); the V scale is applied here, read from
-// the device scalar the attention kernel left.  A half-warp per row, each
-// lane owning 8 of the 128 columns: one 8-byte load per slot, all of a row's
-// loads issued before any is used.
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+// E4M3 in V's code units (128 bytes); a half whose bytes are all the NaN
+// code was kept in bf16 in the slot's overflow row instead (the attention
+// kernel does that for halves of large magnitude).  The V scale is applied
+// here, read from the device scalar the attention kernel left.  A
+// half-warp per row, each lane owning 8 of the 128 columns: one 8-byte load
+// per slot, all of a row's loads issued before any is used, and a 16-byte
+// overflow load for a marked half.  The partials are read once here: they
+// are evicted from L2 first.
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, 4)
 combine16_kernel(const uint8_t* __restrict__ part_o,
+                 const uint8_t* __restrict__ part_big,
                  const float* __restrict__ part_lse,
                  const float* __restrict__ v_scale_ptr,
                  const uint16_t* __restrict__ slot_mask, int64_t group,
@@ -112,18 +118,19 @@ combine16_kernel(const uint8_t* __restrict__ part_o,
                     (lane >> 4);
   const bool live = r < rows;
   const uint32_t mask = live ? slot_mask[r / group] : 0u;
+  const uint64_t pol = l2_policy_evict_first();
   const uint8_t* base = part_o + r * (int64_t)kTopK * kD + sub * 8;
   uint2 v[kTopK];
 #pragma unroll
   for (int j = 0; j < kTopK; ++j) {
     if ((mask >> j) & 1u)
-      v[j] = *reinterpret_cast<const uint2*>(base + j * kD);
+      v[j] = ld_global_v2_hint(base + j * kD, pol);
     else
       v[j] = make_uint2(0u, 0u);
   }
   // lane `sub` of the half-warp holds slot sub's lse
   float l = -INFINITY;
-  if ((mask >> sub) & 1u) l = part_lse[r * kTopK + sub];
+  if ((mask >> sub) & 1u) l = ld_global_f32_hint(part_lse + r * kTopK + sub, pol);
   float M = l;
 #pragma unroll
   for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -131,18 +138,17 @@ combine16_kernel(const uint8_t* __restrict__ part_o,
   float sum = wl;
 #pragma unroll
   for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (!live) return;
-  uint4* dst = reinterpret_cast<uint4*>(out + r * kD + sub * 8);
-  if (M == -INFINITY) {
-    *dst = make_uint4(0u, 0u, 0u, 0u);
-    if (lse_out && sub == 0) lse_out[r] = -INFINITY;
-    return;
-  }
-  const float inv = *v_scale_ptr / sum;
+  // every lane runs the loops below (their shuffles span the warp); rows
+  // past the end or with no partial are written after them
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  uint32_t marked = 0;  // slots whose half (this lane's) is in the overflow rows
 #pragma unroll
   for (int j = 0; j < kTopK; ++j) {
     const float wj = __shfl_sync(0xffffffffu, wl, (lane & 16) + j);
+    if (v[j].x == 0x7F7F7F7Fu) {
+      marked |= 1u << j;
+      continue;
+    }
     const uint32_t w2[2] = {v[j].x, v[j].y};
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
@@ -158,6 +164,33 @@ combine16_kernel(const uint8_t* __restrict__ part_o,
       acc[4 * u + 3] = fmaf(wj, b.y, acc[4 * u + 3]);
     }
   }
+  // halves kept in bf16 (rare): this lane's 8 columns are 16 bytes of the
+  // slot's overflow row
+  // (the loop runs over the slots marked anywhere in the warp, so that every
+  // lane takes part in the shuffle that fetches the slot's weight)
+  const uint8_t* big = part_big + r * (int64_t)kTopK * (2 * kD) + sub * 16;
+  marked &= mask;
+  for (uint32_t bits = __reduce_or_sync(0xffffffffu, marked); bits; bits &= bits - 1) {
+    const int j = __ffs(bits) - 1;
+    const float wj = __shfl_sync(0xffffffffu, wl, (lane & 16) + j);
+    if ((marked >> j) & 1u) {
+      const uint4 b4 = ld_global_v4_hint(big + j * (2 * kD), pol);
+      const uint32_t w4[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc[2 * u] = fmaf(wj, __uint_as_float(w4[u] << 16), acc[2 * u]);
+        acc[2 * u + 1] = fmaf(wj, __uint_as_float(w4[u] & 0xFFFF0000u), acc[2 * u + 1]);
+      }
+    }
+  }
+  if (!live) return;
+  uint4* dst = reinterpret_cast<uint4*>(out + r * kD + sub * 8);
+  if (M == -INFINITY) {
+    *dst = make_uint4(0u, 0u, 0u, 0u);
+    if (lse_out && sub == 0) lse_out[r] = -INFINITY;
+    return;
+  }
+  const float inv = *v_scale_ptr / sum;
   uint32_t o[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
@@ -230,15 +263,16 @@ cudaError_t launch_combine(const void* part_o, int part_dtype,
                     S, out, lse);
 }
 
-cudaError_t launch_combine_attn(const uint8_t* part_o, const float* part_lse,
-                                const float* v_scale, const uint16_t* slot_mask,
-                                int64_t group, int64_t rows, uint16_t* out,
-                                float* lse, cudaStream_t stream) {
+cudaError_t launch_combine_attn(const uint8_t* part_o, const uint8_t* part_big,
+                                const float* part_lse, const float* v_scale,
+                                const uint16_t* slot_mask, int64_t group,
+                                int64_t rows, uint16_t* out, float* lse,
+                                cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   return launch_pdl(combine16_kernel,
                     dim3((unsigned)ceil_div(rows, 2 * kWarpsPerBlock)),
-                    dim3(kWarpsPerBlock * 32), 0, stream, part_o, part_lse, v_scale,
-                    slot_mask, group, rows, out, lse);
+                    dim3(kWarpsPerBlock * 32), 0, stream, part_o, part_big, part_lse,
+                    v_scale, slot_mask, group, rows, out, lse);
 }
 
 cudaError_t launch_decode_seqlens(const int32_t* seq_lens, int64_t B,

@@ -16,13 +16,25 @@ constexpr int kPage = MSA_PAGE_SIZE;  // tokens per KV page
 constexpr int kTopK = MSA_TOPK;       // pages per (token, KV head)
 constexpr int kTileM = 128;           // MMA rows per work item (tokens x G)
 
-// Rows per CTA in the plan's fill kernel, and in its count kernel (a
-// half-warp per row there).
-constexpr int kPlanTile = 256;
-constexpr int kCountTile = 16;
+// The plan's rows kernel: rows per round (a half-warp per row), its
+// threads, and the largest number of tiles (CTAs).  A tile is a multiple of
+// kRowTile rows, as few as keep the tile count within kMaxRowTiles: every
+// tile adds up the totals of all tiles in front of it.
+constexpr int kRowTile = 16;
+constexpr int kRowThreads = 256;
+constexpr int kMaxRowTiles = 512;
+__host__ __device__ inline int64_t plan_tile_rows(int64_t rows) {
+  const int64_t rounds = (rows + (int64_t)kRowTile * kMaxRowTiles - 1) /
+                         ((int64_t)kRowTile * kMaxRowTiles);
+  return kRowTile * (rounds > 0 ? rounds : 1);
+}
 
 // Wall-time bound of every device-side wait (about a second).
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+constexpr uint32_t kWaitLimitNs = 1000000000u;
+
+// The limit the attention kernel's pipeline waits use: kWaitLimitNs unless a
+// test has set a shorter one (msa_test_set_wait_limit_ns).
+uint64_t pipeline_wait_limit_ns();
 
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) {
   return (a + b - 1) / b;
@@ -31,6 +43,13 @@ __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) {
 // Launchers (each returns a cudaError_t from the launch).
 cudaError_t launch_plan(const msa_plan_t& plan, const int32_t* topk,
                         const int32_t* block_table, cudaStream_t stream);
+
+// Split partials: per (token, query head, top-k slot) a 128-byte E4M3 row
+// in V's code units, two halves of 64 columns.  A half whose largest
+// magnitude, in real units, is above kE4M3PartialLimit is kept in bf16 in
+// the slot's 256-byte overflow row instead, and its E4M3 half holds the NaN
+// code 0x7F in every byte as the marker.
+constexpr float kE4M3PartialLimit = 0.5f;
 
 struct AttnArgs {
   const uint8_t* q;
@@ -43,6 +62,7 @@ struct AttnArgs {
   const msa_plan_t* plan;
   uint8_t* part_o;    // [T][Hq][16][128] E4M3: normalised partial outputs in
                       // V's code units (a convex combination of V codes)
+  uint8_t* part_big;  // [T][Hq][16][128] bf16 overflow rows (see above)
   float* part_lse;    // [T][Hq][16]
   float* part_vscale; // one float: v_scale, left here for the combine
   int kv_format;      // MSA_KV_E4M3: kv is the E4M3 pool; MSA_KV_NVFP4: kv
@@ -58,13 +78,15 @@ cudaError_t launch_combine(const void* part_o, int part_dtype,
                            const float* part_lse, int64_t rows, int64_t splits,
                            uint16_t* out, float* lse, cudaStream_t stream);
 
-// Combine of the attention kernel's partials: 16 slots per row, E4M3 O in
-// V's code units scaled by *v_scale, the mask of row r is
+// Combine of the attention kernel's partials: 16 slots per row, O in V's
+// code units (each half E4M3, or bf16 in the overflow rows where the E4M3
+// half holds the marker) scaled by *v_scale, the mask of row r is
 // slot_mask[r / group] and empty slots are not read.
-cudaError_t launch_combine_attn(const uint8_t* part_o, const float* part_lse,
-                                const float* v_scale, const uint16_t* slot_mask,
-                                int64_t group, int64_t rows, uint16_t* out,
-                                float* lse, cudaStream_t stream);
+cudaError_t launch_combine_attn(const uint8_t* part_o, const uint8_t* part_big,
+                                const float* part_lse, const float* v_scale,
+                                const uint16_t* slot_mask, int64_t group,
+                                int64_t rows, uint16_t* out, float* lse,
+                                cudaStream_t stream);
 
 cudaError_t launch_decode_seqlens(const int32_t* seq_lens, int64_t B,
                                   int64_t n, int32_t* cu_q, int32_t* cu_k,

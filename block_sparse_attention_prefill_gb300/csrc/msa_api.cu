@@ -2,6 +2,7 @@
 // checks, workspace layout and the launch sequence of each call.  Nothing
 // here allocates device memory or synchronises, except msa_read_status /
 // msa_read_counters, which are documented to synchronise.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -9,6 +10,15 @@
 #include "common.cuh"
 
 namespace msa {
+
+namespace {
+std::atomic<uint64_t> g_test_wait_ns{0};
+}  // namespace
+
+uint64_t pipeline_wait_limit_ns() {
+  const uint64_t t = g_test_wait_ns.load(std::memory_order_relaxed);
+  return t ? t : kWaitLimitNs;
+}
 
 int num_sms() {
   static int cached[64] = {0};
@@ -67,7 +77,7 @@ int plan_shape(int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t R,
   s->C = kTileM / G;
   s->W = 4 * ceil_div(max_q, 128);  // 32-bit words, a multiple of 4
   s->rows = Hkv * R;
-  s->ntiles = ceil_div(s->rows, kCountTile);
+  s->ntiles = ceil_div(s->rows, plan_tile_rows(s->rows));
   s->max_nnz = T * Hkv * kTopK;
   s->max_work = ceil_div(s->max_nnz, s->C) + std::min(s->rows, s->max_nnz);
   // every index the kernels form must fit in int32
@@ -89,7 +99,7 @@ size_t plan_layout(const PlanShape& s, void* base, msa_plan_t* pl) {
   int32_t* word_pre = c.take<int32_t>(s.rows * s.W);
   int32_t* row_cnt = c.take<int32_t>(s.rows);
   int32_t* row_wptr = c.take<int32_t>(s.rows);
-  int32_t* tile_sums = c.take<int32_t>(2 * s.ntiles + 2);
+  uint64_t* tile_state = c.take<uint64_t>(s.ntiles);
   int32_t* row_ptr = c.take<int32_t>(s.rows + 1);
   int32_t* q_idx = c.take<int32_t>(s.max_nnz);
   uint8_t* slot = c.take<uint8_t>(s.max_nnz);
@@ -104,9 +114,9 @@ size_t plan_layout(const PlanShape& s, void* base, msa_plan_t* pl) {
     pl->word_pre = word_pre;
     pl->row_cnt = row_cnt;
     pl->row_wptr = row_wptr;
+    pl->tile_state = tile_state;
     pl->records = records;
     pl->record_bytes = record_bytes(s);
-    pl->tile_sums = tile_sums;
     pl->row_ptr = row_ptr;
     pl->q_idx = q_idx;
     pl->slot = slot;
@@ -118,15 +128,28 @@ size_t plan_layout(const PlanShape& s, void* base, msa_plan_t* pl) {
   return c.off;
 }
 
-size_t prefill_layout(int64_t T, int64_t Hq, void* base, uint8_t** part_o,
-                      float** part_lse, float** part_vscale) {
+struct PartialBufs {
+  uint8_t* o = nullptr;
+  uint8_t* big = nullptr;
+  float* lse = nullptr;
+  float* vscale = nullptr;
+};
+
+// The prefill workspace: v_scale, then per (token, query head, top-k slot)
+// a 128-byte E4M3 partial row, its lse, and a 256-byte bf16 overflow row
+// (written only for halves of large magnitude).
+size_t prefill_layout(int64_t T, int64_t Hq, void* base, PartialBufs* b) {
   Carver c(base);
   float* vs = c.take<float>(1);
   uint8_t* po = c.take<uint8_t>(T * Hq * kTopK * kD);
   float* pl = c.take<float>(T * Hq * kTopK);
-  if (part_o) *part_o = po;
-  if (part_lse) *part_lse = pl;
-  if (part_vscale) *part_vscale = vs;
+  uint8_t* pb = c.take<uint8_t>(T * Hq * kTopK * 2 * kD);
+  if (b) {
+    b->o = po;
+    b->big = pb;
+    b->lse = pl;
+    b->vscale = vs;
+  }
   return c.off;
 }
 
@@ -196,7 +219,7 @@ int attention_impl(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
       !(softmax_scale > 0.f) || !std::isfinite(q_scale * k_scale * softmax_scale))
     return MSA_ERR_SHAPE;
   if (!aligned(q, 16) || !aligned(kv, 16)) return MSA_ERR_ALIGN;
-  const size_t need = prefill_layout(T, Hq, nullptr, nullptr, nullptr, nullptr);
+  const size_t need = prefill_layout(T, Hq, nullptr, nullptr);
   if (!ws || ws_bytes < need) return MSA_ERR_WORKSPACE;
   if (!aligned(ws, kAlign)) return MSA_ERR_ALIGN;
   AttnArgs a;
@@ -210,7 +233,12 @@ int attention_impl(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
   a.bt_stride = bt_stride;
   a.plan = plan;
   a.kv_format = kv_format;
-  prefill_layout(T, Hq, ws, &a.part_o, &a.part_lse, &a.part_vscale);
+  PartialBufs pb;
+  prefill_layout(T, Hq, ws, &pb);
+  a.part_o = pb.o;
+  a.part_big = pb.big;
+  a.part_lse = pb.lse;
+  a.part_vscale = pb.vscale;
   if (num_pages == 0) return MSA_OK;
   return cuda_rc(launch_attention(a, stream));
 }
@@ -222,14 +250,12 @@ int prefill_combine_impl(const msa_plan_t* plan, void* ws, size_t ws_bytes,
   if (T == 0) return MSA_OK;
   if (!out) return MSA_ERR_NULL;
   if (!aligned(out, 8) || !aligned(lse, 4)) return MSA_ERR_ALIGN;
-  const size_t need = prefill_layout(T, Hq, nullptr, nullptr, nullptr, nullptr);
+  const size_t need = prefill_layout(T, Hq, nullptr, nullptr);
   if (!ws || ws_bytes < need) return MSA_ERR_WORKSPACE;
   if (!aligned(ws, kAlign)) return MSA_ERR_ALIGN;
-  uint8_t* part_o;
-  float* part_lse;
-  float* part_vscale;
-  prefill_layout(T, Hq, ws, &part_o, &part_lse, &part_vscale);
-  return cuda_rc(launch_combine_attn(part_o, part_lse, part_vscale, plan->slot_mask,
+  PartialBufs pb;
+  prefill_layout(T, Hq, ws, &pb);
+  return cuda_rc(launch_combine_attn(pb.o, pb.big, pb.lse, pb.vscale, plan->slot_mask,
                                      Hq / plan->Hkv, T * Hq, out, lse, stream));
 }
 
@@ -266,7 +292,7 @@ int decode_layout(int64_t B, int64_t n, int64_t Hq, int64_t Hkv,
   if (rc) return rc;
   d->cu_bytes = align_up(2 * (size_t)(B + 1) * sizeof(int32_t));
   d->plan_bytes = plan_layout(s, nullptr, nullptr);
-  d->prefill_bytes = prefill_layout(B * n, Hq, nullptr, nullptr, nullptr, nullptr);
+  d->prefill_bytes = prefill_layout(B * n, Hq, nullptr, nullptr);
   d->total = d->cu_bytes + d->plan_bytes + d->prefill_bytes;
   return MSA_OK;
 }
@@ -338,6 +364,8 @@ const char* msa_status_string(int code) {
     case MSA_ERR_NULL: return "a required pointer is NULL";
     case MSA_ERR_TOO_LARGE:
       return "problem needs more scratch than msa_decode_noalloc's fixed array";
+    case MSA_ERR_BUSY:
+      return "msa_decode_noalloc is already being called from another thread";
     default: return "unknown status";
   }
 }
@@ -368,7 +396,7 @@ int msa_plan(const int32_t* topk, const int32_t* cu_seqlens_q,
 int msa_prefill_workspace_bytes(int64_t T, int64_t Hq, size_t* bytes) {
   if (!bytes) return MSA_ERR_NULL;
   if (T < 0 || Hq <= 0 || T * Hq >= kI32Max / kTopK) return MSA_ERR_SHAPE;
-  *bytes = prefill_layout(T, Hq, nullptr, nullptr, nullptr, nullptr);
+  *bytes = prefill_layout(T, Hq, nullptr, nullptr);
   return MSA_OK;
 }
 
@@ -500,25 +528,35 @@ namespace {
 
 // Scratch of msa_decode_noalloc: one fixed array on every GPU that loads this
 // library, kept until the process exits.  Host code must not use its name
-// as a device address; it asks the runtime for the address once per device.
+// as a device address; it asks the runtime for the address instead.
 static __device__ __align__(256) unsigned char
     g_decode_scratch[MSA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+std::atomic<int> g_noalloc_busy{0};
 
-int decode_scratch(void** ptr) {
+// The array's device address in the current device's context.  Outside
+// stream capture it is looked up on every call (the runtime call is cheap
+// once the module is loaded, and a fresh lookup stays right after a context
+// is torn down and rebuilt); under capture, where the first lookup's module
+// load must not happen, the address from this device's last call outside
+// capture is used.
+int decode_scratch(cudaStream_t stream, void** ptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MSA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MSA_ERR_UNSUPPORTED;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return MSA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (cs == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess ||
-        p == nullptr)
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr)
       return MSA_ERR_CUDA;
     g_scratch_ptr[dev] = p;
+  } else if (g_scratch_ptr[dev] == nullptr) {
+    return MSA_ERR_CUDA;  // no call outside capture on this device yet
   }
   *ptr = g_scratch_ptr[dev];
   return MSA_OK;
@@ -540,13 +578,24 @@ int msa_decode_noalloc(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
   if (rc) return rc;
   if (need > (size_t)MSA_NOALLOC_SCRATCH_BYTES) return MSA_ERR_TOO_LARGE;
   if (B == 0) return MSA_OK;
+  // a second host thread entering while one is enqueueing would share the
+  // array: refuse it instead of letting the two overwrite each other
+  int expected = 0;
+  if (!g_noalloc_busy.compare_exchange_strong(expected, 1)) return MSA_ERR_BUSY;
   void* scratch = nullptr;
-  rc = decode_scratch(&scratch);
-  if (rc) return rc;
-  return msa_decode(q, kv, num_pages, q_scale, k_scale, v_scale, softmax_scale,
+  rc = decode_scratch(static_cast<cudaStream_t>(stream), &scratch);
+  if (rc == MSA_OK)
+    rc = msa_decode(q, kv, num_pages, q_scale, k_scale, v_scale, softmax_scale,
                     topk, block_table, bt_stride, seq_lens, B, n, Hq, Hkv,
                     max_seqlen_k, scratch, MSA_NOALLOC_SCRATCH_BYTES, out, lse,
                     nullptr, stream);
+  g_noalloc_busy.store(0);
+  return rc;
+}
+
+int msa_test_set_wait_limit_ns(uint64_t ns) {
+  g_test_wait_ns.store(ns, std::memory_order_relaxed);
+  return MSA_OK;
 }
 
 int msa_read_status(const msa_plan_t* plan, uint32_t* status) {

@@ -5,23 +5,25 @@
 // total_kv_blocks, qhead_per_kv, return_schedule=True); vLLM PR 60930,
 // Details / "Host sync": the plan stays on the device, no host copy.)
 //
-// Steps, all on `stream`, no host synchronisation; every kernel after the
-// first is a programmatic dependent launch (its launch overlaps the tail of
-// the kernel before it, its work does not):
+// Four kernels, all on `stream`, no host synchronisation; every kernel
+// after the first is a programmatic dependent launch (its launch overlaps
+// the tail of the kernel before it, its work does not):
 //   prep     CTA 0: per-request row offsets (sum of page counts), checks,
-//            status word; every CTA: clears its share of the (row, token)
-//            membership bitmap
+//            status word, counters; every CTA: clears its share of the
+//            (row, token) membership bitmap and of the tile states
 //   mark     one thread per top-k entry: validate the id, drop repeats, set
 //            one bit per kept page in the membership bitmap; the (token,
-//            KV head) list's 16 threads together write its slot mask.  This is the histogram, kept as bits: repeats
-//            collapse and the order of arrival cannot change the result.
-//   rows     a half-warp per row: row length (popcount of its words) and
-//            the running count in front of every word; per 16-row tile, the
-//            sums of the lengths and of the chunk counts
-//   emit     each CTA adds up the tile sums in front of it; one thread per
-//            row: row_ptr and the row's first work item; the work items /
-//            record headers of the CTA's rows dealt over all its threads;
-//            the last CTA writes the totals
+//            KV head) list's 16 threads together write its slot mask.  This
+//            is the histogram, kept as bits: repeats collapse and the order
+//            of arrival cannot change the result.
+//   rows     one CTA per tile of rows (at most kMaxRowTiles tiles), tiles
+//            taken in launch order from a ticket counter, a half-warp per
+//            row: the row's length (popcount of its words) and the running
+//            count in front of every word; the tile publishes its totals
+//            (entries, work items) and adds up all its predecessors'
+//            published totals in parallel (the scan, with no kernel
+//            boundary and no chain of waits); then row_ptr, each row's first
+//            work item, and the tile's work items and record headers.
 //   scatter  one thread per top-k entry: each kept entry goes to
 //            row_ptr + (tokens of the same row before it), found in O(1)
 //            from the word prefix and a popcount; it also fills the token
@@ -31,6 +33,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace msa {
 namespace {
@@ -89,11 +92,11 @@ struct PlanDev {
   int64_t total_rows, rows, max_q, max_k;
   int32_t* req_off;
   uint32_t* bitmap;
-  int32_t* word_pre;
-  int32_t* row_cnt;
-  int32_t* row_wptr;
-  int32_t* tile_sums;
-  int ntiles;
+  int32_t* word_pre;     // [rows * W] tokens of the row before each word
+  int32_t* row_cnt;      // [rows] entries of the row
+  int32_t* row_wptr;     // [rows] first work item of the row
+  uint64_t* tile_state;  // [ntiles] published tile totals (see rows)
+  int ntiles, tile_rows;
   int32_t* row_ptr;
   int32_t* q_idx;
   uint8_t* slot;
@@ -111,9 +114,10 @@ __global__ void __launch_bounds__(kScanThreads) plan_prep_kernel(PlanDev d,
   pdl_trigger();
   {
     uint4* bm = reinterpret_cast<uint4*>(d.bitmap);
-    for (int64_t i = (int64_t)blockIdx.x * kScanThreads + threadIdx.x; i < bitmap_vec;
-         i += (int64_t)gridDim.x * kScanThreads)
-      bm[i] = make_uint4(0u, 0u, 0u, 0u);
+    const int64_t stride = (int64_t)gridDim.x * kScanThreads;
+    const int64_t i0 = (int64_t)blockIdx.x * kScanThreads + threadIdx.x;
+    for (int64_t i = i0; i < bitmap_vec; i += stride) bm[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int64_t i = i0; i < d.ntiles; i += stride) d.tile_state[i] = 0ull;
   }
   if (blockIdx.x != 0) return;
   __shared__ int s_bad;
@@ -151,7 +155,8 @@ __global__ void __launch_bounds__(kScanThreads) plan_prep_kernel(PlanDev d,
     d.counters[0] = 0;
     d.counters[1] = 0;
     d.counters[2] = st ? 0 : 1;
-    d.row_ptr[d.rows] = 0;  // the fill kernel's last CTA writes the total
+    d.counters[3] = 0;      // the rows kernel's tile ticket
+    d.row_ptr[d.rows] = 0;  // the rows kernel's last tile writes the total
   }
 }
 
@@ -219,159 +224,252 @@ __global__ void __launch_bounds__(256) plan_mark_kernel(PlanDev d) {
     d.slot_mask[w] = (uint16_t)((bal >> (lane & ~(kTopK - 1))) & 0xFFFFu);
 }
 
-// kCountTile rows per CTA, a half-warp per row: lane l of the half-warp
-// takes the 16-byte vectors [l * per, (l + 1) * per) of the row (rows are
-// 16-byte aligned, W a multiple of 4), so the row is read and written as
-// one contiguous span.  The running count in front of every word is the
-// lane's own popcounts plus an exclusive scan over the 16 lanes.  The CTA's
-// sums of the row lengths and chunk counts go to tile_sums.
-__global__ void __launch_bounds__(kPlanTile) plan_rows_kernel(PlanDev d) {
+// Tile state word: bit 63 set once published, bits 31..61 the tile's work
+// items, bits 0..30 its CSR entries (both below 2^31, checked on the host).
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Exclusive scan of (c, w) over the 16 rows of a round, in warp 0; the
+// round's totals come back in *tc / *tw.
+__device__ __forceinline__ void scan16(int c, int w, int* exc, int* exw, int* tc,
+                                       int* tw) {
+  const int lane = threadIdx.x & 31;
+  int ic = c, iw = w;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int nc = __shfl_up_sync(0xffffffffu, ic, o);
+    const int nw = __shfl_up_sync(0xffffffffu, iw, o);
+    if (lane >= o) {
+      ic += nc;
+      iw += nw;
+    }
+  }
+  *exc = ic - c;
+  *exw = iw - w;
+  *tc = __shfl_sync(0xffffffffu, ic, 31);
+  *tw = __shfl_sync(0xffffffffu, iw, 31);
+}
+
+// One CTA per tile of d.tile_rows rows (a multiple of 16, chosen on the
+// host so that there are at most kMaxRowTiles tiles), worked in rounds of
+// 16 rows, a half-warp per row.
+//   pass 1  per round: lane l of the half-warp takes the 16-byte vectors
+//           [l * per, (l + 1) * per) of its row (rows are 16-byte aligned,
+//           W a multiple of 4), so the row is read and written as one
+//           contiguous span; the running count in front of every word is
+//           the lane's own popcounts plus an exclusive scan over the 16
+//           lanes; the row length goes to row_cnt, and the tile's totals
+//           (entries, work items) add up.
+//   totals  the tile publishes its totals and adds up those of all the
+//           tiles before it, read in parallel by the whole CTA (at most
+//           kMaxRowTiles - 1 words): the exclusive scan across tiles, with
+//           no kernel boundary and no chain of waits.
+//   pass 2  per round: row_ptr and each row's first work item; the round's
+//           work items and record headers dealt over all threads.
+__global__ void __launch_bounds__(kRowThreads) plan_rows_kernel(PlanDev d) {
   pdl_wait();
   pdl_trigger();
-  static_assert(kPlanTile == 16 * kCountTile, "a half-warp per row");
-  __shared__ int s_c[kCountTile], s_w[kCountTile];
+  static_assert(kRowThreads == 16 * kRowTile, "a half-warp per row");
+  __shared__ int s_tile, s_fail;
+  __shared__ int s_cnt[kRowTile], s_exc[kRowTile], s_exw[kRowTile];
+  __shared__ int s_red[3][kRowThreads / 32];
+  __shared__ int4 s_hdr[kRowTile];   // record header without the count
+  __shared__ int2 s_item[kRowTile];  // work item: request, (KV head, page)
+  if (threadIdx.x == 0) {
+    // tiles in launch order: every predecessor of a tile has started, so
+    // waiting for its totals cannot deadlock
+    s_tile = atomicAdd(&d.counters[3], 1);
+    s_fail = 0;
+  }
+  __syncthreads();
+  const int tile = s_tile;
   const int sub = threadIdx.x & 15, k = threadIdx.x >> 4;
-  const int64_t r = (int64_t)blockIdx.x * kCountTile + k;
-  const bool live = d.counters[2] == 1 && r < d.rows;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool ok = d.counters[2] == 1;
   const int nv = d.W >> 2;
   const int per = (nv + 15) >> 4;
-  const uint4* __restrict__ words = reinterpret_cast<const uint4*>(d.bitmap + r * d.W);
-  int own = 0;
-  if (live) {
-    for (int u0 = 0; u0 < per; u0 += 4) {
-      uint4 v[4];
+  const int64_t tile_r0 = (int64_t)tile * d.tile_rows;
+  const int rounds = d.tile_rows / kRowTile;
+
+  // ---- pass 1: row lengths and word prefixes
+  int tc = 0, tw = 0;  // the tile's totals, kept by lane 0 of each half-warp
+  for (int rd = 0; rd < rounds; ++rd) {
+    const int64_t r = tile_r0 + rd * kRowTile + k;
+    const bool live = ok && r < d.rows;
+    const uint4* __restrict__ words = reinterpret_cast<const uint4*>(d.bitmap + r * d.W);
+    int own = 0;
+    if (live) {
+      for (int u0 = 0; u0 < per; u0 += 4) {
+        uint4 v[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int x = sub * per + u0 + u;
-        v[u] = (u0 + u < per && x < nv) ? words[x] : make_uint4(0u, 0u, 0u, 0u);
-      }
+        for (int u = 0; u < 4; ++u) {
+          const int x = sub * per + u0 + u;
+          v[u] = (u0 + u < per && x < nv) ? words[x] : make_uint4(0u, 0u, 0u, 0u);
+        }
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        own += __popc(v[u].x) + __popc(v[u].y) + __popc(v[u].z) + __popc(v[u].w);
-    }
-  }
-  // inclusive scan over the half-warp (all 32 lanes take part)
-  int incl = own;
-#pragma unroll
-  for (int o = 1; o < 16; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, incl, o, 16);
-    if (sub >= o) incl += n;
-  }
-  const int total = __shfl_sync(0xffffffffu, incl, 15, 16);
-  if (live) {
-    int4* __restrict__ pre = reinterpret_cast<int4*>(d.word_pre + r * d.W);
-    int run = incl - own;
-    for (int u = 0; u < per; ++u) {
-      const int x = sub * per + u;
-      if (x < nv) {
-        const uint4 v = words[x];
-        int4 o;
-        o.x = run; run += __popc(v.x);
-        o.y = run; run += __popc(v.y);
-        o.z = run; run += __popc(v.z);
-        o.w = run; run += __popc(v.w);
-        pre[x] = o;
+        for (int u = 0; u < 4; ++u)
+          own += __popc(v[u].x) + __popc(v[u].y) + __popc(v[u].z) + __popc(v[u].w);
       }
     }
-    if (sub == 0) d.row_cnt[r] = total;
+    int incl = own;
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o, 16);
+      if (sub >= o) incl += n;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 15, 16);
+    if (live) {
+      int4* __restrict__ pre = reinterpret_cast<int4*>(d.word_pre + r * d.W);
+      int run = incl - own;
+      for (int u = 0; u < per; ++u) {
+        const int x = sub * per + u;
+        if (x < nv) {
+          const uint4 v = words[x];
+          int4 o;
+          o.x = run; run += __popc(v.x);
+          o.y = run; run += __popc(v.y);
+          o.z = run; run += __popc(v.z);
+          o.w = run; run += __popc(v.w);
+          pre[x] = o;
+        }
+      }
+      if (sub == 0) d.row_cnt[r] = total;
+    }
+    if (sub == 0 && live) {
+      tc += total;
+      tw += (total + d.C - 1) / d.C;
+    }
   }
-  if (sub == 0) {
-    s_c[k] = live ? total : 0;
-    s_w[k] = live ? (total + d.C - 1) / d.C : 0;
+
+  // ---- the tile's totals; publish them; add up the predecessors'
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    tc += __shfl_xor_sync(0xffffffffu, tc, o);
+    tw += __shfl_xor_sync(0xffffffffu, tw, o);
+  }
+  if (lane == 0) {
+    s_red[0][warp] = tc;
+    s_red[1][warp] = tw;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    int tc = 0, tw = 0;
+    int c = 0, w = 0;
 #pragma unroll
-    for (int i = 0; i < kCountTile; ++i) {
-      tc += s_c[i];
-      tw += s_w[i];
+    for (int i = 0; i < kRowThreads / 32; ++i) {
+      c += s_red[0][i];
+      w += s_red[1][i];
     }
-    d.tile_sums[blockIdx.x] = tc;
-    d.tile_sums[d.ntiles + blockIdx.x] = tw;
+    s_red[2][0] = c;
+    s_red[2][1] = w;
+    // row_cnt and word_pre of this tile are written before its totals are
+    // visible to anyone; the totals themselves need no further ordering
+    st_relaxed_u64(&d.tile_state[tile],
+                   (1ull << 63) | ((uint64_t)(uint32_t)w << 31) | (uint32_t)c);
   }
-}
-
-// kPlanTile rows per CTA.  One thread per row finds the row's offsets (the
-// sums of the count tiles in front of the CTA plus a block scan)
-// and its page; then the CTA's chunks are dealt to all its threads, each
-// finding its row by a search over the rows' first chunks, so a row with
-// many chunks does not serialise on one thread.
-__global__ void __launch_bounds__(kPlanTile) plan_emit_kernel(PlanDev d) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ int s_wex[kPlanTile];     // first chunk of the row, within the CTA
-  __shared__ int s_start[kPlanTile];   // first CSR entry of the row
-  __shared__ int s_cnt[kPlanTile];
-  __shared__ int4 s_hdr[kPlanTile];    // record header without the count
-  __shared__ int2 s_item[kPlanTile];   // work item: request, (KV head, page)
-  const int64_t r = (int64_t)blockIdx.x * kPlanTile + threadIdx.x;
-  const bool ok = d.counters[2] == 1;
-  const int c = (ok && r < d.rows) ? d.row_cnt[r] : 0;
-  const int chunks = (c + d.C - 1) / d.C;
-  int tc, tw;
-  const int ex_c = block_excl_scan<kPlanTile>(c, &tc);
-  const int ex_w = block_excl_scan<kPlanTile>(chunks, &tw);
-  // the rows in front of this CTA: the sums of the count tiles before it,
-  // added up by the whole CTA (no separate scan kernel)
-  const int tile0 = blockIdx.x * (kPlanTile / kCountTile);
-  __shared__ int s_red[2][kPlanTile / 32];
   int pc = 0, pw = 0;
-  for (int i = threadIdx.x; i < tile0; i += kPlanTile) {
-    pc += d.tile_sums[i];
-    pw += d.tile_sums[d.ntiles + i];
+  bool fail = false;
+  for (int i = threadIdx.x; i < tile; i += kRowThreads) {
+    uint64_t v = ld_relaxed_u64(&d.tile_state[i]);
+    if (!(v >> 63)) {
+      // bounded wait for a started predecessor to publish (about a second
+      // of wall time at most), polling with a back-off: thousands of
+      // threads polling L2 flat out would slow the very tiles they wait for
+      const uint64_t t0 = global_timer_ns();
+      while (!((v = ld_relaxed_u64(&d.tile_state[i])) >> 63)) {
+        __nanosleep(200);
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          fail = true;
+          break;
+        }
+      }
+    }
+    pc += (int)(v & 0x7fffffffu);
+    pw += (int)((v >> 31) & 0x7fffffffu);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     pc += __shfl_xor_sync(0xffffffffu, pc, o);
     pw += __shfl_xor_sync(0xffffffffu, pw, o);
   }
-  if ((threadIdx.x & 31) == 0) {
-    s_red[0][threadIdx.x >> 5] = pc;
-    s_red[1][threadIdx.x >> 5] = pw;
+  __syncthreads();  // s_red[0..1] is reused below
+  if (lane == 0) {
+    s_red[0][warp] = pc;
+    s_red[1][warp] = pw;
   }
+  if (fail) s_fail = 1;
   __syncthreads();
+  if (s_fail) {
+    // a predecessor never published: the plan is incomplete; the attention
+    // kernel sees the status bit and does no work
+    if (threadIdx.x == 0) atomicOr(d.status, (unsigned)MSA_STATUS_TIMEOUT);
+    return;
+  }
   int base_c = 0, base_w = 0;
 #pragma unroll
-  for (int w = 0; w < kPlanTile / 32; ++w) {
-    base_c += s_red[0][w];
-    base_w += s_red[1][w];
+  for (int i = 0; i < kRowThreads / 32; ++i) {
+    base_c += s_red[0][i];
+    base_w += s_red[1][i];
   }
-  if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) {
-    // the last CTA closes the CSR and publishes the totals
-    d.counters[0] = base_c + tc;
-    d.counters[1] = base_w + tw;
-    d.row_ptr[d.rows] = base_c + tc;
+  if (tile == (int)gridDim.x - 1 && threadIdx.x == 0) {
+    // the last tile closes the CSR and publishes the totals
+    const int all_c = base_c + s_red[2][0], all_w = base_w + s_red[2][1];
+    d.counters[0] = all_c;
+    d.counters[1] = all_w;
+    d.row_ptr[d.rows] = all_c;
   }
-  s_wex[threadIdx.x] = ex_w;
-  s_start[threadIdx.x] = base_c + ex_c;
-  s_cnt[threadIdx.x] = c;
-  if (r < d.rows) {
-    d.row_ptr[r] = base_c + ex_c;
-    d.row_wptr[r] = base_w + ex_w;
-    if (c > 0) {
-      const int h = (int)(r / d.total_rows);
-      const int64_t rr = r - (int64_t)h * d.total_rows;
-      const int b = upper_index(d.req_off, d.B, rr);
-      const int p = (int)(rr - d.req_off[b]);
-      const int32_t phys = d.block_table[(int64_t)b * d.bt_stride + p];
-      // record header: KV tile row of the pool, (token count), first key
-      // position of the page, first query head of the KV head
-      s_hdr[threadIdx.x] = make_int4((phys * d.Hkv + h) * kPage, 0, p * kPage, h * d.G);
-      s_item[threadIdx.x] = make_int2(b, (h << 24) | p);
+
+  // ---- pass 2: row_ptr, first work items, the work items of each round
+  for (int rd = 0; rd < rounds; ++rd) {
+    const int64_t r0 = tile_r0 + rd * kRowTile;
+    if (warp == 0) {
+      const int64_t r = r0 + lane;
+      const int c = (lane < kRowTile && ok && r < d.rows) ? d.row_cnt[r] : 0;
+      const int ch = (c + d.C - 1) / d.C;
+      int exc, exw, rc, rw;
+      scan16(c, ch, &exc, &exw, &rc, &rw);
+      if (lane < kRowTile) {
+        s_cnt[lane] = c;
+        s_exc[lane] = exc;
+        s_exw[lane] = exw;
+        if (r < d.rows) {
+          d.row_ptr[r] = base_c + exc;
+          d.row_wptr[r] = base_w + exw;
+          if (c > 0) {
+            const int h = (int)(r / d.total_rows);
+            const int64_t rq = r - (int64_t)h * d.total_rows;
+            const int b = upper_index(d.req_off, d.B, rq);
+            const int p = (int)(rq - d.req_off[b]);
+            const int32_t phys = d.block_table[(int64_t)b * d.bt_stride + p];
+            // record header: KV tile row of the pool, (token count), first
+            // key position of the page, first query head of the KV head
+            s_hdr[lane] = make_int4((phys * d.Hkv + h) * kPage, 0, p * kPage, h * d.G);
+            s_item[lane] = make_int2(b, (h << 24) | p);
+          }
+        }
+      }
     }
-  }
-  __syncthreads();
-  for (int k = threadIdx.x; k < tw; k += kPlanTile) {
-    const int j = upper_index(s_wex, kPlanTile, k);  // last row starting at or before k
-    const int ch = k - s_wex[j];
-    const int n = min(d.C, s_cnt[j] - ch * d.C);
-    const int64_t wi = (int64_t)base_w + k;
-    reinterpret_cast<int4*>(d.work)[wi] =
-        make_int4(s_start[j] + ch * d.C, n, s_item[j].x, s_item[j].y);
-    int4 hdr = s_hdr[j];
-    hdr.y = n;
-    d.records[wi * d.rec_stride] = hdr;
+    __syncthreads();
+    const int rw = s_exw[kRowTile - 1] + (s_cnt[kRowTile - 1] + d.C - 1) / d.C;
+    for (int q = threadIdx.x; q < rw; q += kRowThreads) {
+      const int j = upper_index(s_exw, kRowTile, q);  // last row starting at or before q
+      const int ch = q - s_exw[j];
+      const int n = min(d.C, s_cnt[j] - ch * d.C);
+      const int64_t wi = (int64_t)base_w + q;
+      reinterpret_cast<int4*>(d.work)[wi] =
+          make_int4(base_c + s_exc[j] + ch * d.C, n, s_item[j].x, s_item[j].y);
+      int4 hdr = s_hdr[j];
+      hdr.y = n;
+      d.records[wi * d.rec_stride] = hdr;
+    }
+    base_c += s_exc[kRowTile - 1] + s_cnt[kRowTile - 1];
+    base_w += rw;
+    __syncthreads();  // the round's shared arrays are rewritten next round
   }
 }
 
@@ -426,8 +524,9 @@ cudaError_t launch_plan(const msa_plan_t& pl, const int32_t* topk,
   d.word_pre = pl.word_pre;
   d.row_cnt = pl.row_cnt;
   d.row_wptr = pl.row_wptr;
-  d.tile_sums = pl.tile_sums;
-  d.ntiles = (int)ceil_div(pl.rows, kCountTile);
+  d.tile_state = pl.tile_state;
+  d.tile_rows = (int)plan_tile_rows(pl.rows);
+  d.ntiles = (int)ceil_div(pl.rows, d.tile_rows);
   d.row_ptr = pl.row_ptr;
   d.q_idx = pl.q_idx;
   d.slot = pl.slot;
@@ -450,10 +549,7 @@ cudaError_t launch_plan(const msa_plan_t& pl, const int32_t* topk,
   if (e == cudaSuccess && marks > 0)
     e = launch_pdl(plan_mark_kernel, mgrid, 256, 0, stream, d);
   if (e == cudaSuccess && d.ntiles > 0)
-    e = launch_pdl(plan_rows_kernel, (unsigned)d.ntiles, kPlanTile, 0, stream, d);
-  const unsigned egrid = (unsigned)ceil_div(pl.rows, kPlanTile);
-  if (e == cudaSuccess && egrid > 0)
-    e = launch_pdl(plan_emit_kernel, egrid, kPlanTile, 0, stream, d);
+    e = launch_pdl(plan_rows_kernel, (unsigned)d.ntiles, kRowThreads, 0, stream, d);
   if (e == cudaSuccess && marks > 0)
     e = launch_pdl(plan_scatter_kernel, mgrid, 256, 0, stream, d);
   return e;

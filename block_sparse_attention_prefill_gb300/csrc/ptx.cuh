@@ -74,16 +74,18 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // `limit_ns` of wall time, or as soon as *abort becomes non-zero; returns
 // false in both cases so the caller can leave its loop cleanly.  A null
 // `abort` waits for the full time limit (used to drain in-flight copies).
+// Elapsed time is taken from the low 32 bits of the nanosecond timer
+// (modular difference), so limits up to about 4 s stay exact.
 __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity,
                                              const volatile int* abort,
-                                             uint64_t limit_ns) {
+                                             uint32_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const uint32_t t0 = (uint32_t)global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (abort != nullptr && *abort) return false;
-      if (global_timer_ns() - t0 > limit_ns) return false;
+      if ((uint32_t)global_timer_ns() - t0 > limit_ns) return false;
     }
   }
 }
@@ -112,6 +114,36 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc,
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
       "[%0], [%1], %2, [%3];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------- L2 policy
+
+// 64-bit L2 cache policies for the .L2::cache_hint forms below: data read
+// once (evict first) and data written now to be read again soon (evict
+// last).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0;" : "=l"(p));
+  return p;
+}
+
+// tma_load_2d with an L2 cache policy.
+__device__ __forceinline__ void tma_load_2d_hint(void* smem_dst,
+                                                 const CUtensorMap* map,
+                                                 uint64_t* bar, int32_t x,
+                                                 int32_t y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::"
+      "complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y),
+      "l"(policy)
       : "memory");
 }
 
@@ -259,6 +291,48 @@ __device__ __forceinline__ void st_global_v8(void* p, uint32_t a0, uint32_t a1,
       "st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p),
       "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
       : "memory");
+}
+
+// st_global_v8 with an L2 cache policy.
+__device__ __forceinline__ void st_global_v8_hint(void* p, uint32_t a0, uint32_t a1,
+                                                  uint32_t a2, uint32_t a3,
+                                                  uint32_t a4, uint32_t a5,
+                                                  uint32_t a6, uint32_t a7,
+                                                  uint64_t policy) {
+  asm volatile(
+      "st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(p),
+      "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7),
+      "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void st_global_f32_hint(float* p, float v,
+                                                   uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v),
+               "l"(policy)
+               : "memory");
+}
+
+// 16-, 8- and 4-byte global loads with an L2 cache policy.
+__device__ __forceinline__ uint4 ld_global_v4_hint(const void* p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.L2::cache_hint.v4.b32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_global_v2_hint(const void* p, uint64_t policy) {
+  uint2 v;
+  asm volatile("ld.global.L2::cache_hint.v2.b32 {%0, %1}, [%2], %3;"
+               : "=r"(v.x), "=r"(v.y)
+               : "l"(p), "l"(policy));
+  return v;
+}
+__device__ __forceinline__ float ld_global_f32_hint(const float* p, uint64_t policy) {
+  float v;
+  asm volatile("ld.global.L2::cache_hint.f32 %0, [%1], %2;"
+               : "=f"(v)
+               : "l"(p), "l"(policy));
+  return v;
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -70,6 +70,7 @@ extern "C" {
 #define MSA_ERR_CUDA 5        /* a CUDA runtime / driver call failed          */
 #define MSA_ERR_NULL 6        /* a required pointer is NULL                   */
 #define MSA_ERR_TOO_LARGE 7   /* beyond msa_decode_noalloc's fixed scratch    */
+#define MSA_ERR_BUSY 8        /* msa_decode_noalloc entered from two threads  */
 
 /* device status bits (msa_read_status) */
 #define MSA_STATUS_BAD_PAGE_ID (1u << 0)  /* top-k id >= page count, or < -1 */
@@ -138,9 +139,9 @@ typedef struct msa_plan {
   int32_t *req_off;            /* [B+1]                                     */
   uint32_t *bitmap;            /* [rows * bitmap_words] token membership    */
   int32_t *word_pre;           /* [rows * bitmap_words] tokens before word  */
-  int32_t *row_cnt;            /* [rows]                                    */
+  int32_t *row_cnt;            /* [rows] entries of the row                 */
   int32_t *row_wptr;           /* [rows] first work item of the row         */
-  int32_t *tile_sums;          /* [2 * tiles] row / chunk sums per tile     */
+  uint64_t *tile_state;        /* [<= 512] published totals of row tiles    */
   int32_t *row_ptr;            /* [rows + 1]                                */
   int32_t *q_idx;              /* [max_nnz] global query token ids          */
   uint8_t *slot;               /* [max_nnz] top-k position j                */
@@ -192,7 +193,7 @@ MSA_API int msa_plan_workspace_bytes(int64_t B, int64_t T, int64_t Hq, int64_t H
  *   workspace     device buffer of msa_plan_workspace_bytes() bytes,
  *                 256-byte aligned; it holds the plan until it is rebuilt.
  *   plan          host struct, filled on return.
- * Launches 6 kernels and 2 memsets on `stream`; never synchronises.
+ * Launches 4 kernels on `stream`; never synchronises.
  */
 MSA_API int msa_plan(const int32_t *topk, const int32_t *cu_seqlens_q,
              const int32_t *cu_seqlens_k, const int32_t *block_table,
@@ -378,13 +379,20 @@ MSA_API int msa_decode_nvfp4(const uint8_t *q, const uint8_t *kv4,
  * allocates and frees nothing.
  *   - A batch whose msa_decode_workspace_bytes() exceeds that size is
  *     rejected with MSA_ERR_TOO_LARGE before anything is launched.
- *   - The first call on a device looks up the array's device address (a
- *     runtime call, made once per device with that device current); make
- *     that first call before any stream capture.
+ *   - Every call outside stream capture looks up the array's device address
+ *     in the current device's context (a runtime call; the first one on a
+ *     device also loads the module).  A call made while `stream` is being
+ *     captured reuses the address of that device's last call outside
+ *     capture, so make one call on each device before capturing; without
+ *     one the captured call returns MSA_ERR_CUDA.
  *   - All calls share the one array and each overwrites it (the parts that
  *     must start at zero are cleared by every call).  Calls whose work
  *     overlaps on the GPU -- on different streams, or from several host
- *     threads -- race and must not be issued.
+ *     threads -- race and must not be issued.  A call entered while another
+ *     host thread is inside this function returns MSA_ERR_BUSY without
+ *     launching anything; the GPU-side overlap of calls enqueued one after
+ *     another on different streams cannot be seen here and stays the
+ *     caller's to avoid.
  *   - Device status bits are not returned (there is no plan_out).
  */
 #define MSA_NOALLOC_SCRATCH_BYTES (16u << 20)
@@ -396,6 +404,19 @@ MSA_API int msa_decode_noalloc(const uint8_t *q, const uint8_t *kv,
                                const int32_t *seq_lens, int64_t B, int64_t n,
                                int64_t Hq, int64_t Hkv, int64_t max_seqlen_k,
                                uint16_t *out, float *lse, void *stream);
+
+/*
+ * For tests of the expiry path only: sets the wall-time limit, in
+ * nanoseconds, of the attention kernel's pipeline waits for every later
+ * launch in this process; 0 restores the default of about one second.  With
+ * a limit shorter than a page load, a wait runs out: the kernel sets
+ * MSA_STATUS_TIMEOUT, stops issuing work, lets the copies and MMAs it has
+ * already started land (those drain waits keep the full limit), frees its
+ * tensor memory and returns; the outputs of that call are not meaningful,
+ * and the next call on the same workspaces computes normally.  (The pages
+ * have no counterpart; this is a library test hook.)
+ */
+MSA_API int msa_test_set_wait_limit_ns(uint64_t ns);
 
 /*
  * Copies the plan's device status word to *status.  This call synchronises

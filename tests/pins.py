@@ -108,6 +108,27 @@ def tiny_sparse_workload(seed=3, corrupt=True):
     return w
 
 
+def flat_large_v_workload(seed=0):
+    """Outputs of large magnitude with exact probabilities: every K row is
+    the same (so each row's scores are all equal, the softmax is flat and
+    the probabilities 2^8 are exact in E4M3), and V codes have magnitudes
+    around 300 with a fixed sign per column, so every page's partial and the
+    output sit near +-19 in real units.  The only rounding left is that of
+    the split partials and of the bf16 output."""
+    import dataclasses
+    w = workloads.make_batch("flat_big_v", [64, 40], [4096, 1700], 16, 2,
+                             seed=seed)
+    kv = w.kv.clone()
+    kv[..., :D] = 0x30                      # E4M3 0.5 everywhere
+    rng = np.random.default_rng(seed + 100)
+    mag = np.clip(300.0 + 60.0 * rng.standard_normal(tuple(kv.shape[:-1]) + (D,)),
+                  200.0, 440.0)
+    sign = np.where(rng.random(D) < 0.5, -1.0, 1.0)
+    v = torch.as_tensor((mag * sign).astype(np.float32)).to(torch.float8_e4m3fn)
+    kv[..., D:] = v.view(torch.uint8)
+    return dataclasses.replace(w, kv=kv, v_scale=1.0 / 16.0)
+
+
 def _close(a, b, tol):
     a = np.asarray(a, np.float64)
     b = np.asarray(b, np.float64)

@@ -126,3 +126,36 @@ def test_binding_rejects_host_tensors_and_wrong_pools():
     assert "CUDA" in _err(msa.msa_nvfp4_to_e4m3, kv4)
     assert "dtype" in _err(msa._need, kv4.to(torch.int16), "kv4", (torch.uint8,),
                            False)
+
+
+def test_decode_bindings_check_shapes_before_the_library():
+    # the library sees only pointers: a pool for the wrong number of KV heads
+    # or an undersized output would be read or written out of bounds on the
+    # device, so the bindings refuse them first (host tensors suffice here:
+    # the shape checks come before the device checks)
+    import torch
+    B, n, Hq, Hkv = 3, 4, 16, 2
+    q = torch.zeros((B * n, Hq, 128), dtype=torch.uint8)
+    topk = torch.zeros((B * n, Hkv, 16), dtype=torch.int32)
+    bt = torch.zeros((B, 8), dtype=torch.int32)
+    seq = torch.full((B,), 900, dtype=torch.int32)
+    kv_bad = torch.zeros((8, Hkv + 1, 128, 256), dtype=torch.uint8)
+    out = torch.zeros((B * n, Hq, 128), dtype=torch.bfloat16)
+    out_small = torch.zeros((B * n - 1, Hq, 128), dtype=torch.bfloat16)
+    lse_bad = torch.zeros((B * n, Hq + 1), dtype=torch.float32)
+    kv = torch.zeros((8, Hkv, 128, 256), dtype=torch.uint8)
+    args = (1.0, 1.0, 1.0, 0.1)
+    assert "kv must be" in _err(msa.msa_decode_noalloc, q, kv_bad, *args, topk,
+                                bt, seq, n, 1000, out, None)
+    assert "out must be" in _err(msa.msa_decode_noalloc, q, kv, *args, topk,
+                                 bt, seq, n, 1000, out_small, None)
+    assert "lse must be" in _err(msa.msa_decode_noalloc, q, kv, *args, topk,
+                                 bt, seq, n, 1000, out, lse_bad)
+    assert "B*n rows" in _err(msa.msa_decode_noalloc, q[:-1], kv, *args, topk,
+                              bt, seq, n, 1000, out, None)
+    assert "out is required" in _err(msa.msa_decode_noalloc, q, kv, *args,
+                                     topk, bt, seq, n, 1000, None, None)
+    assert "kv must be" in _err(msa.msa_decode, q, kv_bad, *args, topk, bt,
+                                seq, n, 1000)
+    assert "out must be" in _err(msa.msa_decode, q, kv, *args, topk, bt, seq,
+                                 n, 1000, None, out_small)

@@ -89,10 +89,12 @@ def test_fused_equals_staged(name):
     assert torch.equal(out4, out8) and torch.equal(lse4, lse8)
 
 
-def test_full_size_sampled_1m():
-    w = workloads.make_config("long_prefill_1m_nvfp4", seed=0)
-    toks = sample_tokens(w.T, 48, seed=2)
-    s, e, st = check_against_oracle(w, tokens=toks, what="1M nvfp4")
+@pytest.mark.parametrize("name", ["long_prefill_1m_nvfp4",
+                                  "long_prefill_150k_nvfp4"])
+def test_full_size_all_tokens(name):
+    # the bench's NVFP4 workloads at full size, every token against the oracle
+    w = workloads.make_config(name, seed=0)
+    s, e, st = check_against_oracle(w, what=name)
     assert st == 0
 
 

@@ -28,6 +28,13 @@ def gpu_plan(w, total_rows=None):
 def compare_plan(w, total_rows=None):
     plan, nnz, nwork = gpu_plan(w, total_rows)
     R = w.total_rows if total_rows is None else total_rows
+    check_plan(plan, nnz, nwork, w, R)
+    return plan
+
+
+def check_plan(plan, nnz, nwork, w, R):
+    """The GPU plan against the oracle's CSR (plain loops) and its work-list
+    rule, bit for bit, plus the attention kernel's records."""
     row_ptr, q_idx, slot, mask = oracle.k2q_csr(w, total_rows=R)
     assert nnz == len(q_idx)
     assert np.array_equal(plan.row_ptr().cpu().numpy(), row_ptr)
@@ -56,7 +63,6 @@ def compare_plan(w, total_rows=None):
             t = int(q_idx[start + k])
             pos = w.seq_lens[b] - w.q_lens[b] + (t - int(cu_q[b]))
             assert list(recs[wi, 1 + k, :3]) == [t, pos, int(slot[start + k])]
-    return plan
 
 
 @pytest.mark.parametrize("name", ["tiny_full_prefill", "chunked_prefill_32k",
@@ -126,3 +132,32 @@ def test_plan_is_deterministic():
     for _ in range(3):
         p2, n2, _ = gpu_plan(w)
         assert n2 == n1 and torch.equal(p2.q_idx()[:n2], a)
+
+
+@pytest.mark.parametrize("name", ["long_prefill_1m", "long_prefill_150k"])
+def test_plan_full_size(name):
+    # the bench's workloads: 16,384 rows with ~4 tokens each (1M), and
+    # 2,400 rows of up to hundreds of tokens (150K)
+    w = workloads.make_config(name, seed=0)
+    plan = compare_plan(w)
+    assert plan.status() == 0
+
+
+def test_decode_plan_over_65535_rows():
+    # msa_decode's plan for 64 requests x 8 tokens over contexts up to 131,072
+    # tokens: 2 x 64 x 1024 = 131,072 rows, more than a grid's y or z extent
+    # could hold (vLLM PR 64631, Details: page counts go on grid x); checked
+    # bit for bit like every other plan
+    w = workloads.make_config("decode_64x8", seed=0, kv_device="cuda")
+    wd = w.to("cuda")
+    n = w.q_lens[0]
+    seq = torch.tensor(w.seq_lens, dtype=torch.int32, device="cuda")
+    out, lse, plan = msa.msa_decode(wd.q, wd.kv, w.q_scale, w.k_scale,
+                                    w.v_scale, w.softmax_scale, wd.topk,
+                                    wd.block_table, seq, n, w.max_seqlen_k)
+    torch.cuda.synchronize()
+    R = int(plan.struct.total_rows)
+    assert w.Hkv * R > 65535
+    nnz, nwork = plan.counters()
+    check_plan(plan, nnz, nwork, w, R)
+    assert plan.status() == 0

@@ -23,7 +23,7 @@ def test_tiny_full_prefill_equals_dense(seed):
     assert st == 0
 
 
-@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("seed", range(16))
 def test_chunked_prefill_32k(seed):
     w = workloads.make_config("chunked_prefill_32k", seed=seed)
     check_against_oracle(w, what="chunked seed %d" % seed)
@@ -97,11 +97,10 @@ def test_long_rows_from_empty_cache():
 
 
 @pytest.mark.parametrize("name", ["long_prefill_150k", "long_prefill_1m"])
-def test_full_size_sampled(name):
-    # the bench's workloads at full size, oracle on a sample of tokens
+def test_full_size_all_tokens(name):
+    # the bench's workloads at full size, every token against the oracle
     w = workloads.make_config(name, seed=0)
-    toks = sample_tokens(w.T, 48, seed=2)
-    s, e, st = check_against_oracle(w, tokens=toks, what=name)
+    s, e, st = check_against_oracle(w, what=name)
     assert st == 0
 
 
@@ -124,4 +123,14 @@ def test_mixed_decode_and_prefill_batch(seed):
                              [40000, 65536, 9000, 131072, 5000, 1024],
                              16, 2, seed=40 + seed)
     s, e, st = check_against_oracle(w, what="mixed seed %d" % seed)
+    assert st == 0
+
+
+def test_large_outputs_keep_the_acceptance_rule():
+    # outputs near +-19 with exact probabilities (pins.flat_large_v_workload):
+    # partials rounded to E4M3 alone would break the rule of vLLM PR 60684
+    # (Validation) on a sixth of the elements; the kernel keeps such halves
+    # in bf16, so the rule holds here as on the pages' own inputs
+    w = pins.flat_large_v_workload(0)
+    s, e, st = check_against_oracle(w, what="large |out|")
     assert st == 0
