@@ -55,6 +55,7 @@
 // by different warps at the same time.
 #include <cuda.h>
 #include <atomic>
+#include <cmath>
 #include <cstring>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -169,7 +170,8 @@ struct Params {
   uint8_t* part_big;    // bf16 overflow rows, 256 bytes each
   float* part_vscale;   // the combine's copy of v_scale
   float* part_lse;
-  float e4m3_limit;     // largest |O| (code units) a half keeps in E4M3
+  uint32_t e4m3_over4;  // (0x7F - largest E4M3 magnitude code a half keeps)
+                        // in each byte
   uint32_t* status;
   int Hq, G;
   int q_tma;       // 1: Q rows by TMA (G % 8 == 0), 0: by cp.async
@@ -181,6 +183,15 @@ struct Params {
   // MMAs in flight before a CTA exits always keep kWaitLimitNs)
   uint32_t wait_ns;
 };
+
+// bounded_wait taken by a whole warp: every lane waits, and the warp goes on
+// only if every lane saw the phase complete, so that on a timeout the lanes
+// of a warp never part ways before a warp-wide step (a shuffle, a vote, a
+// tcgen05.ld or a __syncwarp)
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
+                                          const volatile int* abort, uint32_t limit_ns) {
+  return __all_sync(0xffffffffu, bounded_wait(bar, parity, abort, limit_ns));
+}
 
 __device__ __forceinline__ void set_timeout(Barriers* bars, uint32_t* status) {
   bars->abort = 1;
@@ -208,7 +219,7 @@ __device__ __forceinline__ int div_G(int lrow, float inv_G) {
 // stored as two 16-byte chunks of the 128-byte-swizzled P row; adds the
 // (unrounded) probabilities to four independent partial sums (column
 // e % 4 to l[e % 4]), so the additions form four short chains instead of
-// one long one.  kMask: columns past kv_lim are 0.
+// one long one.  Masked columns hold -inf and give 0.
 // Two floats rounded to bf16 (nearest even) in one word, the first in the
 // low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -224,10 +235,8 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return lo | (hi << 16);
 }
 
-template <bool kMask>
-__device__ __forceinline__ void exp_pack32(const uint32_t (&r)[32], int col0,
-                                           int kv_lim, float c, float off,
-                                           uint8_t* prow, int row, float (&l)[4]) {
+__device__ __forceinline__ void exp_pack32(const uint32_t (&r)[32], int col0, float c,
+                                           float off, uint8_t* prow, int row, float (&l)[4]) {
   uint32_t packed[8];
 #pragma unroll
   for (int e = 0; e < 32; e += 4) {
@@ -236,7 +245,6 @@ __device__ __forceinline__ void exp_pack32(const uint32_t (&r)[32], int col0,
     for (int u = 0; u < 4; ++u) {
       const float x = __uint_as_float(r[e + u]);
       pv[u] = ex2_approx(fmaf(x, c, off));
-      if (kMask && col0 + e + u > kv_lim) pv[u] = 0.f;
       l[u] += pv[u];
     }
     const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(pv[0], pv[1]),
@@ -254,14 +262,19 @@ __device__ __forceinline__ void exp_pack32(const uint32_t (&r)[32], int col0,
 
 // Row maximum over 32 score columns into four independent partial maxima
 // (column e % 4 to m[e % 4]): four short dependency chains.
-template <bool kMask>
-__device__ __forceinline__ void max32(const uint32_t (&r)[32], int col0,
-                                      int kv_lim, float (&m)[4]) {
+__device__ __forceinline__ void max32(const uint32_t (&r)[32], float (&m)[4]) {
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    const float x = __uint_as_float(r[e]);
-    if (!kMask || col0 + e <= kv_lim) m[e & 3] = fmaxf(m[e & 3], x);
-  }
+  for (int e = 0; e < 32; ++e) m[e & 3] = fmaxf(m[e & 3], __uint_as_float(r[e]));
+}
+
+// The causal mask of an item on the token's own page: the score columns past
+// kv_lim become -inf, so that the one unmasked code path serves every item
+// (a second, masked copy of the max and exponential loops would not fit the
+// instruction cache beside the other warp roles' loops).
+__device__ __forceinline__ void mask32(uint32_t (&r)[32], int col0, int kv_lim) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    if (col0 + e > kv_lim) r[e] = 0xFF800000u;
 }
 
 // One 128-token slot (K or V) of an NVFP4 page-head, dequantised into a
@@ -626,9 +639,9 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       cp_async_commit();
     };
     auto wait_rec_q = [&](int li) {
-      return bounded_wait(&bars->rec_full[li % L::rec], (li / L::rec) & 1, abort,
+      return warp_wait(&bars->rec_full[li % L::rec], (li / L::rec) & 1, abort,
                           p.wait_ns) &&
-             (li < L::q || bounded_wait(&bars->q_empty[li % L::q],
+             (li < L::q || warp_wait(&bars->q_empty[li % L::q],
                                         ((li / L::q) - 1) & 1, abort, p.wait_ns));
     };
     if constexpr (kFp4) {
@@ -648,8 +661,8 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->q_full[li % L::q]);
         }
-        if (!bounded_wait(&bars->vraw_full[r], (li / L::vraw) & 1, abort, p.wait_ns) ||
-            (li >= L::v && !bounded_wait(&bars->v_empty[vs], ((li / L::v) - 1) & 1,
+        if (!warp_wait(&bars->vraw_full[r], (li / L::vraw) & 1, abort, p.wait_ns) ||
+            (li >= L::v && !warp_wait(&bars->v_empty[vs], ((li / L::v) - 1) & 1,
                                           abort, p.wait_ns))) {
           ok = false;
           break;
@@ -697,8 +710,8 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     auto convert_k = [&](int j) {
       constexpr int R = kFp4 ? L::kraw : 1;  // (E4M3: never called)
       const int ks = j % L::k, r = j % R;
-      if (!bounded_wait(&bars->kraw_full[r], (j / R) & 1, abort, p.wait_ns) ||
-          (j >= L::k && !bounded_wait(&bars->k_empty[ks], ((j / L::k) - 1) & 1,
+      if (!warp_wait(&bars->kraw_full[r], (j / R) & 1, abort, p.wait_ns) ||
+          (j >= L::k && !warp_wait(&bars->k_empty[ks], ((j / L::k) - 1) & 1,
                                        abort, p.wait_ns))) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         return false;
@@ -719,7 +732,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       const int li = 2 * k + w;
       if (li >= cnt) break;
       const int rs = li % L::rec;
-      if (!bounded_wait(&bars->rec_full[rs], (li / L::rec) & 1, abort,
+      if (!warp_wait(&bars->rec_full[rs], (li / L::rec) & 1, abort,
                         p.wait_ns)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
@@ -739,7 +752,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         kv_lim = min(tok.y - hdr.z, 127);
       }
       const bool need_mask = __any_sync(0xffffffffu, valid && kv_lim < 127);
-      if (!bounded_wait(&bars->s_full[w], k & 1, abort, p.wait_ns)) {
+      if (!warp_wait(&bars->s_full[w], k & 1, abort, p.wait_ns)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
@@ -761,18 +774,17 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       uint8_t* prow_s = smem + L::off_q + (li % L::q) * kTile + row * 128;
       float m2 = -INFINITY, l = 0.f;
       if (warp_valid) {
-        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (need_mask) {
-          max32<true>(r0, 0, kv_lim, mq);
-          max32<true>(r1, 32, kv_lim, mq);
-          max32<true>(r2, 64, kv_lim, mq);
-          max32<true>(r3, 96, kv_lim, mq);
-        } else {
-          max32<false>(r0, 0, kv_lim, mq);
-          max32<false>(r1, 32, kv_lim, mq);
-          max32<false>(r2, 64, kv_lim, mq);
-          max32<false>(r3, 96, kv_lim, mq);
+          mask32(r0, 0, kv_lim);
+          mask32(r1, 32, kv_lim);
+          mask32(r2, 64, kv_lim);
+          mask32(r3, 96, kv_lim);
         }
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        max32(r0, mq);
+        max32(r1, mq);
+        max32(r2, mq);
+        max32(r3, mq);
         const float m = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
         m2 = m * p.score_log2;
         // p = 2^(x * c - m2 + 8): probabilities scaled by 256 so that small
@@ -781,22 +793,15 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
         const float off = (m2 == -INFINITY) ? 0.f : 8.f - m2;
         const float c = p.score_log2;
         float lq[4] = {0.f, 0.f, 0.f, 0.f};
-        if (need_mask) {
-          exp_pack32<true>(r0, 0, kv_lim, c, off, prow_s, row, lq);
-          exp_pack32<true>(r1, 32, kv_lim, c, off, prow_s, row, lq);
-          exp_pack32<true>(r2, 64, kv_lim, c, off, prow_s, row, lq);
-          exp_pack32<true>(r3, 96, kv_lim, c, off, prow_s, row, lq);
-        } else {
-          exp_pack32<false>(r0, 0, kv_lim, c, off, prow_s, row, lq);
-          exp_pack32<false>(r1, 32, kv_lim, c, off, prow_s, row, lq);
-          exp_pack32<false>(r2, 64, kv_lim, c, off, prow_s, row, lq);
-          exp_pack32<false>(r3, 96, kv_lim, c, off, prow_s, row, lq);
-        }
+        exp_pack32(r0, 0, c, off, prow_s, row, lq);
+        exp_pack32(r1, 32, c, off, prow_s, row, lq);
+        exp_pack32(r2, 64, c, off, prow_s, row, lq);
+        exp_pack32(r3, 96, c, off, prow_s, row, lq);
         l = (lq[0] + lq[1]) + (lq[2] + lq[3]);
       }
       // the row-meta slot is free once the epilogue has read item li - 4's
       if (li >= kMetaSlots &&
-          !bounded_wait(&bars->meta_free[li % kMetaSlots], ((li / kMetaSlots) - 1) & 1,
+          !warp_wait(&bars->meta_free[li % kMetaSlots], ((li / kMetaSlots) - 1) & 1,
                         abort, p.wait_ns)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
@@ -825,7 +830,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     const uint64_t pol_keep = l2_policy_evict_last();
     for (int li = 0; li < cnt; ++li) {
       const int w = li & 1, k = li >> 1;
-      if (!bounded_wait(&bars->meta_full[li % kMetaSlots],
+      if (!warp_wait(&bars->meta_full[li % kMetaSlots],
                         (li / kMetaSlots) & 1, abort, p.wait_ns)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
@@ -834,7 +839,7 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       mbar_arrive(&bars->meta_free[li % kMetaSlots]);
       const bool valid = mt.prow >= 0;
       const bool warp_valid = __any_sync(0xffffffffu, valid);
-      if (!bounded_wait(&bars->o_full[w], k & 1, abort, p.wait_ns)) {
+      if (!warp_wait(&bars->o_full[w], k & 1, abort, p.wait_ns)) {
         if (lane == 0 && !*abort) set_timeout(bars, p.status);
         break;
       }
@@ -842,7 +847,9 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       if (warp_valid) {
         const uint32_t o_tmem = tmem + lane_off + (uint32_t)(w * 256 + 128);
         uint8_t* dst = p.part_o + mt.prow * (int64_t)kD;
-#pragma unroll
+        // one half per iteration, the loop kept rolled: the instruction
+        // cache is shared with the other warp roles' loops
+#pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           uint32_t ra[32], rb[32];
           __syncwarp();
@@ -851,38 +858,36 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
           tmem_wait_ld();
           if (valid) {
             // The normalised row in V's code units is a convex combination
-            // of E4M3 V codes, so it stays within E4M3's range.  A half whose
-            // largest magnitude is at most p.e4m3_limit (0.5 in real units)
-            // is kept in E4M3 (rounding error at most 2^-4 of that, 0.031).
-            // A larger one goes to the bf16 overflow rows (error at most
+            // of E4M3 V codes, so it stays within E4M3's range; word k holds
+            // columns 4k .. 4k+3 of this half.  A half with a code above
+            // p.e4m3_max_code (magnitude kE4M3PartialLimit, 2.0 in real
+            // units) goes to the bf16 overflow rows instead (error at most
             // 2^-9 of the value), and its E4M3 half is filled with the NaN
             // code, which no partial produces (the conversion saturates), as
-            // the marker the combine looks for.  So the partials never cost
-            // more than a small fraction of the acceptance rule however large
-            // the output, and the common case moves 64 bytes per half.
-            float mx[4] = {0.f, 0.f, 0.f, 0.f};
+            // the marker the combine looks for.  So the E4M3 rounding error of
+            // a partial stays at most 2^-4 * 2.0 = 0.125 absolute however
+            // large the output, and the common case moves 64 bytes a half.
+            uint32_t o[16];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              mx[k & 3] = fmaxf(mx[k & 3], fabsf(__uint_as_float(ra[k])));
-              mx[k & 3] = fmaxf(mx[k & 3], fabsf(__uint_as_float(rb[k])));
+            for (int k = 0; k < 8; ++k) {
+              o[k] = pack_e4m3x4(__uint_as_float(ra[4 * k]) * mt.inv,
+                                 __uint_as_float(ra[4 * k + 1]) * mt.inv,
+                                 __uint_as_float(ra[4 * k + 2]) * mt.inv,
+                                 __uint_as_float(ra[4 * k + 3]) * mt.inv);
+              o[8 + k] = pack_e4m3x4(__uint_as_float(rb[4 * k]) * mt.inv,
+                                     __uint_as_float(rb[4 * k + 1]) * mt.inv,
+                                     __uint_as_float(rb[4 * k + 2]) * mt.inv,
+                                     __uint_as_float(rb[4 * k + 3]) * mt.inv);
             }
-            const float amax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * mt.inv;
-            uint8_t* d = dst + half * 64;
-            if (amax <= p.e4m3_limit) {
-              // word k holds columns 4k .. 4k+3 of this half; 64 bytes as
-              // two whole 32-byte sectors
-              uint32_t o[16];
+            // any magnitude byte above the limit: (b & 0x7F) + (0x7F - limit)
+            // carries into bit 7 exactly when b & 0x7F exceeds the limit, and
+            // no byte carries into the next (both terms are at most 0x7F)
+            uint32_t over = 0;
 #pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                o[k] = pack_e4m3x4(__uint_as_float(ra[4 * k]) * mt.inv,
-                                   __uint_as_float(ra[4 * k + 1]) * mt.inv,
-                                   __uint_as_float(ra[4 * k + 2]) * mt.inv,
-                                   __uint_as_float(ra[4 * k + 3]) * mt.inv);
-                o[8 + k] = pack_e4m3x4(__uint_as_float(rb[4 * k]) * mt.inv,
-                                       __uint_as_float(rb[4 * k + 1]) * mt.inv,
-                                       __uint_as_float(rb[4 * k + 2]) * mt.inv,
-                                       __uint_as_float(rb[4 * k + 3]) * mt.inv);
-              }
+            for (int k = 0; k < 16; ++k) over |= (o[k] & 0x7F7F7F7Fu) + p.e4m3_over4;
+            uint8_t* d = dst + half * 64;
+            if (!(over & 0x80808080u)) {
+              // 64 bytes as two whole 32-byte sectors
               st_global_v8_hint(d, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7],
                                 pol_keep);
               st_global_v8_hint(d + 32, o[8], o[9], o[10], o[11], o[12], o[13], o[14],
@@ -929,6 +934,13 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// Value of a non-negative E4M3 code 0x00 .. 0x7E (OCP E4M3: bias 7,
+// subnormals m * 2^-9), for the host-side limit above.
+double e4m3_code_value(uint32_t c) {
+  const int e = (int)(c >> 3), m = (int)(c & 7);
+  return e == 0 ? std::ldexp((double)m, -9) : std::ldexp(1.0 + m / 8.0, e - 7);
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
@@ -1021,7 +1033,15 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   p.part_vscale = a.part_vscale;
   p.part_lse = a.part_lse;
   p.part_big = a.part_big;
-  p.e4m3_limit = kE4M3PartialLimit / a.v_scale;
+  // the largest E4M3 magnitude code whose value (in V's code units) is at
+  // most kE4M3PartialLimit / v_scale; every code when that passes 448
+  {
+    const double lim = (double)kE4M3PartialLimit / (double)a.v_scale;
+    uint32_t c = 0;
+    while (c < 0x7E && e4m3_code_value(c + 1) <= lim) ++c;
+    if (lim >= 448.0) c = 0x7F;
+    p.e4m3_over4 = (0x7Fu - c) * 0x01010101u;
+  }
   p.status = pl.status;
   p.Hq = (int)pl.Hq;
   p.G = G;

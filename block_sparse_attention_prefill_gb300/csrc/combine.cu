@@ -102,7 +102,7 @@ combine_kernel(const TIn* __restrict__ part_o, const float* __restrict__ part_ls
 // per slot, all of a row's loads issued before any is used, and a 16-byte
 // overflow load for a marked half.  The partials are read once here: they
 // are evicted from L2 first.
-__global__ void __launch_bounds__(kWarpsPerBlock * 32, 4)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
 combine16_kernel(const uint8_t* __restrict__ part_o,
                  const uint8_t* __restrict__ part_big,
                  const float* __restrict__ part_lse,
@@ -145,11 +145,11 @@ combine16_kernel(const uint8_t* __restrict__ part_o,
 #pragma unroll
   for (int j = 0; j < kTopK; ++j) {
     const float wj = __shfl_sync(0xffffffffu, wl, (lane & 16) + j);
-    if (v[j].x == 0x7F7F7F7Fu) {
-      marked |= 1u << j;
-      continue;
-    }
-    const uint32_t w2[2] = {v[j].x, v[j].y};
+    // a marked half counts here as zeros (its NaN bytes must not reach the
+    // sums); its bf16 values are added below
+    const bool mk = v[j].x == 0x7F7F7F7Fu;
+    marked |= (uint32_t)mk << j;
+    const uint32_t w2[2] = {mk ? 0u : v[j].x, mk ? 0u : v[j].y};
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(

@@ -17,16 +17,20 @@ constexpr int kTopK = MSA_TOPK;       // pages per (token, KV head)
 constexpr int kTileM = 128;           // MMA rows per work item (tokens x G)
 
 // The plan's rows kernel: rows per round (a half-warp per row), its
-// threads, and the largest number of tiles (CTAs).  A tile is a multiple of
-// kRowTile rows, as few as keep the tile count within kMaxRowTiles: every
-// tile adds up the totals of all tiles in front of it.
+// threads, and its tiles (CTAs).  A tile is as few rounds of kRowTile rows
+// as keep the tile count within kMaxRowTiles, and at most kMaxRounds rounds
+// (above kMaxRowTiles * kMaxRounds * kRowTile rows the tile count grows
+// instead): every tile adds up the totals of all tiles in front of it.
 constexpr int kRowTile = 16;
 constexpr int kRowThreads = 256;
-constexpr int kMaxRowTiles = 512;
+constexpr int kMaxRowTiles = 1024;
+constexpr int kMaxRounds = 32;
 __host__ __device__ inline int64_t plan_tile_rows(int64_t rows) {
-  const int64_t rounds = (rows + (int64_t)kRowTile * kMaxRowTiles - 1) /
-                         ((int64_t)kRowTile * kMaxRowTiles);
-  return kRowTile * (rounds > 0 ? rounds : 1);
+  int64_t rounds = (rows + (int64_t)kRowTile * kMaxRowTiles - 1) /
+                   ((int64_t)kRowTile * kMaxRowTiles);
+  if (rounds < 1) rounds = 1;
+  if (rounds > kMaxRounds) rounds = kMaxRounds;
+  return kRowTile * rounds;
 }
 
 // Wall-time bound of every device-side wait (about a second).
@@ -45,11 +49,11 @@ cudaError_t launch_plan(const msa_plan_t& plan, const int32_t* topk,
                         const int32_t* block_table, cudaStream_t stream);
 
 // Split partials: per (token, query head, top-k slot) a 128-byte E4M3 row
-// in V's code units, two halves of 64 columns.  A half whose largest
+// in V's code units, two halves of 64 columns.  A half with a value whose
 // magnitude, in real units, is above kE4M3PartialLimit is kept in bf16 in
 // the slot's 256-byte overflow row instead, and its E4M3 half holds the NaN
 // code 0x7F in every byte as the marker.
-constexpr float kE4M3PartialLimit = 0.5f;
+constexpr float kE4M3PartialLimit = 2.0f;
 
 struct AttnArgs {
   const uint8_t* q;

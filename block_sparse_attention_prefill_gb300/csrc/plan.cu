@@ -165,16 +165,41 @@ struct TokenInfo {
   int64_t row0;
 };
 
-__device__ __forceinline__ TokenInfo token_info(const PlanDev& d, int t, int h) {
+// Per-request metadata (cu_seqlens_q, cu_seqlens_k, row offsets), copied
+// into shared memory by every CTA of the mark and scatter kernels when the
+// batch has at most kMetaCache requests, so that a thread's reads of it do
+// not add global round trips after its top-k entry; read from global memory
+// otherwise.
+constexpr int kMetaCache = 512;
+struct ReqMeta {
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  const int32_t* req_off;
+};
+
+__device__ __forceinline__ ReqMeta stage_req_meta(const PlanDev& d, int32_t* s_cuq,
+                                                  int32_t* s_cuk, int32_t* s_off) {
+  if (d.B >= kMetaCache) return ReqMeta{d.cu_q, d.cu_k, d.req_off};
+  for (int i = threadIdx.x; i <= d.B; i += blockDim.x) {
+    s_cuq[i] = d.cu_q[i];
+    s_cuk[i] = d.cu_k[i];
+    s_off[i] = d.req_off[i];
+  }
+  __syncthreads();
+  return ReqMeta{s_cuq, s_cuk, s_off};
+}
+
+__device__ __forceinline__ TokenInfo token_info(const PlanDev& d, const ReqMeta& m,
+                                                int t, int h) {
   TokenInfo k;
-  k.b = upper_index(d.cu_q, d.B, t);
-  k.i = t - d.cu_q[k.b];
-  const int64_t ql = d.cu_q[k.b + 1] - d.cu_q[k.b];
-  const int64_t sl = d.cu_k[k.b + 1] - d.cu_k[k.b];
+  k.b = upper_index(m.cu_q, d.B, t);
+  k.i = t - m.cu_q[k.b];
+  const int64_t ql = m.cu_q[k.b + 1] - m.cu_q[k.b];
+  const int64_t sl = m.cu_k[k.b + 1] - m.cu_k[k.b];
   k.pos = (int)(sl - ql + k.i);
   k.own = k.pos / kPage;
   k.P = (int)ceil_div(sl, kPage);
-  k.row0 = (int64_t)h * d.total_rows + d.req_off[k.b];
+  k.row0 = (int64_t)h * d.total_rows + m.req_off[k.b];
   return k;
 }
 
@@ -190,6 +215,9 @@ __global__ void __launch_bounds__(256) plan_mark_kernel(PlanDev d) {
   const bool live = e < total;
   const int64_t w = e / kTopK;
   const int32_t p = live ? d.topk[e] : -1;
+  const int valid_plan = d.counters[2];
+  __shared__ int32_t s_cuq[kMetaCache + 1], s_cuk[kMetaCache + 1], s_off[kMetaCache + 1];
+  const ReqMeta m = stage_req_meta(d, s_cuq, s_cuk, s_off);
   // ids of the same list at positions before j
   bool dup = false;
 #pragma unroll
@@ -198,10 +226,10 @@ __global__ void __launch_bounds__(256) plan_mark_kernel(PlanDev d) {
     dup |= (q < j) && (o == p);
   }
   bool keep = false;
-  if (live && d.counters[2] == 1) {
+  if (live && valid_plan == 1) {
     const int t = (int)(w / d.Hkv);
     const int h = (int)(w % d.Hkv);
-    const TokenInfo k = token_info(d, t, h);
+    const TokenInfo k = token_info(d, m, t, h);
     unsigned st = 0;
     if (p != -1) {
       if (p < -1 || p >= k.P) {
@@ -257,38 +285,47 @@ __device__ __forceinline__ void scan16(int c, int w, int* exc, int* exw, int* tc
 }
 
 // One CTA per tile of d.tile_rows rows (a multiple of 16, chosen on the
-// host so that there are at most kMaxRowTiles tiles), worked in rounds of
-// 16 rows, a half-warp per row.
+// host so that there are at most kMaxRowTiles tiles while that keeps a tile
+// within kMaxRounds rounds), worked in rounds of 16 rows, a half-warp per
+// row.
 //   pass 1  per round: lane l of the half-warp takes the 16-byte vectors
 //           [l * per, (l + 1) * per) of its row (rows are 16-byte aligned,
 //           W a multiple of 4), so the row is read and written as one
 //           contiguous span; the running count in front of every word is
 //           the lane's own popcounts plus an exclusive scan over the 16
-//           lanes; the row length goes to row_cnt, and the tile's totals
-//           (entries, work items) add up.
-//   totals  the tile publishes its totals and adds up those of all the
-//           tiles before it, read in parallel by the whole CTA (at most
-//           kMaxRowTiles - 1 words): the exclusive scan across tiles, with
-//           no kernel boundary and no chain of waits.
-//   pass 2  per round: row_ptr and each row's first work item; the round's
-//           work items and record headers dealt over all threads.
+//           lanes; the row length and, for a row that has entries, its
+//           record header (through block_table) stay in shared memory.
+//   totals  the tile publishes its totals (entries, work items) and adds up
+//           those of all the tiles before it, read in parallel by the whole
+//           CTA: the exclusive scan across tiles, with no kernel boundary and
+//           no chain of waits.
+//   pass 2  per round, from shared memory only: row_ptr, each row's first
+//           work item, and the round's work items and record headers dealt
+//           over all threads.
 __global__ void __launch_bounds__(kRowThreads) plan_rows_kernel(PlanDev d) {
   pdl_wait();
   pdl_trigger();
   static_assert(kRowThreads == 16 * kRowTile, "a half-warp per row");
+  constexpr int kReqCache = 1024;
   __shared__ int s_tile, s_fail;
-  __shared__ int s_cnt[kRowTile], s_exc[kRowTile], s_exw[kRowTile];
+  __shared__ int s_req[kReqCache + 1];               // req_off, when B fits
+  __shared__ int s_cnt[kMaxRounds * kRowTile];
+  __shared__ int4 s_hdr[kMaxRounds * kRowTile];      // record header without the count
+  __shared__ int2 s_item[kMaxRounds * kRowTile];     // work item: b, (h << 24) | p
+  __shared__ int s_exc[kRowTile], s_exw[kRowTile];
   __shared__ int s_red[3][kRowThreads / 32];
-  __shared__ int4 s_hdr[kRowTile];   // record header without the count
-  __shared__ int2 s_item[kRowTile];  // work item: request, (KV head, page)
   if (threadIdx.x == 0) {
     // tiles in launch order: every predecessor of a tile has started, so
     // waiting for its totals cannot deadlock
     s_tile = atomicAdd(&d.counters[3], 1);
     s_fail = 0;
   }
+  const bool cache_req = d.B < kReqCache;
+  if (cache_req)
+    for (int i = threadIdx.x; i <= d.B; i += kRowThreads) s_req[i] = d.req_off[i];
   __syncthreads();
   const int tile = s_tile;
+  const int32_t* req_off = cache_req ? s_req : d.req_off;
   const int sub = threadIdx.x & 15, k = threadIdx.x >> 4;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool ok = d.counters[2] == 1;
@@ -297,7 +334,7 @@ __global__ void __launch_bounds__(kRowThreads) plan_rows_kernel(PlanDev d) {
   const int64_t tile_r0 = (int64_t)tile * d.tile_rows;
   const int rounds = d.tile_rows / kRowTile;
 
-  // ---- pass 1: row lengths and word prefixes
+  // ---- pass 1: row lengths, word prefixes, record headers
   int tc = 0, tw = 0;  // the tile's totals, kept by lane 0 of each half-warp
   for (int rd = 0; rd < rounds; ++rd) {
     const int64_t r = tile_r0 + rd * kRowTile + k;
@@ -323,6 +360,7 @@ __global__ void __launch_bounds__(kRowThreads) plan_rows_kernel(PlanDev d) {
       const int n = __shfl_up_sync(0xffffffffu, incl, o, 16);
       if (sub >= o) incl += n;
     }
+    // every lane takes part in the shuffle (a row past the end has 0)
     const int total = __shfl_sync(0xffffffffu, incl, 15, 16);
     if (live) {
       int4* __restrict__ pre = reinterpret_cast<int4*>(d.word_pre + r * d.W);
@@ -339,11 +377,23 @@ __global__ void __launch_bounds__(kRowThreads) plan_rows_kernel(PlanDev d) {
           pre[x] = o;
         }
       }
-      if (sub == 0) d.row_cnt[r] = total;
     }
-    if (sub == 0 && live) {
-      tc += total;
-      tw += (total + d.C - 1) / d.C;
+    if (sub == 0) {
+      const int idx = rd * kRowTile + k;
+      s_cnt[idx] = total;
+      if (total > 0) {
+        tc += total;
+        tw += (total + d.C - 1) / d.C;
+        const int h = (int)(r / d.total_rows);
+        const int64_t rq = r - (int64_t)h * d.total_rows;
+        const int b = upper_index(req_off, d.B, rq);
+        const int p = (int)(rq - req_off[b]);
+        const int32_t phys = d.block_table[(int64_t)b * d.bt_stride + p];
+        // record header: KV tile row of the pool, (token count), first key
+        // position of the page, first query head of the KV head
+        s_hdr[idx] = make_int4((phys * d.Hkv + h) * kPage, 0, p * kPage, h * d.G);
+        s_item[idx] = make_int2(b, (h << 24) | p);
+      }
     }
   }
 
@@ -367,8 +417,6 @@ __global__ void __launch_bounds__(kRowThreads) plan_rows_kernel(PlanDev d) {
     }
     s_red[2][0] = c;
     s_red[2][1] = w;
-    // row_cnt and word_pre of this tile are written before its totals are
-    // visible to anyone; the totals themselves need no further ordering
     st_relaxed_u64(&d.tile_state[tile],
                    (1ull << 63) | ((uint64_t)(uint32_t)w << 31) | (uint32_t)c);
   }
@@ -427,49 +475,39 @@ __global__ void __launch_bounds__(kRowThreads) plan_rows_kernel(PlanDev d) {
   // ---- pass 2: row_ptr, first work items, the work items of each round
   for (int rd = 0; rd < rounds; ++rd) {
     const int64_t r0 = tile_r0 + rd * kRowTile;
+    const int* cnt = s_cnt + rd * kRowTile;
     if (warp == 0) {
       const int64_t r = r0 + lane;
-      const int c = (lane < kRowTile && ok && r < d.rows) ? d.row_cnt[r] : 0;
+      const int c = lane < kRowTile ? cnt[lane] : 0;
       const int ch = (c + d.C - 1) / d.C;
       int exc, exw, rc, rw;
       scan16(c, ch, &exc, &exw, &rc, &rw);
       if (lane < kRowTile) {
-        s_cnt[lane] = c;
         s_exc[lane] = exc;
         s_exw[lane] = exw;
         if (r < d.rows) {
           d.row_ptr[r] = base_c + exc;
           d.row_wptr[r] = base_w + exw;
-          if (c > 0) {
-            const int h = (int)(r / d.total_rows);
-            const int64_t rq = r - (int64_t)h * d.total_rows;
-            const int b = upper_index(d.req_off, d.B, rq);
-            const int p = (int)(rq - d.req_off[b]);
-            const int32_t phys = d.block_table[(int64_t)b * d.bt_stride + p];
-            // record header: KV tile row of the pool, (token count), first
-            // key position of the page, first query head of the KV head
-            s_hdr[lane] = make_int4((phys * d.Hkv + h) * kPage, 0, p * kPage, h * d.G);
-            s_item[lane] = make_int2(b, (h << 24) | p);
-          }
         }
       }
     }
     __syncthreads();
-    const int rw = s_exw[kRowTile - 1] + (s_cnt[kRowTile - 1] + d.C - 1) / d.C;
+    const int rw = s_exw[kRowTile - 1] + (cnt[kRowTile - 1] + d.C - 1) / d.C;
     for (int q = threadIdx.x; q < rw; q += kRowThreads) {
       const int j = upper_index(s_exw, kRowTile, q);  // last row starting at or before q
       const int ch = q - s_exw[j];
-      const int n = min(d.C, s_cnt[j] - ch * d.C);
+      const int n = min(d.C, cnt[j] - ch * d.C);
       const int64_t wi = (int64_t)base_w + q;
+      const int2 item = s_item[rd * kRowTile + j];
       reinterpret_cast<int4*>(d.work)[wi] =
-          make_int4(base_c + s_exc[j] + ch * d.C, n, s_item[j].x, s_item[j].y);
-      int4 hdr = s_hdr[j];
+          make_int4(base_c + s_exc[j] + ch * d.C, n, item.x, item.y);
+      int4 hdr = s_hdr[rd * kRowTile + j];
       hdr.y = n;
       d.records[wi * d.rec_stride] = hdr;
     }
-    base_c += s_exc[kRowTile - 1] + s_cnt[kRowTile - 1];
+    base_c += s_exc[kRowTile - 1] + cnt[kRowTile - 1];
     base_w += rw;
-    __syncthreads();  // the round's shared arrays are rewritten next round
+    __syncthreads();  // s_exc / s_exw are rewritten next round
   }
 }
 
@@ -479,15 +517,20 @@ __global__ void __launch_bounds__(256) plan_scatter_kernel(PlanDev d) {
   pdl_wait();
   pdl_trigger();
   const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= (int64_t)d.T * d.Hkv * kTopK) return;
-  if (d.counters[2] != 1) return;
+  const bool live = e < (int64_t)d.T * d.Hkv * kTopK;
   const int64_t w = e / kTopK;
   const int j = (int)(e % kTopK);
-  if (!((d.slot_mask[w] >> j) & 1u)) return;
+  // the entry's loads go out together with the metadata's
+  const int32_t p = live ? d.topk[e] : -1;
+  const uint32_t mask = live ? d.slot_mask[w] : 0u;
+  const int valid_plan = d.counters[2];
+  __shared__ int32_t s_cuq[kMetaCache + 1], s_cuk[kMetaCache + 1], s_off[kMetaCache + 1];
+  const ReqMeta m = stage_req_meta(d, s_cuq, s_cuk, s_off);
+  if (!live || valid_plan != 1 || !((mask >> j) & 1u)) return;
   const int t = (int)(w / d.Hkv);
   const int h = (int)(w % d.Hkv);
-  const TokenInfo k = token_info(d, t, h);
-  const int64_t r = k.row0 + d.topk[e];
+  const TokenInfo k = token_info(d, m, t, h);
+  const int64_t r = k.row0 + p;
   const int64_t wi = r * d.W + (k.i >> 5);
   const uint32_t below = (1u << (k.i & 31)) - 1u;
   const int rank = d.word_pre[wi] + __popc(d.bitmap[wi] & below);

@@ -141,7 +141,7 @@ typedef struct msa_plan {
   int32_t *word_pre;           /* [rows * bitmap_words] tokens before word  */
   int32_t *row_cnt;            /* [rows] entries of the row                 */
   int32_t *row_wptr;           /* [rows] first work item of the row         */
-  uint64_t *tile_state;        /* [<= 512] published totals of row tiles    */
+  uint64_t *tile_state;        /* [row tiles] published tile totals         */
   int32_t *row_ptr;            /* [rows + 1]                                */
   int32_t *q_idx;              /* [max_nnz] global query token ids          */
   uint8_t *slot;               /* [max_nnz] top-k position j                */

@@ -4,9 +4,10 @@ The attention kernel keeps each per-page partial output, normalised by its
 own softmax sum, in the code units of V, and the combine applies v_scale.
 In those units the partial is a convex combination of E4M3 V codes, so it
 stays inside E4M3's range.  Each half of a partial row (64 columns) is kept
-in E4M3 when its largest magnitude, in real units, is at most 0.5 -- the
-rounding error is then at most 2^-4 * 0.5 = 0.031 -- and in bf16 otherwise
-(relative error at most 2^-9).  This test restates the per-page arithmetic
+in E4M3 when every value, rounded to E4M3, is at most 2.0 in magnitude in
+real units -- the rounding error is then at most 2^-4 * 2.0 = 0.125, half
+the rule's hard bound -- and in bf16 otherwise (relative error at most
+2^-9).  This test restates the per-page arithmetic
 in float64:
 
 - P = 2^(x*c - m*c + 8) rounded to E4M3;
@@ -48,19 +49,20 @@ def _bf16(x):
         torch.float64).numpy()
 
 
-E4M3_HALF_LIMIT = 0.5   # real units
+E4M3_HALF_LIMIT = 2.0   # real units
 
 
 def _adaptive(o_codes, v_scale):
-    """Each 64-column half in E4M3 when its largest magnitude (real units)
-    is at most E4M3_HALF_LIMIT, else in bf16; returns real units."""
+    """Each 64-column half in E4M3 when every value rounded to E4M3 is at
+    most E4M3_HALF_LIMIT in magnitude (real units), else in bf16; returns
+    real units."""
     out = np.empty_like(o_codes)
     for h in (slice(0, 64), slice(64, 128)):
-        half = o_codes[h]
-        if np.abs(half).max() * v_scale <= E4M3_HALF_LIMIT:
-            out[h] = _e4m3(half) * v_scale
+        e = _e4m3(o_codes[h])
+        if np.abs(e).max() * v_scale <= E4M3_HALF_LIMIT:
+            out[h] = e * v_scale
         else:
-            out[h] = _bf16(half) * v_scale
+            out[h] = _bf16(o_codes[h]) * v_scale
     return out
 
 

@@ -161,3 +161,15 @@ def test_decode_plan_over_65535_rows():
     nnz, nwork = plan.counters()
     check_plan(plan, nnz, nwork, w, R)
     assert plan.status() == 0
+
+
+@pytest.mark.parametrize("hq,q_lens,seq_lens", [
+    (16, [100, 30], [1000, 300]),      # 8 + 3 = 11 rows
+    (8, [200, 7, 50], [3000, 7, 500]),  # 24 + 1 + 4 = 29 rows
+])
+def test_plan_odd_row_counts(hq, q_lens, seq_lens):
+    # one KV head and an odd number of pages: the last row tile ends inside
+    # a warp (two rows per warp, a half-warp each)
+    w = workloads.make_batch("odd", q_lens, seq_lens, hq, 1, seed=9)
+    assert (w.Hkv * w.total_rows) % 2 == 1
+    compare_plan(w)
