@@ -16,21 +16,29 @@ constexpr int kPage = MSA_PAGE_SIZE;  // tokens per KV page
 constexpr int kTopK = MSA_TOPK;       // pages per (token, KV head)
 constexpr int kTileM = 128;           // MMA rows per work item (tokens x G)
 
-// The plan's rows kernel: rows per round (a half-warp per row), its
-// threads, and its tiles (CTAs).  A tile is as few rounds of kRowTile rows
-// as keep the tile count within kMaxRowTiles, and at most kMaxRounds rounds
-// (above kMaxRowTiles * kMaxRounds * kRowTile rows the tile count grows
-// instead): every tile adds up the totals of all tiles in front of it.
-constexpr int kRowTile = 16;
+// The plan's rows kernel: its threads, the lanes that share one row (the
+// row's 16-byte vectors rounded up to a power of two, at most 16), and its
+// tiles (CTAs).  A round is kRowThreads / lanes rows; a tile is a whole
+// number of rounds, at most kMaxTileRows rows, and as few as keep the tile
+// count within kMaxRowTiles (above kMaxRowTiles * kMaxTileRows rows the
+// tile count grows instead): every tile adds up the totals of all tiles in
+// front of it, so few tiles keep those reads few.
 constexpr int kRowThreads = 256;
-constexpr int kMaxRowTiles = 1024;
-constexpr int kMaxRounds = 32;
-__host__ __device__ inline int64_t plan_tile_rows(int64_t rows) {
-  int64_t rounds = (rows + (int64_t)kRowTile * kMaxRowTiles - 1) /
-                   ((int64_t)kRowTile * kMaxRowTiles);
-  if (rounds < 1) rounds = 1;
-  if (rounds > kMaxRounds) rounds = kMaxRounds;
-  return kRowTile * rounds;
+constexpr int kMaxRowTiles = 256;
+constexpr int kMaxTileRows = 512;  // a multiple of every round (16 .. 256 rows)
+__host__ __device__ inline int plan_row_lane_shift(int64_t W) {
+  const int64_t nv = W / 4;  // 16-byte vectors per row
+  int s = 0;
+  while (s < 4 && ((int64_t)1 << s) < nv) ++s;
+  return s;
+}
+__host__ __device__ inline int64_t plan_tile_rows(int64_t rows, int64_t W) {
+  const int64_t rp = kRowThreads >> plan_row_lane_shift(W);  // rows per round
+  int64_t tr = (rows + kMaxRowTiles - 1) / kMaxRowTiles;
+  tr = (tr + rp - 1) / rp * rp;
+  if (tr < rp) tr = rp;
+  if (tr > kMaxTileRows) tr = kMaxTileRows;
+  return tr;
 }
 
 // Wall-time bound of every device-side wait (about a second).

@@ -77,7 +77,7 @@ int plan_shape(int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t R,
   s->C = kTileM / G;
   s->W = 4 * ceil_div(max_q, 128);  // 32-bit words, a multiple of 4
   s->rows = Hkv * R;
-  s->ntiles = ceil_div(s->rows, plan_tile_rows(s->rows));
+  s->ntiles = ceil_div(s->rows, plan_tile_rows(s->rows, s->W));
   s->max_nnz = T * Hkv * kTopK;
   s->max_work = ceil_div(s->max_nnz, s->C) + std::min(s->rows, s->max_nnz);
   // every index the kernels form must fit in int32

@@ -5,25 +5,28 @@
 // total_kv_blocks, qhead_per_kv, return_schedule=True); vLLM PR 60930,
 // Details / "Host sync": the plan stays on the device, no host copy.)
 //
-// Four kernels, all on `stream`, no host synchronisation; every kernel
+// Five kernels, all on `stream`, no host synchronisation; every kernel
 // after the first is a programmatic dependent launch (its launch overlaps
 // the tail of the kernel before it, its work does not):
 //   prep     CTA 0: per-request row offsets (sum of page counts), checks,
 //            status word, counters; every CTA: clears its share of the
-//            (row, token) membership bitmap and of the tile states
+//            (row, token) membership bitmap
 //   mark     one thread per top-k entry: validate the id, drop repeats, set
 //            one bit per kept page in the membership bitmap; the (token,
 //            KV head) list's 16 threads together write its slot mask.  This
 //            is the histogram, kept as bits: repeats collapse and the order
 //            of arrival cannot change the result.
-//   rows     one CTA per tile of rows (at most kMaxRowTiles tiles), tiles
-//            taken in launch order from a ticket counter, a half-warp per
-//            row: the row's length (popcount of its words) and the running
-//            count in front of every word; the tile publishes its totals
-//            (entries, work items) and adds up all its predecessors'
-//            published totals in parallel (the scan, with no kernel
-//            boundary and no chain of waits); then row_ptr, each row's first
-//            work item, and the tile's work items and record headers.
+//   rows     one CTA per tile of rows (at most kMaxRowTiles tiles while a
+//            tile stays within kMaxTileRows rows), 1 to 16 lanes per row by
+//            the row's width: the row's length (popcount of its words), the
+//            running count in front of every word, and the tile's totals
+//            (entries, work items).
+//   emit     one CTA per tile: the sum of the totals of the tiles before it
+//            (the exclusive scan across tiles: at most kMaxRowTiles loads,
+//            all issued at once), a scan over its own rows, then row_ptr,
+//            each row's first work item, and the tile's work items and
+//            record headers.  A tile waits for no other tile: the kernel
+//            boundary orders them.
 //   scatter  one thread per top-k entry: each kept entry goes to
 //            row_ptr + (tokens of the same row before it), found in O(1)
 //            from the word prefix and a popcount; it also fills the token
@@ -95,8 +98,8 @@ struct PlanDev {
   int32_t* word_pre;     // [rows * W] tokens of the row before each word
   int32_t* row_cnt;      // [rows] entries of the row
   int32_t* row_wptr;     // [rows] first work item of the row
-  uint64_t* tile_state;  // [ntiles] published tile totals (see rows)
-  int ntiles, tile_rows;
+  uint64_t* tile_state;  // [ntiles] tile totals: entries << 32 | work items
+  int ntiles, tile_rows, lane_shift;  // rows kernel tiling (see rows)
   int32_t* row_ptr;
   int32_t* q_idx;
   uint8_t* slot;
@@ -117,7 +120,6 @@ __global__ void __launch_bounds__(kScanThreads) plan_prep_kernel(PlanDev d,
     const int64_t stride = (int64_t)gridDim.x * kScanThreads;
     const int64_t i0 = (int64_t)blockIdx.x * kScanThreads + threadIdx.x;
     for (int64_t i = i0; i < bitmap_vec; i += stride) bm[i] = make_uint4(0u, 0u, 0u, 0u);
-    for (int64_t i = i0; i < d.ntiles; i += stride) d.tile_state[i] = 0ull;
   }
   if (blockIdx.x != 0) return;
   __shared__ int s_bad;
@@ -155,8 +157,7 @@ __global__ void __launch_bounds__(kScanThreads) plan_prep_kernel(PlanDev d,
     d.counters[0] = 0;
     d.counters[1] = 0;
     d.counters[2] = st ? 0 : 1;
-    d.counters[3] = 0;      // the rows kernel's tile ticket
-    d.row_ptr[d.rows] = 0;  // the rows kernel's last tile writes the total
+    d.row_ptr[d.rows] = 0;  // the emit kernel's last tile writes the total
   }
 }
 
@@ -252,262 +253,238 @@ __global__ void __launch_bounds__(256) plan_mark_kernel(PlanDev d) {
     d.slot_mask[w] = (uint16_t)((bal >> (lane & ~(kTopK - 1))) & 0xFFFFu);
 }
 
-// Tile state word: bit 63 set once published, bits 31..61 the tile's work
-// items, bits 0..30 its CSR entries (both below 2^31, checked on the host).
-__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
-  uint64_t v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
-  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+// The rows of a tile, kPass1Rounds rounds at a time: lane `sub` of a row
+// holds the 16-byte vectors [sub * per, (sub + 1) * per) of the row (rows
+// are 16-byte aligned, W a multiple of 4), so a row is read, and its word
+// prefixes written, as one contiguous span.  The running count in front of
+// each word is the lane's own popcounts plus an exclusive scan over the
+// row's lanes.  When a lane has one vector per row, a group's vectors are
+// all loaded before the first is used.
+constexpr int kPass1Rounds = 4;
+
+// Packed (entries, work items) sums: entries in the high word, work items
+// in the low word (both below 2^31, so sums of them cannot carry from one
+// word into the other).
+__device__ __forceinline__ uint64_t pack_cw(int c, int w) {
+  return ((uint64_t)(uint32_t)c << 32) | (uint32_t)w;
 }
 
-// Exclusive scan of (c, w) over the 16 rows of a round, in warp 0; the
-// round's totals come back in *tc / *tw.
-__device__ __forceinline__ void scan16(int c, int w, int* exc, int* exw, int* tc,
-                                       int* tw) {
-  const int lane = threadIdx.x & 31;
-  int ic = c, iw = w;
+// Inclusive scan over the CTA of one 64-bit value per thread; every thread
+// also receives the total.
+__device__ __forceinline__ uint64_t block_incl_scan64(uint64_t v, uint64_t* s_warp,
+                                                      uint64_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int nc = __shfl_up_sync(0xffffffffu, ic, o);
-    const int nw = __shfl_up_sync(0xffffffffu, iw, o);
-    if (lane >= o) {
-      ic += nc;
-      iw += nw;
-    }
+    const uint64_t n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
   }
-  *exc = ic - c;
-  *exw = iw - w;
-  *tc = __shfl_sync(0xffffffffu, ic, 31);
-  *tw = __shfl_sync(0xffffffffu, iw, 31);
+  __syncthreads();  // s_warp may still be read from a previous scan
+  if (lane == 31) s_warp[warp] = v;
+  __syncthreads();
+  uint64_t before = 0, all = 0;
+#pragma unroll
+  for (int i = 0; i < kRowThreads / 32; ++i) {
+    const uint64_t x = s_warp[i];
+    before += i < warp ? x : 0ull;
+    all += x;
+  }
+  *total = all;
+  return before + v;
 }
 
-// One CTA per tile of d.tile_rows rows (a multiple of 16, chosen on the
-// host so that there are at most kMaxRowTiles tiles while that keeps a tile
-// within kMaxRounds rounds), worked in rounds of 16 rows, a half-warp per
-// row.
-//   pass 1  per round: lane l of the half-warp takes the 16-byte vectors
-//           [l * per, (l + 1) * per) of its row (rows are 16-byte aligned,
-//           W a multiple of 4), so the row is read and written as one
-//           contiguous span; the running count in front of every word is
-//           the lane's own popcounts plus an exclusive scan over the 16
-//           lanes; the row length and, for a row that has entries, its
-//           record header (through block_table) stay in shared memory.
-//   totals  the tile publishes its totals (entries, work items) and adds up
-//           those of all the tiles before it, read in parallel by the whole
-//           CTA: the exclusive scan across tiles, with no kernel boundary and
-//           no chain of waits.
-//   pass 2  per round, from shared memory only: row_ptr, each row's first
-//           work item, and the round's work items and record headers dealt
-//           over all threads.
+// One CTA per tile of d.tile_rows rows (a whole number of rounds; the host
+// keeps the tile count within kMaxRowTiles while a tile stays within
+// kMaxTileRows rows).  L = 2^d.lane_shift lanes share a row, kRowThreads / L
+// rows per round.  Writes each row's length (row_cnt), the running count in
+// front of every word (word_pre), and the tile's totals (entries, work
+// items) for the emit kernel.
 __global__ void __launch_bounds__(kRowThreads) plan_rows_kernel(PlanDev d) {
   pdl_wait();
   pdl_trigger();
-  static_assert(kRowThreads == 16 * kRowTile, "a half-warp per row");
-  constexpr int kReqCache = 1024;
-  __shared__ int s_tile, s_fail;
-  __shared__ int s_req[kReqCache + 1];               // req_off, when B fits
-  __shared__ int s_cnt[kMaxRounds * kRowTile];
-  __shared__ int4 s_hdr[kMaxRounds * kRowTile];      // record header without the count
-  __shared__ int2 s_item[kMaxRounds * kRowTile];     // work item: b, (h << 24) | p
-  __shared__ int s_exc[kRowTile], s_exw[kRowTile];
-  __shared__ int s_red[3][kRowThreads / 32];
-  if (threadIdx.x == 0) {
-    // tiles in launch order: every predecessor of a tile has started, so
-    // waiting for its totals cannot deadlock
-    s_tile = atomicAdd(&d.counters[3], 1);
-    s_fail = 0;
+  __shared__ int s_cnt[kMaxTileRows];
+  __shared__ uint64_t s_warp[kRowThreads / 32];
+  const int tile = blockIdx.x;
+  const int L = 1 << d.lane_shift;
+  const int sub = threadIdx.x & (L - 1), k = threadIdx.x >> d.lane_shift;
+  const int rp = kRowThreads >> d.lane_shift;  // rows per round
+  const int rounds = d.tile_rows / rp;
+  const int nv = d.W >> 2;
+  const int per = (nv + L - 1) >> d.lane_shift;
+  const int64_t r0 = (int64_t)tile * d.tile_rows;
+  const bool ok = d.counters[2] == 1;
+
+  for (int rd0 = 0; rd0 < rounds; rd0 += kPass1Rounds) {
+    uint4 v[kPass1Rounds];
+#pragma unroll
+    for (int u = 0; u < kPass1Rounds; ++u) {
+      const int64_t r = r0 + (int64_t)(rd0 + u) * rp + k;
+      v[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (per == 1 && ok && rd0 + u < rounds && r < d.rows && sub < nv)
+        v[u] = reinterpret_cast<const uint4*>(d.bitmap + r * d.W)[sub];
+    }
+#pragma unroll
+    for (int u = 0; u < kPass1Rounds; ++u) {
+      const int rd = rd0 + u;
+      if (rd >= rounds) break;  // the same for the whole CTA
+      const int64_t r = r0 + (int64_t)rd * rp + k;
+      const bool live = ok && r < d.rows;
+      const uint4* __restrict__ words = reinterpret_cast<const uint4*>(d.bitmap + r * d.W);
+      int own = 0;
+      if (per == 1) {
+        own = __popc(v[u].x) + __popc(v[u].y) + __popc(v[u].z) + __popc(v[u].w);
+      } else if (live) {
+        for (int u0 = 0; u0 < per; u0 += 4) {
+          uint4 w4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int x = sub * per + u0 + i;
+            w4[i] = (u0 + i < per && x < nv) ? words[x] : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            own += __popc(w4[i].x) + __popc(w4[i].y) + __popc(w4[i].z) + __popc(w4[i].w);
+        }
+      }
+      int incl = own;
+      for (int o = 1; o < L; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o, L);
+        if (sub >= o) incl += n;
+      }
+      // every lane takes part in the shuffle (a row past the end has 0)
+      const int total = __shfl_sync(0xffffffffu, incl, L - 1, L);
+      if (sub == 0) s_cnt[rd * rp + k] = total;
+      if (live) {
+        int4* __restrict__ pre = reinterpret_cast<int4*>(d.word_pre + r * d.W);
+        int run = incl - own;
+        for (int i = 0; i < per; ++i) {
+          const int x = sub * per + i;
+          if (x < nv) {
+            const uint4 w1 = per == 1 ? v[u] : words[x];
+            int4 o;
+            o.x = run; run += __popc(w1.x);
+            o.y = run; run += __popc(w1.y);
+            o.z = run; run += __popc(w1.z);
+            o.w = run; run += __popc(w1.w);
+            pre[x] = o;
+          }
+        }
+      }
+    }
   }
+  __syncthreads();
+  // row lengths out; the tile's totals
+  uint64_t mine = 0;
+  for (int i = threadIdx.x; i < d.tile_rows; i += kRowThreads) {
+    const int c = s_cnt[i];
+    if (r0 + i < d.rows) d.row_cnt[r0 + i] = c;
+    mine += pack_cw(c, (c + d.C - 1) / d.C);
+  }
+  uint64_t all;
+  block_incl_scan64(mine, s_warp, &all);
+  if (threadIdx.x == 0) d.tile_state[tile] = all;
+}
+
+// One CTA per tile of the rows kernel, launched after it: adds up the
+// totals of the tiles before it (all final by now: the exclusive scan
+// across tiles), scans its own rows (two per thread), and writes row_ptr,
+// each row's first work item, and the tile's work items and record headers
+// dealt over all threads.  The last tile closes the CSR and writes the
+// totals.
+__global__ void __launch_bounds__(kRowThreads) plan_emit_kernel(PlanDev d) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int kReqCache = 1024;
+  __shared__ int s_req[kReqCache + 1];   // req_off, when B fits
+  __shared__ int s_cnt[kMaxTileRows];    // entries of each row
+  __shared__ int s_exc[kMaxTileRows];    // first entry in the tile
+  __shared__ int s_exw[kMaxTileRows];    // first work item in the tile
+  __shared__ int4 s_hdr[kMaxTileRows];   // record header without the count
+  __shared__ int2 s_item[kMaxTileRows];  // work item: b, (h << 24) | p
+  __shared__ uint64_t s_warp[kRowThreads / 32];
+  const int tile = blockIdx.x;
+  const int64_t r0 = (int64_t)tile * d.tile_rows;
   const bool cache_req = d.B < kReqCache;
+  // the loads that do not depend on one another go out together
+  uint64_t pred = 0;
+  for (int i = threadIdx.x; i < tile; i += kRowThreads) pred += d.tile_state[i];
+  const int i0 = 2 * threadIdx.x;  // this thread's rows: i0, i0 + 1
+  int cnt[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e)
+    cnt[e] = (i0 + e < d.tile_rows && r0 + i0 + e < d.rows) ? d.row_cnt[r0 + i0 + e] : 0;
   if (cache_req)
     for (int i = threadIdx.x; i <= d.B; i += kRowThreads) s_req[i] = d.req_off[i];
   __syncthreads();
-  const int tile = s_tile;
   const int32_t* req_off = cache_req ? s_req : d.req_off;
-  const int sub = threadIdx.x & 15, k = threadIdx.x >> 4;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool ok = d.counters[2] == 1;
-  const int nv = d.W >> 2;
-  const int per = (nv + 15) >> 4;
-  const int64_t tile_r0 = (int64_t)tile * d.tile_rows;
-  const int rounds = d.tile_rows / kRowTile;
-
-  // ---- pass 1: row lengths, word prefixes, record headers
-  int tc = 0, tw = 0;  // the tile's totals, kept by lane 0 of each half-warp
-  for (int rd = 0; rd < rounds; ++rd) {
-    const int64_t r = tile_r0 + rd * kRowTile + k;
-    const bool live = ok && r < d.rows;
-    const uint4* __restrict__ words = reinterpret_cast<const uint4*>(d.bitmap + r * d.W);
-    int own = 0;
-    if (live) {
-      for (int u0 = 0; u0 < per; u0 += 4) {
-        uint4 v[4];
+  int32_t phys[2];
+  int hb[2], hp[2], hh[2];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int x = sub * per + u0 + u;
-          v[u] = (u0 + u < per && x < nv) ? words[x] : make_uint4(0u, 0u, 0u, 0u);
-        }
+  for (int e = 0; e < 2; ++e) {
+    const int64_t r = r0 + i0 + e;
+    phys[e] = 0;
+    hb[e] = hp[e] = hh[e] = 0;
+    if (i0 + e < d.tile_rows && r < d.rows) {
+      const int h = (int)(r / d.total_rows);
+      const int64_t rq = r - (int64_t)h * d.total_rows;
+      const int b = upper_index(req_off, d.B, rq);
+      const int p = (int)(rq - req_off[b]);
+      phys[e] = d.block_table[(int64_t)b * d.bt_stride + p];
+      hb[e] = b;
+      hp[e] = p;
+      hh[e] = h;
+    }
+  }
+  uint64_t base;
+  block_incl_scan64(pred, s_warp, &base);
+  const int base_c = (int)(base >> 32), base_w = (int)(uint32_t)base;
+  const int w0 = (cnt[0] + d.C - 1) / d.C, w1 = (cnt[1] + d.C - 1) / d.C;
+  uint64_t all;
+  const uint64_t incl = block_incl_scan64(pack_cw(cnt[0] + cnt[1], w0 + w1), s_warp, &all);
+  int ex_c = (int)(incl >> 32) - (cnt[0] + cnt[1]);
+  int ex_w = (int)(uint32_t)incl - (w0 + w1);
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          own += __popc(v[u].x) + __popc(v[u].y) + __popc(v[u].z) + __popc(v[u].w);
-      }
-    }
-    int incl = own;
-#pragma unroll
-    for (int o = 1; o < 16; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, incl, o, 16);
-      if (sub >= o) incl += n;
-    }
-    // every lane takes part in the shuffle (a row past the end has 0)
-    const int total = __shfl_sync(0xffffffffu, incl, 15, 16);
-    if (live) {
-      int4* __restrict__ pre = reinterpret_cast<int4*>(d.word_pre + r * d.W);
-      int run = incl - own;
-      for (int u = 0; u < per; ++u) {
-        const int x = sub * per + u;
-        if (x < nv) {
-          const uint4 v = words[x];
-          int4 o;
-          o.x = run; run += __popc(v.x);
-          o.y = run; run += __popc(v.y);
-          o.z = run; run += __popc(v.z);
-          o.w = run; run += __popc(v.w);
-          pre[x] = o;
-        }
-      }
-    }
-    if (sub == 0) {
-      const int idx = rd * kRowTile + k;
-      s_cnt[idx] = total;
-      if (total > 0) {
-        tc += total;
-        tw += (total + d.C - 1) / d.C;
-        const int h = (int)(r / d.total_rows);
-        const int64_t rq = r - (int64_t)h * d.total_rows;
-        const int b = upper_index(req_off, d.B, rq);
-        const int p = (int)(rq - req_off[b]);
-        const int32_t phys = d.block_table[(int64_t)b * d.bt_stride + p];
+  for (int e = 0; e < 2; ++e) {
+    const int i = i0 + e;
+    const int64_t r = r0 + i;
+    if (i < d.tile_rows) {
+      s_cnt[i] = cnt[e];
+      s_exc[i] = ex_c;
+      s_exw[i] = ex_w;
+      if (cnt[e] > 0) {
         // record header: KV tile row of the pool, (token count), first key
         // position of the page, first query head of the KV head
-        s_hdr[idx] = make_int4((phys * d.Hkv + h) * kPage, 0, p * kPage, h * d.G);
-        s_item[idx] = make_int2(b, (h << 24) | p);
+        s_hdr[i] = make_int4((phys[e] * d.Hkv + hh[e]) * kPage, 0, hp[e] * kPage,
+                             hh[e] * d.G);
+        s_item[i] = make_int2(hb[e], (hh[e] << 24) | hp[e]);
+      }
+      if (r < d.rows) {
+        d.row_ptr[r] = base_c + ex_c;
+        d.row_wptr[r] = base_w + ex_w;
       }
     }
+    ex_c += cnt[e];
+    ex_w += e == 0 ? w0 : w1;
   }
-
-  // ---- the tile's totals; publish them; add up the predecessors'
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    tc += __shfl_xor_sync(0xffffffffu, tc, o);
-    tw += __shfl_xor_sync(0xffffffffu, tw, o);
-  }
-  if (lane == 0) {
-    s_red[0][warp] = tc;
-    s_red[1][warp] = tw;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int c = 0, w = 0;
-#pragma unroll
-    for (int i = 0; i < kRowThreads / 32; ++i) {
-      c += s_red[0][i];
-      w += s_red[1][i];
-    }
-    s_red[2][0] = c;
-    s_red[2][1] = w;
-    st_relaxed_u64(&d.tile_state[tile],
-                   (1ull << 63) | ((uint64_t)(uint32_t)w << 31) | (uint32_t)c);
-  }
-  int pc = 0, pw = 0;
-  bool fail = false;
-  for (int i = threadIdx.x; i < tile; i += kRowThreads) {
-    uint64_t v = ld_relaxed_u64(&d.tile_state[i]);
-    if (!(v >> 63)) {
-      // bounded wait for a started predecessor to publish (about a second
-      // of wall time at most), polling with a back-off: thousands of
-      // threads polling L2 flat out would slow the very tiles they wait for
-      const uint64_t t0 = global_timer_ns();
-      while (!((v = ld_relaxed_u64(&d.tile_state[i])) >> 63)) {
-        __nanosleep(200);
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-          fail = true;
-          break;
-        }
-      }
-    }
-    pc += (int)(v & 0x7fffffffu);
-    pw += (int)((v >> 31) & 0x7fffffffu);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    pc += __shfl_xor_sync(0xffffffffu, pc, o);
-    pw += __shfl_xor_sync(0xffffffffu, pw, o);
-  }
-  __syncthreads();  // s_red[0..1] is reused below
-  if (lane == 0) {
-    s_red[0][warp] = pc;
-    s_red[1][warp] = pw;
-  }
-  if (fail) s_fail = 1;
-  __syncthreads();
-  if (s_fail) {
-    // a predecessor never published: the plan is incomplete; the attention
-    // kernel sees the status bit and does no work
-    if (threadIdx.x == 0) atomicOr(d.status, (unsigned)MSA_STATUS_TIMEOUT);
-    return;
-  }
-  int base_c = 0, base_w = 0;
-#pragma unroll
-  for (int i = 0; i < kRowThreads / 32; ++i) {
-    base_c += s_red[0][i];
-    base_w += s_red[1][i];
-  }
+  const int tile_w = (int)(uint32_t)all;
   if (tile == (int)gridDim.x - 1 && threadIdx.x == 0) {
-    // the last tile closes the CSR and publishes the totals
-    const int all_c = base_c + s_red[2][0], all_w = base_w + s_red[2][1];
+    const int all_c = base_c + (int)(all >> 32), all_w = base_w + tile_w;
     d.counters[0] = all_c;
     d.counters[1] = all_w;
     d.row_ptr[d.rows] = all_c;
   }
-
-  // ---- pass 2: row_ptr, first work items, the work items of each round
-  for (int rd = 0; rd < rounds; ++rd) {
-    const int64_t r0 = tile_r0 + rd * kRowTile;
-    const int* cnt = s_cnt + rd * kRowTile;
-    if (warp == 0) {
-      const int64_t r = r0 + lane;
-      const int c = lane < kRowTile ? cnt[lane] : 0;
-      const int ch = (c + d.C - 1) / d.C;
-      int exc, exw, rc, rw;
-      scan16(c, ch, &exc, &exw, &rc, &rw);
-      if (lane < kRowTile) {
-        s_exc[lane] = exc;
-        s_exw[lane] = exw;
-        if (r < d.rows) {
-          d.row_ptr[r] = base_c + exc;
-          d.row_wptr[r] = base_w + exw;
-        }
-      }
-    }
-    __syncthreads();
-    const int rw = s_exw[kRowTile - 1] + (cnt[kRowTile - 1] + d.C - 1) / d.C;
-    for (int q = threadIdx.x; q < rw; q += kRowThreads) {
-      const int j = upper_index(s_exw, kRowTile, q);  // last row starting at or before q
-      const int ch = q - s_exw[j];
-      const int n = min(d.C, cnt[j] - ch * d.C);
-      const int64_t wi = (int64_t)base_w + q;
-      const int2 item = s_item[rd * kRowTile + j];
-      reinterpret_cast<int4*>(d.work)[wi] =
-          make_int4(base_c + s_exc[j] + ch * d.C, n, item.x, item.y);
-      int4 hdr = s_hdr[rd * kRowTile + j];
-      hdr.y = n;
-      d.records[wi * d.rec_stride] = hdr;
-    }
-    base_c += s_exc[kRowTile - 1] + cnt[kRowTile - 1];
-    base_w += rw;
-    __syncthreads();  // s_exc / s_exw are rewritten next round
+  __syncthreads();
+  for (int q = threadIdx.x; q < tile_w; q += kRowThreads) {
+    const int j = upper_index(s_exw, d.tile_rows, q);  // last row starting at or before q
+    const int ch = q - s_exw[j];
+    const int n = min(d.C, s_cnt[j] - ch * d.C);
+    const int64_t wi = (int64_t)base_w + q;
+    const int2 item = s_item[j];
+    reinterpret_cast<int4*>(d.work)[wi] =
+        make_int4(base_c + s_exc[j] + ch * d.C, n, item.x, item.y);
+    int4 hdr = s_hdr[j];
+    hdr.y = n;
+    d.records[wi * d.rec_stride] = hdr;
   }
 }
 
@@ -568,7 +545,8 @@ cudaError_t launch_plan(const msa_plan_t& pl, const int32_t* topk,
   d.row_cnt = pl.row_cnt;
   d.row_wptr = pl.row_wptr;
   d.tile_state = pl.tile_state;
-  d.tile_rows = (int)plan_tile_rows(pl.rows);
+  d.lane_shift = plan_row_lane_shift(pl.bitmap_words);
+  d.tile_rows = (int)plan_tile_rows(pl.rows, pl.bitmap_words);
   d.ntiles = (int)ceil_div(pl.rows, d.tile_rows);
   d.row_ptr = pl.row_ptr;
   d.q_idx = pl.q_idx;
@@ -593,6 +571,8 @@ cudaError_t launch_plan(const msa_plan_t& pl, const int32_t* topk,
     e = launch_pdl(plan_mark_kernel, mgrid, 256, 0, stream, d);
   if (e == cudaSuccess && d.ntiles > 0)
     e = launch_pdl(plan_rows_kernel, (unsigned)d.ntiles, kRowThreads, 0, stream, d);
+  if (e == cudaSuccess && d.ntiles > 0)
+    e = launch_pdl(plan_emit_kernel, (unsigned)d.ntiles, kRowThreads, 0, stream, d);
   if (e == cudaSuccess && marks > 0)
     e = launch_pdl(plan_scatter_kernel, mgrid, 256, 0, stream, d);
   return e;

@@ -173,3 +173,40 @@ def test_plan_odd_row_counts(hq, q_lens, seq_lens):
     w = workloads.make_batch("odd", q_lens, seq_lens, hq, 1, seed=9)
     assert (w.Hkv * w.total_rows) % 2 == 1
     compare_plan(w)
+
+
+@pytest.mark.parametrize("q_lens,seq_lens", [
+    ([100, 7], [900, 7]),            # 4 words a row: one lane per row
+    ([200, 30], [1500, 300]),        # 8 words: two lanes
+    ([300, 5], [2600, 500]),         # 12 words: four lanes, one idle
+    ([600, 64], [3000, 640]),        # 20 words: eight lanes, three idle
+    ([1500, 9], [6000, 900]),        # 48 words: sixteen lanes, four idle
+    ([2100, 33], [7000, 3000]),      # 68 words: two vectors a lane, ragged
+])
+@pytest.mark.parametrize("spare", [0, 300])
+def test_plan_row_widths(q_lens, seq_lens, spare):
+    # the rows kernel gives a row 1 to 16 lanes by its width (the longest
+    # query chunk sets the words per row); odd row counts end a tile inside
+    # a round, and spare rows past the pages make several tiles
+    w = workloads.make_batch("width", q_lens, seq_lens, 8, 1, seed=len(q_lens) + q_lens[0])
+    assert (w.Hkv * (w.total_rows + spare)) % 2 == 1
+    compare_plan(w, total_rows=w.total_rows + spare)
+
+
+@pytest.mark.parametrize("q_len,seq_len,rows", [
+    (2048, 300000, 12000),   # 64 words a row, tiles of 6 rounds of 16 rows
+    (4096, 40000, 9000),     # 128 words, two vectors a lane, 5 rounds
+])
+def test_plan_tiles_of_many_rounds(q_len, seq_len, rows):
+    # spare rows past the last request's pages make the tiles several rounds
+    # deep, more than one group of rounds whose loads go out together
+    w = workloads.make_batch("deep", [q_len], [seq_len], 16, 2, seed=q_len)
+    compare_plan(w, total_rows=rows)
+
+
+def test_plan_more_tiles_than_the_tile_target():
+    # 2 x 70,000 rows of one lane: more rows than 256 tiles of 512 rows hold,
+    # so the tile count grows past 256
+    sl = workloads.decode_lengths(3, 16, 4096, 20000)
+    w = workloads.make_batch("dec", [8] * 16, sl, 16, 2, seed=11)
+    compare_plan(w, total_rows=70000)
