@@ -53,8 +53,8 @@ METRIC = "selected-token attention TFLOP/s"
 # the HBM figure the per-layer target is stated against
 NOMINAL_HBM_GBS = 8000.0
 L2_FLUSH_BYTES = 256 << 20
-KERNELS_PER_STEP = 7  # plan: prep, mark, rows, emit, scatter; attention; combine
-DECODE_KERNELS_PER_STEP = 8  # msa_decode: seq-lens prefix sums, then the same 7
+KERNELS_PER_STEP = 6  # plan: prep, mark, rows, scatter; attention; combine
+DECODE_KERNELS_PER_STEP = 7  # msa_decode: seq-lens prefix sums, then the same 6
 # one (page, KV head) of an NVFP4 pool: K and V slots of 128 x 64 code
 # bytes and 128 x 8 E4M3 block scales
 NVFP4_PAGE_HEAD_BYTES = 2 * (128 * 64 + 128 * 8)

@@ -42,7 +42,7 @@ _I64 = ("B", "T", "Hq", "Hkv", "total_rows", "max_seqlen_q", "max_seqlen_k",
         "num_pages", "bt_stride", "bitmap_words", "chunk_tokens", "max_nnz",
         "max_work", "rows", "record_bytes")
 _PTR = ("cu_seqlens_q", "cu_seqlens_k", "req_off", "bitmap", "word_pre",
-        "row_cnt", "row_wptr", "tile_state", "row_ptr", "q_idx", "slot", "work",
+        "row_cnt", "row_loc", "tile_state", "row_ptr", "q_idx", "slot", "work",
         "records", "counters", "slot_mask", "status")
 
 

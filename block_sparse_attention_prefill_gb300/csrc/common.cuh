@@ -18,13 +18,12 @@ constexpr int kTileM = 128;           // MMA rows per work item (tokens x G)
 
 // The plan's rows kernel: its threads, the lanes that share one row (the
 // row's 16-byte vectors rounded up to a power of two, at most 16), and its
-// tiles (CTAs).  A round is kRowThreads / lanes rows; a tile is a whole
-// number of rounds, at most kMaxTileRows rows, and as few as keep the tile
-// count within kMaxRowTiles (above kMaxRowTiles * kMaxTileRows rows the
-// tile count grows instead): every tile adds up the totals of all tiles in
-// front of it, so few tiles keep those reads few.
+// tiles (CTAs).  A round is kRowThreads / lanes rows; a tile is the fewest
+// whole rounds that keep the tile count within kMaxRowTiles, so the scatter
+// kernel's CTAs can each scan all tiles' totals (one per thread).  A tile
+// is worked in segments of at most kMaxTileRows rows.
 constexpr int kRowThreads = 256;
-constexpr int kMaxRowTiles = 256;
+constexpr int kMaxRowTiles = kRowThreads;
 constexpr int kMaxTileRows = 512;  // a multiple of every round (16 .. 256 rows)
 __host__ __device__ inline int plan_row_lane_shift(int64_t W) {
   const int64_t nv = W / 4;  // 16-byte vectors per row
@@ -36,9 +35,7 @@ __host__ __device__ inline int64_t plan_tile_rows(int64_t rows, int64_t W) {
   const int64_t rp = kRowThreads >> plan_row_lane_shift(W);  // rows per round
   int64_t tr = (rows + kMaxRowTiles - 1) / kMaxRowTiles;
   tr = (tr + rp - 1) / rp * rp;
-  if (tr < rp) tr = rp;
-  if (tr > kMaxTileRows) tr = kMaxTileRows;
-  return tr;
+  return tr < rp ? rp : tr;
 }
 
 // Wall-time bound of every device-side wait (about a second).

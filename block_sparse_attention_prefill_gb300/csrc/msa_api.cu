@@ -98,7 +98,7 @@ size_t plan_layout(const PlanShape& s, void* base, msa_plan_t* pl) {
   uint32_t* bitmap = c.take<uint32_t>(s.rows * s.W);
   int32_t* word_pre = c.take<int32_t>(s.rows * s.W);
   int32_t* row_cnt = c.take<int32_t>(s.rows);
-  int32_t* row_wptr = c.take<int32_t>(s.rows);
+  int32_t* row_loc = c.take<int32_t>(2 * s.rows);
   uint64_t* tile_state = c.take<uint64_t>(s.ntiles);
   int32_t* row_ptr = c.take<int32_t>(s.rows + 1);
   int32_t* q_idx = c.take<int32_t>(s.max_nnz);
@@ -113,7 +113,7 @@ size_t plan_layout(const PlanShape& s, void* base, msa_plan_t* pl) {
     pl->bitmap = bitmap;
     pl->word_pre = word_pre;
     pl->row_cnt = row_cnt;
-    pl->row_wptr = row_wptr;
+    pl->row_loc = row_loc;
     pl->tile_state = tile_state;
     pl->records = records;
     pl->record_bytes = record_bytes(s);

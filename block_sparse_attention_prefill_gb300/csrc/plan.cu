@@ -5,7 +5,7 @@
 // total_kv_blocks, qhead_per_kv, return_schedule=True); vLLM PR 60930,
 // Details / "Host sync": the plan stays on the device, no host copy.)
 //
-// Five kernels, all on `stream`, no host synchronisation; every kernel
+// Four kernels, all on `stream`, no host synchronisation; every kernel
 // after the first is a programmatic dependent launch (its launch overlaps
 // the tail of the kernel before it, its work does not):
 //   prep     CTA 0: per-request row offsets (sum of page counts), checks,
@@ -16,21 +16,19 @@
 //            KV head) list's 16 threads together write its slot mask.  This
 //            is the histogram, kept as bits: repeats collapse and the order
 //            of arrival cannot change the result.
-//   rows     one CTA per tile of rows (at most kMaxRowTiles tiles while a
-//            tile stays within kMaxTileRows rows), 1 to 16 lanes per row by
-//            the row's width: the row's length (popcount of its words), the
-//            running count in front of every word, and the tile's totals
-//            (entries, work items).
-//   emit     one CTA per tile: the sum of the totals of the tiles before it
-//            (the exclusive scan across tiles: at most kMaxRowTiles loads,
-//            all issued at once), a scan over its own rows, then row_ptr,
-//            each row's first work item, and the tile's work items and
-//            record headers.  A tile waits for no other tile: the kernel
-//            boundary orders them.
-//   scatter  one thread per top-k entry: each kept entry goes to
-//            row_ptr + (tokens of the same row before it), found in O(1)
-//            from the word prefix and a popcount; it also fills the token
-//            slot of the work record the attention kernel will read.
+//   rows     one CTA per tile of rows (at most kMaxRowTiles tiles), 1 to 16
+//            lanes per row by the row's width: the row's length (popcount of
+//            its words), the running count in front of every word, each
+//            row's entries and work items in front of it within the tile,
+//            and the tile's totals.
+//   scatter  every CTA first scans the tiles' totals in shared memory (the
+//            exclusive scan across tiles: one load per thread, no waiting
+//            on other CTAs) and writes its share of row_ptr; then one thread
+//            per top-k entry: each kept entry goes to row_ptr + (tokens of
+//            the same row before it), found in O(1) from the word prefix and
+//            a popcount, and fills its token slot of the work record the
+//            attention kernel will read; the first entry of each chunk also
+//            writes the chunk's work item and record header.
 // Every output is a function of the inputs alone: bit-exact and
 // deterministic run to run.
 #include <algorithm>
@@ -97,7 +95,7 @@ struct PlanDev {
   uint32_t* bitmap;
   int32_t* word_pre;     // [rows * W] tokens of the row before each word
   int32_t* row_cnt;      // [rows] entries of the row
-  int32_t* row_wptr;     // [rows] first work item of the row
+  int32_t* row_loc;      // [rows][2] entries, work items before the row in its tile
   uint64_t* tile_state;  // [ntiles] tile totals: entries << 32 | work items
   int ntiles, tile_rows, lane_shift;  // rows kernel tiling (see rows)
   int32_t* row_ptr;
@@ -154,10 +152,7 @@ __global__ void __launch_bounds__(kScanThreads) plan_prep_kernel(PlanDev d,
     if (s_bad) st |= MSA_STATUS_BAD_SEQLENS;
     if (!s_bad && overflow) st |= MSA_STATUS_ROWS_OVERFLOW;
     *d.status = st;
-    d.counters[0] = 0;
-    d.counters[1] = 0;
-    d.counters[2] = st ? 0 : 1;
-    d.row_ptr[d.rows] = 0;  // the emit kernel's last tile writes the total
+    d.counters[2] = st ? 0 : 1;  // the scatter kernel writes [0] and [1]
   }
 }
 
@@ -293,12 +288,13 @@ __device__ __forceinline__ uint64_t block_incl_scan64(uint64_t v, uint64_t* s_wa
   return before + v;
 }
 
-// One CTA per tile of d.tile_rows rows (a whole number of rounds; the host
-// keeps the tile count within kMaxRowTiles while a tile stays within
-// kMaxTileRows rows).  L = 2^d.lane_shift lanes share a row, kRowThreads / L
-// rows per round.  Writes each row's length (row_cnt), the running count in
-// front of every word (word_pre), and the tile's totals (entries, work
-// items) for the emit kernel.
+// One CTA per tile of d.tile_rows rows (a whole number of rounds, at least
+// rows / kMaxRowTiles: at most kMaxRowTiles tiles), worked in segments of at
+// most kMaxTileRows rows.  L = 2^d.lane_shift lanes share a row,
+// kRowThreads / L rows per round.  Writes each row's length (row_cnt), the
+// running count in front of every word (word_pre), the entries and work
+// items in front of each row within its tile (row_loc), and the tile's
+// totals (tile_state) for the scatter kernel.
 __global__ void __launch_bounds__(kRowThreads) plan_rows_kernel(PlanDev d) {
   pdl_wait();
   pdl_trigger();
@@ -308,214 +304,177 @@ __global__ void __launch_bounds__(kRowThreads) plan_rows_kernel(PlanDev d) {
   const int L = 1 << d.lane_shift;
   const int sub = threadIdx.x & (L - 1), k = threadIdx.x >> d.lane_shift;
   const int rp = kRowThreads >> d.lane_shift;  // rows per round
-  const int rounds = d.tile_rows / rp;
   const int nv = d.W >> 2;
   const int per = (nv + L - 1) >> d.lane_shift;
   const int64_t r0 = (int64_t)tile * d.tile_rows;
   const bool ok = d.counters[2] == 1;
 
-  for (int rd0 = 0; rd0 < rounds; rd0 += kPass1Rounds) {
-    uint4 v[kPass1Rounds];
+  uint64_t carry = 0;  // entries and work items of the segments before
+  for (int s0 = 0; s0 < d.tile_rows; s0 += kMaxTileRows) {
+    const int seg = min(kMaxTileRows, d.tile_rows - s0);  // a multiple of rp
+    const int rounds = seg / rp;
+    const int64_t rs = r0 + s0;
+    for (int rd0 = 0; rd0 < rounds; rd0 += kPass1Rounds) {
+      uint4 v[kPass1Rounds];
 #pragma unroll
-    for (int u = 0; u < kPass1Rounds; ++u) {
-      const int64_t r = r0 + (int64_t)(rd0 + u) * rp + k;
-      v[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (per == 1 && ok && rd0 + u < rounds && r < d.rows && sub < nv)
-        v[u] = reinterpret_cast<const uint4*>(d.bitmap + r * d.W)[sub];
-    }
-#pragma unroll
-    for (int u = 0; u < kPass1Rounds; ++u) {
-      const int rd = rd0 + u;
-      if (rd >= rounds) break;  // the same for the whole CTA
-      const int64_t r = r0 + (int64_t)rd * rp + k;
-      const bool live = ok && r < d.rows;
-      const uint4* __restrict__ words = reinterpret_cast<const uint4*>(d.bitmap + r * d.W);
-      int own = 0;
-      if (per == 1) {
-        own = __popc(v[u].x) + __popc(v[u].y) + __popc(v[u].z) + __popc(v[u].w);
-      } else if (live) {
-        for (int u0 = 0; u0 < per; u0 += 4) {
-          uint4 w4[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int x = sub * per + u0 + i;
-            w4[i] = (u0 + i < per && x < nv) ? words[x] : make_uint4(0u, 0u, 0u, 0u);
-          }
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            own += __popc(w4[i].x) + __popc(w4[i].y) + __popc(w4[i].z) + __popc(w4[i].w);
-        }
+      for (int u = 0; u < kPass1Rounds; ++u) {
+        const int64_t r = rs + (int64_t)(rd0 + u) * rp + k;
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (per == 1 && ok && rd0 + u < rounds && r < d.rows && sub < nv)
+          v[u] = reinterpret_cast<const uint4*>(d.bitmap + r * d.W)[sub];
       }
-      int incl = own;
-      for (int o = 1; o < L; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o, L);
-        if (sub >= o) incl += n;
-      }
-      // every lane takes part in the shuffle (a row past the end has 0)
-      const int total = __shfl_sync(0xffffffffu, incl, L - 1, L);
-      if (sub == 0) s_cnt[rd * rp + k] = total;
-      if (live) {
-        int4* __restrict__ pre = reinterpret_cast<int4*>(d.word_pre + r * d.W);
-        int run = incl - own;
-        for (int i = 0; i < per; ++i) {
-          const int x = sub * per + i;
-          if (x < nv) {
-            const uint4 w1 = per == 1 ? v[u] : words[x];
-            int4 o;
-            o.x = run; run += __popc(w1.x);
-            o.y = run; run += __popc(w1.y);
-            o.z = run; run += __popc(w1.z);
-            o.w = run; run += __popc(w1.w);
-            pre[x] = o;
+#pragma unroll
+      for (int u = 0; u < kPass1Rounds; ++u) {
+        const int rd = rd0 + u;
+        if (rd >= rounds) break;  // the same for the whole CTA
+        const int64_t r = rs + (int64_t)rd * rp + k;
+        const bool live = ok && r < d.rows;
+        const uint4* __restrict__ words = reinterpret_cast<const uint4*>(d.bitmap + r * d.W);
+        int own = 0;
+        if (per == 1) {
+          own = __popc(v[u].x) + __popc(v[u].y) + __popc(v[u].z) + __popc(v[u].w);
+        } else if (live) {
+          for (int u0 = 0; u0 < per; u0 += 4) {
+            uint4 w4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int x = sub * per + u0 + i;
+              w4[i] = (u0 + i < per && x < nv) ? words[x] : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              own += __popc(w4[i].x) + __popc(w4[i].y) + __popc(w4[i].z) + __popc(w4[i].w);
           }
         }
+        int incl = own;
+        for (int o = 1; o < L; o <<= 1) {
+          const int n = __shfl_up_sync(0xffffffffu, incl, o, L);
+          if (sub >= o) incl += n;
+        }
+        // every lane takes part in the shuffle (a row past the end has 0)
+        const int total = __shfl_sync(0xffffffffu, incl, L - 1, L);
+        if (sub == 0) s_cnt[rd * rp + k] = total;
+        if (live) {
+          int4* __restrict__ pre = reinterpret_cast<int4*>(d.word_pre + r * d.W);
+          int run = incl - own;
+          for (int i = 0; i < per; ++i) {
+            const int x = sub * per + i;
+            if (x < nv) {
+              const uint4 w1 = per == 1 ? v[u] : words[x];
+              int4 o;
+              o.x = run; run += __popc(w1.x);
+              o.y = run; run += __popc(w1.y);
+              o.z = run; run += __popc(w1.z);
+              o.w = run; run += __popc(w1.w);
+              pre[x] = o;
+            }
+          }
+        }
       }
     }
+    __syncthreads();  // s_cnt is complete
+    // two rows per thread: lengths and offsets within the tile
+    const int i0 = 2 * threadIdx.x;
+    const int c0 = i0 < seg ? s_cnt[i0] : 0;
+    const int c1 = i0 + 1 < seg ? s_cnt[i0 + 1] : 0;
+    const uint64_t p0 = pack_cw(c0, (c0 + d.C - 1) / d.C);
+    const uint64_t p1 = pack_cw(c1, (c1 + d.C - 1) / d.C);
+    uint64_t all;
+    // (the scan's barriers also end every read of s_cnt before the next
+    // segment writes it)
+    uint64_t ex = carry + block_incl_scan64(p0 + p1, s_warp, &all) - (p0 + p1);
+    if (i0 < seg && rs + i0 < d.rows) {
+      d.row_cnt[rs + i0] = c0;
+      reinterpret_cast<int2*>(d.row_loc)[rs + i0] = make_int2((int)(ex >> 32), (int)(uint32_t)ex);
+    }
+    ex += p0;
+    if (i0 + 1 < seg && rs + i0 + 1 < d.rows) {
+      d.row_cnt[rs + i0 + 1] = c1;
+      reinterpret_cast<int2*>(d.row_loc)[rs + i0 + 1] =
+          make_int2((int)(ex >> 32), (int)(uint32_t)ex);
+    }
+    carry += all;
   }
-  __syncthreads();
-  // row lengths out; the tile's totals
-  uint64_t mine = 0;
-  for (int i = threadIdx.x; i < d.tile_rows; i += kRowThreads) {
-    const int c = s_cnt[i];
-    if (r0 + i < d.rows) d.row_cnt[r0 + i] = c;
-    mine += pack_cw(c, (c + d.C - 1) / d.C);
-  }
-  uint64_t all;
-  block_incl_scan64(mine, s_warp, &all);
-  if (threadIdx.x == 0) d.tile_state[tile] = all;
+  if (threadIdx.x == 0) d.tile_state[tile] = carry;
 }
 
-// One CTA per tile of the rows kernel, launched after it: adds up the
-// totals of the tiles before it (all final by now: the exclusive scan
-// across tiles), scans its own rows (two per thread), and writes row_ptr,
-// each row's first work item, and the tile's work items and record headers
-// dealt over all threads.  The last tile closes the CSR and writes the
-// totals.
-__global__ void __launch_bounds__(kRowThreads) plan_emit_kernel(PlanDev d) {
+// One thread per top-k entry (at least one per 2048 rows): each CTA first
+// adds up the row tiles' totals in shared memory (the exclusive scan across
+// tiles, at most kMaxRowTiles of them) and writes its share of row_ptr.  A
+// kept entry's place in its row is the number of tokens of the row before
+// it, read from the word prefix plus a popcount; its CSR slot and work item
+// follow from its tile's base and its row's offsets in the tile.  The first
+// entry of each chunk of a row also writes the chunk's work item and record
+// header.
+__global__ void __launch_bounds__(kRowThreads) plan_scatter_kernel(PlanDev d) {
   pdl_wait();
   pdl_trigger();
-  constexpr int kReqCache = 1024;
-  __shared__ int s_req[kReqCache + 1];   // req_off, when B fits
-  __shared__ int s_cnt[kMaxTileRows];    // entries of each row
-  __shared__ int s_exc[kMaxTileRows];    // first entry in the tile
-  __shared__ int s_exw[kMaxTileRows];    // first work item in the tile
-  __shared__ int4 s_hdr[kMaxTileRows];   // record header without the count
-  __shared__ int2 s_item[kMaxTileRows];  // work item: b, (h << 24) | p
+  __shared__ uint64_t s_base[kMaxRowTiles];  // entries << 32 | work items before each tile
   __shared__ uint64_t s_warp[kRowThreads / 32];
-  const int tile = blockIdx.x;
-  const int64_t r0 = (int64_t)tile * d.tile_rows;
-  const bool cache_req = d.B < kReqCache;
-  // the loads that do not depend on one another go out together
-  uint64_t pred = 0;
-  for (int i = threadIdx.x; i < tile; i += kRowThreads) pred += d.tile_state[i];
-  const int i0 = 2 * threadIdx.x;  // this thread's rows: i0, i0 + 1
-  int cnt[2];
-#pragma unroll
-  for (int e = 0; e < 2; ++e)
-    cnt[e] = (i0 + e < d.tile_rows && r0 + i0 + e < d.rows) ? d.row_cnt[r0 + i0 + e] : 0;
-  if (cache_req)
-    for (int i = threadIdx.x; i <= d.B; i += kRowThreads) s_req[i] = d.req_off[i];
-  __syncthreads();
-  const int32_t* req_off = cache_req ? s_req : d.req_off;
-  int32_t phys[2];
-  int hb[2], hp[2], hh[2];
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int64_t r = r0 + i0 + e;
-    phys[e] = 0;
-    hb[e] = hp[e] = hh[e] = 0;
-    if (i0 + e < d.tile_rows && r < d.rows) {
-      const int h = (int)(r / d.total_rows);
-      const int64_t rq = r - (int64_t)h * d.total_rows;
-      const int b = upper_index(req_off, d.B, rq);
-      const int p = (int)(rq - req_off[b]);
-      phys[e] = d.block_table[(int64_t)b * d.bt_stride + p];
-      hb[e] = b;
-      hp[e] = p;
-      hh[e] = h;
-    }
-  }
-  uint64_t base;
-  block_incl_scan64(pred, s_warp, &base);
-  const int base_c = (int)(base >> 32), base_w = (int)(uint32_t)base;
-  const int w0 = (cnt[0] + d.C - 1) / d.C, w1 = (cnt[1] + d.C - 1) / d.C;
-  uint64_t all;
-  const uint64_t incl = block_incl_scan64(pack_cw(cnt[0] + cnt[1], w0 + w1), s_warp, &all);
-  int ex_c = (int)(incl >> 32) - (cnt[0] + cnt[1]);
-  int ex_w = (int)(uint32_t)incl - (w0 + w1);
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int i = i0 + e;
-    const int64_t r = r0 + i;
-    if (i < d.tile_rows) {
-      s_cnt[i] = cnt[e];
-      s_exc[i] = ex_c;
-      s_exw[i] = ex_w;
-      if (cnt[e] > 0) {
-        // record header: KV tile row of the pool, (token count), first key
-        // position of the page, first query head of the KV head
-        s_hdr[i] = make_int4((phys[e] * d.Hkv + hh[e]) * kPage, 0, hp[e] * kPage,
-                             hh[e] * d.G);
-        s_item[i] = make_int2(hb[e], (hh[e] << 24) | hp[e]);
-      }
-      if (r < d.rows) {
-        d.row_ptr[r] = base_c + ex_c;
-        d.row_wptr[r] = base_w + ex_w;
-      }
-    }
-    ex_c += cnt[e];
-    ex_w += e == 0 ? w0 : w1;
-  }
-  const int tile_w = (int)(uint32_t)all;
-  if (tile == (int)gridDim.x - 1 && threadIdx.x == 0) {
-    const int all_c = base_c + (int)(all >> 32), all_w = base_w + tile_w;
-    d.counters[0] = all_c;
-    d.counters[1] = all_w;
-    d.row_ptr[d.rows] = all_c;
-  }
-  __syncthreads();
-  for (int q = threadIdx.x; q < tile_w; q += kRowThreads) {
-    const int j = upper_index(s_exw, d.tile_rows, q);  // last row starting at or before q
-    const int ch = q - s_exw[j];
-    const int n = min(d.C, s_cnt[j] - ch * d.C);
-    const int64_t wi = (int64_t)base_w + q;
-    const int2 item = s_item[j];
-    reinterpret_cast<int4*>(d.work)[wi] =
-        make_int4(base_c + s_exc[j] + ch * d.C, n, item.x, item.y);
-    int4 hdr = s_hdr[j];
-    hdr.y = n;
-    d.records[wi * d.rec_stride] = hdr;
-  }
-}
-
-// One thread per kept top-k entry: its place in the row is the number of
-// tokens of the row before it, read from the word prefix plus a popcount.
-__global__ void __launch_bounds__(256) plan_scatter_kernel(PlanDev d) {
-  pdl_wait();
-  pdl_trigger();
+  __shared__ int32_t s_cuq[kMetaCache + 1], s_cuk[kMetaCache + 1], s_off[kMetaCache + 1];
   const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const bool live = e < (int64_t)d.T * d.Hkv * kTopK;
   const int64_t w = e / kTopK;
   const int j = (int)(e % kTopK);
-  // the entry's loads go out together with the metadata's
+  // the entry's loads go out together with the metadata's and the tiles'
   const int32_t p = live ? d.topk[e] : -1;
   const uint32_t mask = live ? d.slot_mask[w] : 0u;
   const int valid_plan = d.counters[2];
-  __shared__ int32_t s_cuq[kMetaCache + 1], s_cuk[kMetaCache + 1], s_off[kMetaCache + 1];
+  const uint64_t tv = (int)threadIdx.x < d.ntiles ? d.tile_state[threadIdx.x] : 0ull;
+  // this thread's rows of row_ptr: r0, r0 + grid threads, ... (rows < 2^31:
+  // 32-bit indices); the first one's offset is loaded here too
+  const int r0 = blockIdx.x * blockDim.x + threadIdx.x;
+  const int loc0 = r0 < (int)d.rows ? d.row_loc[2 * (int64_t)r0] : 0;
   const ReqMeta m = stage_req_meta(d, s_cuq, s_cuk, s_off);
-  if (!live || valid_plan != 1 || !((mask >> j) & 1u)) return;
+  // a kept entry's second loads go out before the tiles' scan
+  const bool kept = live && valid_plan == 1 && ((mask >> j) & 1u);
   const int t = (int)(w / d.Hkv);
   const int h = (int)(w % d.Hkv);
-  const TokenInfo k = token_info(d, m, t, h);
-  const int64_t r = k.row0 + p;
-  const int64_t wi = r * d.W + (k.i >> 5);
+  TokenInfo k = {};
+  int32_t phys = 0;
+  int64_t r = 0, wi = 0;
+  int2 loc = make_int2(0, 0);
+  int cnt = 0, pre = 0;
+  uint32_t word = 0;
+  if (kept) {
+    k = token_info(d, m, t, h);
+    phys = d.block_table[(int64_t)k.b * d.bt_stride + p];  // checked by mark
+    r = k.row0 + p;
+    wi = r * d.W + (k.i >> 5);
+    loc = reinterpret_cast<const int2*>(d.row_loc)[r];
+    cnt = d.row_cnt[r];
+    pre = d.word_pre[wi];
+    word = d.bitmap[wi];
+  }
+  uint64_t all;
+  const uint64_t tin = block_incl_scan64(tv, s_warp, &all);
+  if ((int)threadIdx.x < d.ntiles) s_base[threadIdx.x] = tin - tv;
+  __syncthreads();
+  if (r0 < (int)d.rows) d.row_ptr[r0] = (int)(s_base[r0 / d.tile_rows] >> 32) + loc0;
+  for (int rr = r0 + gridDim.x * blockDim.x; rr < (int)d.rows; rr += gridDim.x * blockDim.x)
+    d.row_ptr[rr] = (int)(s_base[rr / d.tile_rows] >> 32) + d.row_loc[2 * (int64_t)rr];
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    // the totals, and the CSR's closing entry
+    d.counters[0] = (int)(all >> 32);
+    d.counters[1] = (int)(uint32_t)all;
+    d.row_ptr[d.rows] = (int)(all >> 32);
+  }
+  if (!kept) return;
   const uint32_t below = (1u << (k.i & 31)) - 1u;
-  const int rank = d.word_pre[wi] + __popc(d.bitmap[wi] & below);
-  const int at = d.row_ptr[r] + rank;
-  const int64_t rec = d.row_wptr[r] + rank / d.C;
+  const int rank = pre + __popc(word & below);
+  const uint64_t base = s_base[(int)r / d.tile_rows];
+  const int at = (int)(base >> 32) + loc.x + rank;
+  const int64_t rec = (int64_t)(uint32_t)base + loc.y + rank / d.C;
   d.q_idx[at] = t;
   d.slot[at] = (uint8_t)j;
   d.records[rec * d.rec_stride + 1 + rank % d.C] = make_int4(t, k.pos, j, 0);
+  if (rank % d.C == 0) {
+    const int n = min(d.C, cnt - rank);
+    reinterpret_cast<int4*>(d.work)[rec] = make_int4(at, n, k.b, (h << 24) | p);
+    // record header: KV tile row of the pool, token count, first key
+    // position of the page, first query head of the KV head
+    d.records[rec * d.rec_stride] = make_int4((phys * d.Hkv + h) * kPage, n, p * kPage, h * d.G);
+  }
 }
 
 }  // namespace
@@ -543,7 +502,7 @@ cudaError_t launch_plan(const msa_plan_t& pl, const int32_t* topk,
   d.bitmap = pl.bitmap;
   d.word_pre = pl.word_pre;
   d.row_cnt = pl.row_cnt;
-  d.row_wptr = pl.row_wptr;
+  d.row_loc = pl.row_loc;
   d.tile_state = pl.tile_state;
   d.lane_shift = plan_row_lane_shift(pl.bitmap_words);
   d.tile_rows = (int)plan_tile_rows(pl.rows, pl.bitmap_words);
@@ -571,10 +530,11 @@ cudaError_t launch_plan(const msa_plan_t& pl, const int32_t* topk,
     e = launch_pdl(plan_mark_kernel, mgrid, 256, 0, stream, d);
   if (e == cudaSuccess && d.ntiles > 0)
     e = launch_pdl(plan_rows_kernel, (unsigned)d.ntiles, kRowThreads, 0, stream, d);
-  if (e == cudaSuccess && d.ntiles > 0)
-    e = launch_pdl(plan_emit_kernel, (unsigned)d.ntiles, kRowThreads, 0, stream, d);
-  if (e == cudaSuccess && marks > 0)
-    e = launch_pdl(plan_scatter_kernel, mgrid, 256, 0, stream, d);
+  // the scatter kernel also writes row_ptr: at most 2048 rows per CTA
+  const unsigned sgrid = (unsigned)std::max<int64_t>(
+      std::max<int64_t>(mgrid, ceil_div(pl.rows, 2048)), 1);
+  if (e == cudaSuccess)
+    e = launch_pdl(plan_scatter_kernel, sgrid, kRowThreads, 0, stream, d);
   return e;
 }
 

@@ -140,7 +140,8 @@ typedef struct msa_plan {
   uint32_t *bitmap;            /* [rows * bitmap_words] token membership    */
   int32_t *word_pre;           /* [rows * bitmap_words] tokens before word  */
   int32_t *row_cnt;            /* [rows] entries of the row                 */
-  int32_t *row_wptr;           /* [rows] first work item of the row         */
+  int32_t *row_loc;            /* [rows][2] entries, work items before the
+                                  row within its row tile                   */
   uint64_t *tile_state;        /* [row tiles] tile totals                   */
   int32_t *row_ptr;            /* [rows + 1]                                */
   int32_t *q_idx;              /* [max_nnz] global query token ids          */
@@ -193,7 +194,7 @@ MSA_API int msa_plan_workspace_bytes(int64_t B, int64_t T, int64_t Hq, int64_t H
  *   workspace     device buffer of msa_plan_workspace_bytes() bytes,
  *                 256-byte aligned; it holds the plan until it is rebuilt.
  *   plan          host struct, filled on return.
- * Launches 5 kernels on `stream`; never synchronises.
+ * Launches 4 kernels on `stream`; never synchronises.
  */
 MSA_API int msa_plan(const int32_t *topk, const int32_t *cu_seqlens_q,
              const int32_t *cu_seqlens_k, const int32_t *block_table,

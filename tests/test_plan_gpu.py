@@ -196,6 +196,7 @@ def test_plan_row_widths(q_lens, seq_lens, spare):
 @pytest.mark.parametrize("q_len,seq_len,rows", [
     (2048, 300000, 12000),   # 64 words a row, tiles of 6 rounds of 16 rows
     (4096, 40000, 9000),     # 128 words, two vectors a lane, 5 rounds
+    (2048, 300000, 70000),   # 560-row tiles: a 512-row segment, then 48 rows
 ])
 def test_plan_tiles_of_many_rounds(q_len, seq_len, rows):
     # spare rows past the last request's pages make the tiles several rounds
@@ -204,9 +205,9 @@ def test_plan_tiles_of_many_rounds(q_len, seq_len, rows):
     compare_plan(w, total_rows=rows)
 
 
-def test_plan_more_tiles_than_the_tile_target():
-    # 2 x 70,000 rows of one lane: more rows than 256 tiles of 512 rows hold,
-    # so the tile count grows past 256
+def test_plan_tiles_of_several_segments():
+    # 2 x 70,000 rows of one lane: 256 tiles of 768 rows, each worked as a
+    # 512-row segment and a 256-row one
     sl = workloads.decode_lengths(3, 16, 4096, 20000)
     w = workloads.make_batch("dec", [8] * 16, sl, 16, 2, seed=11)
     compare_plan(w, total_rows=70000)
