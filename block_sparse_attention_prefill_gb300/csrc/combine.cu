@@ -204,6 +204,8 @@ combine16_kernel(const uint8_t* __restrict__ part_o,
 __global__ void __launch_bounds__(1024)
 decode_seqlens_kernel(const int32_t* seq_lens, int64_t B, int64_t n,
                       int32_t* cu_q, int32_t* cu_k) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int warp_sums[33];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int carry = 0;
@@ -278,8 +280,8 @@ cudaError_t launch_combine_attn(const uint8_t* part_o, const uint8_t* part_big,
 cudaError_t launch_decode_seqlens(const int32_t* seq_lens, int64_t B,
                                   int64_t n, int32_t* cu_q, int32_t* cu_k,
                                   cudaStream_t stream) {
-  decode_seqlens_kernel<<<1, 1024, 0, stream>>>(seq_lens, B, n, cu_q, cu_k);
-  return cudaGetLastError();
+  return launch_pdl(decode_seqlens_kernel, dim3(1), dim3(1024), 0, stream, seq_lens, B, n,
+                    cu_q, cu_k);
 }
 
 }  // namespace msa

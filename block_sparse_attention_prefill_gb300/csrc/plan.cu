@@ -5,9 +5,9 @@
 // total_kv_blocks, qhead_per_kv, return_schedule=True); vLLM PR 60930,
 // Details / "Host sync": the plan stays on the device, no host copy.)
 //
-// Four kernels, all on `stream`, no host synchronisation; every kernel
-// after the first is a programmatic dependent launch (its launch overlaps
-// the tail of the kernel before it, its work does not):
+// Four kernels, all on `stream`, no host synchronisation; each is a
+// programmatic dependent launch (its launch overlaps the tail of the kernel
+// before it on the stream, its work does not):
 //   prep     CTA 0: per-request row offsets (sum of page counts), checks,
 //            status word, counters; every CTA: clears its share of the
 //            (row, token) membership bitmap
@@ -112,6 +112,10 @@ struct PlanDev {
 // counters[2] == 1 when the per-request metadata passed the checks.
 __global__ void __launch_bounds__(kScanThreads) plan_prep_kernel(PlanDev d,
                                                                  int64_t bitmap_vec) {
+  // launched as a dependent of whatever kernel ran before it on the stream
+  // (the top-k ids may be its output): the launch overlaps that kernel's
+  // tail, the work waits for it
+  pdl_wait();
   pdl_trigger();
   {
     uint4* bm = reinterpret_cast<uint4*>(d.bitmap);
@@ -523,9 +527,8 @@ cudaError_t launch_plan(const msa_plan_t& pl, const int32_t* topk,
                                           2 * (int64_t)num_sms());
   const int64_t marks = (int64_t)pl.T * pl.Hkv * kTopK;
   const unsigned mgrid = (unsigned)ceil_div(marks, 256);
-  plan_prep_kernel<<<(unsigned)std::max<int64_t>(zgrid, 1), kScanThreads, 0, stream>>>(
-      d, bitmap_vec);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(plan_prep_kernel, (unsigned)std::max<int64_t>(zgrid, 1),
+                             kScanThreads, 0, stream, d, bitmap_vec);
   if (e == cudaSuccess && marks > 0)
     e = launch_pdl(plan_mark_kernel, mgrid, 256, 0, stream, d);
   if (e == cudaSuccess && d.ntiles > 0)

@@ -114,6 +114,28 @@ def test_repeatable_and_stream_ordered():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("name", ["chunked_prefill_32k", "long_prefill_1m"])
+def test_one_plan_serves_repeated_launches(name):
+    # one plan, several prefill launches on one workspace: each (token,
+    # head, slot) partial has exactly one writer, so the results are
+    # bit-identical launch after launch
+    w = workloads.make_config(name, seed=3).to("cuda")
+    plan = msa.msa_plan(w.topk, w.cu_q, w.cu_k, w.block_table, w.num_pages,
+                        w.Hq, w.total_rows, w.max_seqlen_q, w.max_seqlen_k)
+    ws = torch.empty(msa.prefill_workspace_bytes(w.T, w.Hq),
+                     dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(4):
+        out, lse = msa.msa_prefill(w.q, w.kv, w.q_scale, w.k_scale, w.v_scale,
+                                   w.softmax_scale, w.block_table, plan,
+                                   workspace=ws)
+        outs.append((out.clone(), lse.clone()))
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+
+
 @pytest.mark.parametrize("seed", [0, 1])
 def test_mixed_decode_and_prefill_batch(seed):
     # decode / speculative-verify requests (1 to 8 tokens at the tail of a
