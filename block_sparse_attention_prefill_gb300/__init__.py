@@ -79,6 +79,8 @@ def load():
         "msa_plan_workspace_bytes": ([i64, i64, i64, i64, i64, i64, SZ], i32),
         "msa_plan": ([P, P, P, P, i64, i64, i64, i64, i64, i64, i64, i64, i64,
                       P, ctypes.c_size_t, PL, P], i32),
+        "msa_plan_heads": ([P, i64, i64, P, P, P, i64, i64, i64, i64, i64, i64,
+                            i64, i64, i64, P, ctypes.c_size_t, PL, P], i32),
         "msa_prefill_workspace_bytes": ([i64, i64, SZ], i32),
         "msa_prefill": ([P, P, i64, f32, f32, f32, f32, P, i64, PL, P,
                          ctypes.c_size_t, P, P, P], i32),
@@ -239,27 +241,46 @@ class Plan:
 
 def msa_plan(topk, cu_seqlens_q, cu_seqlens_k, block_table, num_pages, Hq,
              total_rows, max_seqlen_q, max_seqlen_k, workspace=None,
-             stream=None) -> Plan:
+             stream=None, h_begin=None, h_count=None) -> Plan:
     """build_k2q_csr on the device.  topk int32 [T, Hkv, 16]; cu_seqlens_q/k
-    int32 [B+1]; block_table int32 [B, bt_stride]."""
+    int32 [B+1]; block_table int32 [B, bt_stride].  With h_begin / h_count
+    (msa_plan_heads) the plan covers KV heads [h_begin, h_begin + h_count) of
+    topk, and Hq is the shard's query heads."""
     _need(topk, "topk", (torch.int32,))
     _need(cu_seqlens_q, "cu_seqlens_q", (torch.int32,))
     _need(cu_seqlens_k, "cu_seqlens_k", (torch.int32,))
     _need(block_table, "block_table", (torch.int32,))
-    T, Hkv = int(topk.shape[0]), int(topk.shape[1])
     if topk.dim() != 3 or topk.shape[2] != TOPK:
         raise MsaError("topk must be [T, Hkv, 16]")
+    T, topk_hkv = int(topk.shape[0]), int(topk.shape[1])
+    sharded = h_begin is not None or h_count is not None
+    h0 = int(h_begin or 0)
+    Hkv = int(h_count) if h_count is not None else topk_hkv - h0
     B = int(cu_seqlens_q.numel()) - 1
     bt_stride = int(block_table.shape[1]) if block_table.dim() == 2 else 1
     need = plan_workspace_bytes(B, T, Hq, Hkv, total_rows, max_seqlen_q)
     ws = _workspace(need, topk.device, workspace)
     st = MsaPlanStruct()
-    _check(load().msa_plan(_ptr(topk), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
-                           _ptr(block_table), bt_stride, int(num_pages), B, T,
-                           int(Hq), Hkv, int(total_rows), int(max_seqlen_q),
-                           int(max_seqlen_k), _ptr(ws), need,
-                           ctypes.byref(st), _stream(stream)), "msa_plan")
+    args = (_ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(block_table), bt_stride,
+            int(num_pages), B, T, int(Hq), Hkv, int(total_rows),
+            int(max_seqlen_q), int(max_seqlen_k), _ptr(ws), need,
+            ctypes.byref(st), _stream(stream))
+    if sharded:
+        _check(load().msa_plan_heads(_ptr(topk), topk_hkv, h0, *args), "msa_plan_heads")
+    else:
+        _check(load().msa_plan(_ptr(topk), *args), "msa_plan")
     return Plan(st, ws, (topk, cu_seqlens_q, cu_seqlens_k, block_table))
+
+
+def head_shard(Hkv, world, rank):
+    """(h_begin, h_count): rank's contiguous share of Hkv KV heads when
+    `world` ranks split them evenly (tensor parallelism: each rank owns
+    Hkv / world KV heads and their query heads; msa_plan(h_begin=,
+    h_count=) then plans that shard)."""
+    if world < 1 or not 0 <= rank < world or Hkv % world:
+        raise MsaError("%d KV heads do not split evenly over %d ranks" % (Hkv, world))
+    n = Hkv // world
+    return rank * n, n
 
 
 def _kv_shape(kv, Hkv, fp4):

@@ -50,8 +50,11 @@ __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) {
 }
 
 // Launchers (each returns a cudaError_t from the launch).
+// topk holds topk_hkv KV heads per token; the plan covers heads
+// [h_begin, h_begin + plan.Hkv) of them.
 cudaError_t launch_plan(const msa_plan_t& plan, const int32_t* topk,
-                        const int32_t* block_table, cudaStream_t stream);
+                        const int32_t* block_table, cudaStream_t stream,
+                        int topk_hkv, int h_begin);
 
 // Split partials: per (token, query head, top-k slot) a 128-byte E4M3 row
 // in V's code units, two halves of 64 columns.  A half with a value whose

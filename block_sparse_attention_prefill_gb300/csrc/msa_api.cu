@@ -159,15 +159,22 @@ bool aligned(const void* p, size_t a) {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
 
+// topk_hkv / h_begin: the KV heads of topk's layout and the first of this
+// call's Hkv among them (a head shard; topk_hkv == Hkv, h_begin == 0 else).
 int plan_impl(const int32_t* topk, const int32_t* cu_q, const int32_t* cu_k,
               const int32_t* block_table, int64_t bt_stride, int64_t num_pages,
               int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t R,
               int64_t max_q, int64_t max_k, void* ws, size_t ws_bytes,
-              msa_plan_t* plan, cudaStream_t stream) {
+              msa_plan_t* plan, cudaStream_t stream, int64_t topk_hkv = -1,
+              int64_t h_begin = 0) {
   if (!plan) return MSA_ERR_NULL;
   PlanShape s;
   int rc = plan_shape(B, T, Hq, Hkv, R, max_q, &s);
   if (rc) return rc;
+  if (topk_hkv < 0) topk_hkv = Hkv;
+  if (h_begin < 0 || h_begin + Hkv > topk_hkv || topk_hkv > 127 ||
+      T * topk_hkv >= kI32Max / kTopK)
+    return MSA_ERR_SHAPE;
   if (max_k < 0 || max_k > kI32Max || num_pages < 0 || bt_stride < 0 ||
       max_q > max_k)
     return MSA_ERR_SHAPE;
@@ -199,7 +206,7 @@ int plan_impl(const int32_t* topk, const int32_t* cu_q, const int32_t* cu_k,
   plan->cu_seqlens_q = cu_q;
   plan->cu_seqlens_k = cu_k;
   plan_layout(s, ws, plan);
-  return cuda_rc(launch_plan(*plan, topk, block_table, stream));
+  return cuda_rc(launch_plan(*plan, topk, block_table, stream, (int)topk_hkv, (int)h_begin));
 }
 
 int attention_impl(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
@@ -391,6 +398,18 @@ int msa_plan(const int32_t* topk, const int32_t* cu_seqlens_q,
                    num_pages, B, T, Hq, Hkv, total_rows, max_seqlen_q,
                    max_seqlen_k, workspace, workspace_bytes, plan,
                    static_cast<cudaStream_t>(stream));
+}
+
+int msa_plan_heads(const int32_t* topk, int64_t topk_hkv, int64_t h_begin,
+                   const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                   const int32_t* block_table, int64_t bt_stride, int64_t num_pages,
+                   int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t total_rows,
+                   int64_t max_seqlen_q, int64_t max_seqlen_k, void* workspace,
+                   size_t workspace_bytes, msa_plan_t* plan, void* stream) {
+  return plan_impl(topk, cu_seqlens_q, cu_seqlens_k, block_table, bt_stride,
+                   num_pages, B, T, Hq, Hkv, total_rows, max_seqlen_q,
+                   max_seqlen_k, workspace, workspace_bytes, plan,
+                   static_cast<cudaStream_t>(stream), topk_hkv, h_begin);
 }
 
 int msa_prefill_workspace_bytes(int64_t T, int64_t Hq, size_t* bytes) {

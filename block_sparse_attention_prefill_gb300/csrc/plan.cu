@@ -90,6 +90,7 @@ struct PlanDev {
   const int32_t* block_table;
   int64_t bt_stride, num_pages;
   int B, T, Hkv, G, W, C;
+  int topk_hkv, h_begin;  // topk's KV heads, and the first of this plan's
   int64_t total_rows, rows, max_q, max_k;
   int32_t* req_off;
   uint32_t* bitmap;
@@ -160,6 +161,14 @@ __global__ void __launch_bounds__(kScanThreads) plan_prep_kernel(PlanDev d,
   }
 }
 
+// Element of topk for list w = t * Hkv + h (h among this plan's heads) and
+// position j: topk holds topk_hkv heads per token, this plan's from h_begin.
+__device__ __forceinline__ int64_t topk_index(const PlanDev& d, int64_t w, int j) {
+  if (d.topk_hkv == d.Hkv) return w * kTopK + j;
+  const int64_t t = w / d.Hkv;
+  return ((t * d.topk_hkv + d.h_begin) + (w - t * d.Hkv)) * kTopK + j;
+}
+
 struct TokenInfo {
   int b, i, pos, own, P;
   int64_t row0;
@@ -214,7 +223,7 @@ __global__ void __launch_bounds__(256) plan_mark_kernel(PlanDev d) {
   const int j = lane & (kTopK - 1);
   const bool live = e < total;
   const int64_t w = e / kTopK;
-  const int32_t p = live ? d.topk[e] : -1;
+  const int32_t p = live ? d.topk[topk_index(d, w, j)] : -1;
   const int valid_plan = d.counters[2];
   __shared__ int32_t s_cuq[kMetaCache + 1], s_cuk[kMetaCache + 1], s_off[kMetaCache + 1];
   const ReqMeta m = stage_req_meta(d, s_cuq, s_cuk, s_off);
@@ -421,7 +430,7 @@ __global__ void __launch_bounds__(kRowThreads) plan_scatter_kernel(PlanDev d) {
   const int64_t w = e / kTopK;
   const int j = (int)(e % kTopK);
   // the entry's loads go out together with the metadata's and the tiles'
-  const int32_t p = live ? d.topk[e] : -1;
+  const int32_t p = live ? d.topk[topk_index(d, w, j)] : -1;
   const uint32_t mask = live ? d.slot_mask[w] : 0u;
   const int valid_plan = d.counters[2];
   const uint64_t tv = (int)threadIdx.x < d.ntiles ? d.tile_state[threadIdx.x] : 0ull;
@@ -484,9 +493,12 @@ __global__ void __launch_bounds__(kRowThreads) plan_scatter_kernel(PlanDev d) {
 }  // namespace
 
 cudaError_t launch_plan(const msa_plan_t& pl, const int32_t* topk,
-                        const int32_t* block_table, cudaStream_t stream) {
+                        const int32_t* block_table, cudaStream_t stream,
+                        int topk_hkv, int h_begin) {
   PlanDev d;
   d.topk = topk;
+  d.topk_hkv = topk_hkv;
+  d.h_begin = h_begin;
   d.cu_q = pl.cu_seqlens_q;
   d.cu_k = pl.cu_seqlens_k;
   d.block_table = block_table;

@@ -204,6 +204,32 @@ MSA_API int msa_plan(const int32_t *topk, const int32_t *cu_seqlens_q,
              size_t workspace_bytes, msa_plan_t *plan, void *stream);
 
 /*
+ * msa_plan for one shard of KV heads: heads [h_begin, h_begin + Hkv) of a
+ * top-k tensor that holds topk_hkv KV heads per token.  Under tensor
+ * parallelism a rank owns num_attention_heads / tp_size query heads and
+ * the KV heads of its own cache ([P4] MiniMaxM3SparseMSAMetadataBuilder:
+ * num_q_heads = num_attention_heads // tp_size); the heads shard with no
+ * exchange inside the attention.  With this plan the rank passes its own
+ * tensors to msa_prefill / msa_prefill_attention / msa_prefill_combine:
+ * q [T][Hq][128] and out [T][Hq][128] hold the shard's Hq = Hkv * G query
+ * heads, the pool its Hkv KV heads.  Each shard's result is bit-identical
+ * to the same heads of one unsharded call.
+ *   topk       int32 [T][topk_hkv][16] (the whole tensor, not a copy of
+ *              the slice)
+ *   topk_hkv   KV heads in topk's layout, 1 .. 127
+ *   h_begin    first KV head of the shard; h_begin + Hkv <= topk_hkv
+ *   (the other arguments as msa_plan, Hq and Hkv those of the shard)
+ * Returns MSA_ERR_SHAPE when the head range does not fit.  Launches the same
+ * 4 kernels as msa_plan.
+ */
+MSA_API int msa_plan_heads(const int32_t *topk, int64_t topk_hkv, int64_t h_begin,
+                   const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                   const int32_t *block_table, int64_t bt_stride, int64_t num_pages,
+                   int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t total_rows,
+                   int64_t max_seqlen_q, int64_t max_seqlen_k, void *workspace,
+                   size_t workspace_bytes, msa_plan_t *plan, void *stream);
+
+/*
  * Bytes of device workspace msa_prefill() needs: the split partials,
  * T * Hq * 16 * (128 E4M3 bytes + 1 fp32), plus the V scale for the combine.
  */

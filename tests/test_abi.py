@@ -86,6 +86,14 @@ def test_host_validation_before_launch(lib):
     # misaligned workspace
     assert lib.msa_plan(fake, fake, fake, fake, 4, 8, 1, 10, 16, 2, 8, 10, 100,
                         P(4096 + 8), 1 << 30, ctypes.byref(plan), None) == 3
+    # head shard: past the end of topk's heads, negative start; a range
+    # that fits gets as far as the workspace check
+    assert lib.msa_plan_heads(fake, 2, 1, fake, fake, fake, 4, 8, 1, 10, 16, 2, 8, 10,
+                              100, fake, 1 << 30, ctypes.byref(plan), None) == 1
+    assert lib.msa_plan_heads(fake, 2, -1, fake, fake, fake, 4, 8, 1, 10, 8, 1, 8, 10,
+                              100, fake, 1 << 30, ctypes.byref(plan), None) == 1
+    assert lib.msa_plan_heads(fake, 2, 1, fake, fake, fake, 4, 8, 1, 10, 8, 1, 8, 10,
+                              100, fake, 16, ctypes.byref(plan), None) == 4
     # combine: bad split count, bad dtype
     assert lib.msa_combine(fake, 0, fake, 10, 0, fake, None, None) == 1
     assert lib.msa_combine(fake, 7, fake, 10, 4, fake, None, None) == 2
