@@ -32,7 +32,10 @@
  *   R9  score = (q . k) * softmax_scale with q = dec(Q) * q_scale,
  *       k = dec(K) * k_scale, v = dec(V) * v_scale;
  *   R11 lse is the natural log of the sum of exp(score) over attended keys;
- *   R16 keys at or past seq_len are masked.
+ *   R16 keys at or past seq_len are masked;
+ *   R24 a BF16 query ([P2] Details: the BF16-Q x FP8-K/V mode stages K/V up
+ *       to BF16; Overview: a BF16 query already carries q_scale) enters as
+ *       q = bf16(Q) * q_scale, everything else unchanged.
  */
 #include <math.h>
 #include <stdint.h>
@@ -135,6 +138,23 @@ void oracle_nvfp4_to_e4m3(const uint8_t *kv4, int64_t page_heads, uint8_t *kv8) 
     }
 }
 
+/* bfloat16: bit 15 sign, bits 14..7 exponent with bias 127, bits 6..0
+ * mantissa.  Exponent 0 holds the subnormals m * 2^-133; exponent 255 is
+ * infinity (mantissa 0) or NaN; every other code is (1 + m/128) * 2^(e-127).
+ */
+double oracle_bf16_decode(uint16_t code) {
+    const int sign = (code >> 15) & 1;
+    const int e = (code >> 7) & 0xFF;
+    const int m = code & 0x7F;
+    double v;
+    if (e == 0xFF) return m ? NAN : (sign ? -INFINITY : INFINITY);
+    if (e == 0)
+        v = ldexp((double)m, -133);
+    else
+        v = ldexp(1.0 + (double)m / 128.0, e - 127);
+    return sign ? -v : v;
+}
+
 static double g_dec[256];
 static int g_dec_ready = 0;
 
@@ -180,20 +200,22 @@ static int selected_pages(const int32_t *topk, int Hkv, int64_t t, int h,
 
 /*
  * Attention for the listed query tokens (all tokens when tokens == NULL).
- *   q      [T][Hq][128]          E4M3 codes
+ *   q      [T][Hq][128]          E4M3 codes (q16 == NULL), or
+ *   q16    [T][Hq][128]          bfloat16 codes (q == NULL; R24)
  *   kv     [num_pages][Hkv][128][256] E4M3 codes, K = bytes 0..127, V = 128..255
  *   topk   [T][Hkv][16]          logical page ids, -1 = padding
  *   block_table [B][bt_stride]
  *   out    [n][Hq][128], lse [n][Hq], nkeys [n][Hkv] (nullable)
  * Returns 0, or -1 when a listed token belongs to no request.
  */
-int oracle_attention(const uint8_t *q, const uint8_t *kv, int64_t num_pages,
-                     const int32_t *topk, const int32_t *block_table,
-                     int bt_stride, const int32_t *cu_q, const int32_t *cu_k,
-                     int B, int Hq, int Hkv, double q_scale, double k_scale,
-                     double v_scale, double softmax_scale,
-                     const int64_t *tokens, int64_t n_tokens, double *out,
-                     double *lse, int32_t *nkeys, int nthreads) {
+static int attention_rows(const uint8_t *q, const uint16_t *q16,
+                          const uint8_t *kv, int64_t num_pages,
+                          const int32_t *topk, const int32_t *block_table,
+                          int bt_stride, const int32_t *cu_q, const int32_t *cu_k,
+                          int B, int Hq, int Hkv, double q_scale, double k_scale,
+                          double v_scale, double softmax_scale,
+                          const int64_t *tokens, int64_t n_tokens, double *out,
+                          double *lse, int32_t *nkeys, int nthreads) {
     init_table();
     const int G = Hq / Hkv;
     int bad = 0;
@@ -232,8 +254,10 @@ int oracle_attention(const uint8_t *q, const uint8_t *kv, int64_t num_pages,
             const int hq = h * G + g;
             double *o = out + (n * Hq + hq) * ORACLE_D;
             double qv[ORACLE_D];
-            for (int d = 0; d < ORACLE_D; ++d)
-                qv[d] = g_dec[q[(t * Hq + hq) * ORACLE_D + d]] * q_scale;
+            for (int d = 0; d < ORACLE_D; ++d) {
+                const int64_t at = (t * Hq + hq) * ORACLE_D + d;
+                qv[d] = (q16 ? oracle_bf16_decode(q16[at]) : g_dec[q[at]]) * q_scale;
+            }
             if (nk == 0) {
                 for (int d = 0; d < ORACLE_D; ++d) o[d] = 0.0;
                 lse[n * Hq + hq] = -INFINITY;
@@ -270,6 +294,36 @@ int oracle_attention(const uint8_t *q, const uint8_t *kv, int64_t num_pages,
         }
     }
     return bad ? -1 : 0;
+}
+
+/* E4M3 query over E4M3 K/V ([P2] Overview). */
+int oracle_attention(const uint8_t *q, const uint8_t *kv, int64_t num_pages,
+                     const int32_t *topk, const int32_t *block_table,
+                     int bt_stride, const int32_t *cu_q, const int32_t *cu_k,
+                     int B, int Hq, int Hkv, double q_scale, double k_scale,
+                     double v_scale, double softmax_scale,
+                     const int64_t *tokens, int64_t n_tokens, double *out,
+                     double *lse, int32_t *nkeys, int nthreads) {
+    return attention_rows(q, NULL, kv, num_pages, topk, block_table, bt_stride,
+                          cu_q, cu_k, B, Hq, Hkv, q_scale, k_scale, v_scale,
+                          softmax_scale, tokens, n_tokens, out, lse, nkeys,
+                          nthreads);
+}
+
+/* BF16 query over E4M3 K/V ([P2] Details: the BF16-Q x FP8-K/V mode; R24). */
+int oracle_attention_bf16q(const uint16_t *q16, const uint8_t *kv,
+                           int64_t num_pages, const int32_t *topk,
+                           const int32_t *block_table, int bt_stride,
+                           const int32_t *cu_q, const int32_t *cu_k, int B,
+                           int Hq, int Hkv, double q_scale, double k_scale,
+                           double v_scale, double softmax_scale,
+                           const int64_t *tokens, int64_t n_tokens,
+                           double *out, double *lse, int32_t *nkeys,
+                           int nthreads) {
+    return attention_rows(NULL, q16, kv, num_pages, topk, block_table,
+                          bt_stride, cu_q, cu_k, B, Hq, Hkv, q_scale, k_scale,
+                          v_scale, softmax_scale, tokens, n_tokens, out, lse,
+                          nkeys, nthreads);
 }
 
 /*

@@ -54,6 +54,10 @@ def _lib_setup(lib):
                                      i32, f64, f64, f64, f64, P, i64, P, P, P,
                                      i32]
     lib.oracle_attention.restype = i32
+    lib.oracle_attention_bf16q.argtypes = lib.oracle_attention.argtypes
+    lib.oracle_attention_bf16q.restype = i32
+    lib.oracle_bf16_decode.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_decode.restype = f64
     lib.oracle_k2q_csr.argtypes = [P, P, i32, i64, P, P, i32, i32, i64, P, P,
                                    P, i64, P]
     lib.oracle_k2q_csr.restype = i64
@@ -79,6 +83,14 @@ def _ptr(a):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
+def _bf16_bits(x) -> np.ndarray:
+    """The uint16 codes of a torch bfloat16 tensor (or a uint16 array)."""
+    if hasattr(x, "detach"):
+        import torch
+        x = x.detach().cpu().contiguous().view(torch.int16).numpy()
+    return np.ascontiguousarray(np.asarray(x).view(np.uint16))
+
+
 def max_threads() -> int:
     return int(_load().oracle_max_threads())
 
@@ -90,6 +102,11 @@ def e4m3_decode(code: int) -> float:
 
 def e4m3_table() -> np.ndarray:
     return np.array([e4m3_decode(c) for c in range(256)], dtype=np.float64)
+
+
+def bf16_decode(code: int) -> float:
+    """bfloat16 decoding, from the format definition (bias 127)."""
+    return float(_load().oracle_bf16_decode(int(code) & 0xFFFF))
 
 
 def e4m3_encode(x: float) -> int:
@@ -124,12 +141,16 @@ def attention(w, tokens=None, nthreads: int = 0, lib=None):
     through block_table) with k <= pos and k < seq_len_b ([P4]: causal=True,
     seqused_k); score = (dec(Q) q_scale) . (dec(K) k_scale) * softmax_scale;
     out = softmax-weighted sum of dec(V) v_scale; lse = ln sum exp(score).
+    A workload with a BF16 query (``w.q16``, [P2] Details: the BF16-Q x
+    FP8-K/V mode) takes bf16(Q) q_scale for dec(Q) q_scale.
 
     Returns (out [n, Hq, 128], lse [n, Hq], nkeys [n, Hkv]) for the listed
     tokens (all when ``tokens`` is None).
     """
     lib = lib or _load()
-    q = _np(w.q, np.uint8)
+    q16 = getattr(w, "q16", None)
+    q = _bf16_bits(q16) if q16 is not None else _np(w.q, np.uint8)
+    fn = lib.oracle_attention_bf16q if q16 is not None else lib.oracle_attention
     # an NVFP4 workload is attended over the E4M3 pool its kernel reads; its
     # k_scale / v_scale are the global scales
     kv = nvfp4_to_e4m3(w.kv4, lib) if w.kv is None else _np(w.kv, np.uint8)
@@ -148,7 +169,7 @@ def attention(w, tokens=None, nthreads: int = 0, lib=None):
     lse = np.zeros((n, w.Hq), np.float64)
     nk = np.zeros((n, w.Hkv), np.int32)
     bt_stride = bt.shape[1] if bt.ndim == 2 else 1
-    rc = lib.oracle_attention(
+    rc = fn(
         _ptr(q), _ptr(kv), int(kv.shape[0]), _ptr(topk), _ptr(bt), bt_stride,
         _ptr(cu_q), _ptr(cu_k), w.B, w.Hq, w.Hkv, float(w.q_scale),
         float(w.k_scale), float(w.v_scale), float(w.softmax_scale),
@@ -230,14 +251,17 @@ def brute_force_attention(w):
     for every (token, query head) it walks *all* keys 0..seq_len-1 of the
     request and keeps a key when its page appears among the token's valid
     top-k entries and the key is not after the query.  E4M3 decoding here is
-    torch's float8_e4m3fn cast (a library routine), not the oracle's table."""
+    torch's float8_e4m3fn cast (a library routine), not the oracle's table;
+    a BF16 query (``w.q16``) is widened by torch's bfloat16 cast."""
     import torch
 
     def dec(x):
         t = torch.as_tensor(np.asarray(x, dtype=np.uint8))
         return t.view(torch.float8_e4m3fn).to(torch.float64).numpy()
 
-    q = dec(_np(w.q, np.uint8))
+    q16 = getattr(w, "q16", None)
+    q = (q16.to(torch.float64).numpy() if q16 is not None
+         else dec(_np(w.q, np.uint8)))
     kv = dec(_np(w.kv, np.uint8))
     topk = _np(w.topk, np.int32)
     bt = _np(w.block_table, np.int32)

@@ -37,7 +37,8 @@ def _dec_torch(codes) -> np.ndarray:
 
 def _replace(w, **kw):
     d = dict(q=w.q, kv=w.kv, topk=w.topk, block_table=w.block_table,
-             cu_q=w.cu_q, cu_k=w.cu_k, kv4=getattr(w, "kv4", None))
+             cu_q=w.cu_q, cu_k=w.cu_k, kv4=getattr(w, "kv4", None),
+             q16=getattr(w, "q16", None))
     d.update(kw)
     return workloads.Workload(w.name, list(w.q_lens), list(w.seq_lens), w.Hq,
                               w.Hkv, q_scale=w.q_scale, k_scale=w.k_scale,
@@ -49,7 +50,10 @@ def _sdpa_reference(w):
     """Dense attention via torch SDPA in float64, valid when every visible
     page of every token is selected (then the sparse key set equals the
     causal prefix)."""
-    q = torch.from_numpy(_dec_torch(w.q.numpy())) * w.q_scale
+    if w.q16 is not None:
+        q = w.q16.to(torch.float64) * w.q_scale
+    else:
+        q = torch.from_numpy(_dec_torch(w.q.numpy())) * w.q_scale
     kvf = torch.from_numpy(_dec_torch(w.kv.numpy()))
     G = w.G
     outs = []
@@ -421,6 +425,46 @@ def check_nvfp4(lib):
     assert np.array_equal(out, want)
 
 
+def check_bf16(lib):
+    """All 65536 bfloat16 codes decode like torch's bfloat16 -> float64 cast
+    (NaN codes to NaN, signed zeros and infinities included)."""
+    codes = np.arange(65536, dtype=np.uint32)
+    ours = np.array([lib.oracle_bf16_decode(int(c)) for c in codes])
+    ref = torch.from_numpy(codes.astype(np.int32).astype(np.int16)).view(
+        torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    m = ~np.isnan(ref)
+    assert np.array_equal(ours[m], ref[m])
+    assert np.array_equal(np.signbit(ours[m]), np.signbit(ref[m]))
+
+
+def check_bf16_query(lib):
+    """The BF16-query attention ([P2] Details: BF16-Q x FP8-K/V): (1) given
+    the E4M3 query widened to bfloat16 (exact: every E4M3 value is a
+    bfloat16 value) and the same q_scale, it returns the E4M3-query result
+    bit for bit, on a batch with invalid entries; (2) with a BF16 query of
+    N(0,1) values (not E4M3 values) and every visible page selected, it
+    equals dense causal attention by torch SDPA in float64; (3) it equals
+    the numpy brute force on tiny inputs."""
+    w = tiny_sparse_workload(3)
+    out, lse, nk = orc.attention(w, lib=lib)
+    q16 = torch.from_numpy(_dec_torch(w.q.numpy())).to(torch.bfloat16)
+    assert np.array_equal(q16.to(torch.float64).numpy(), _dec_torch(w.q.numpy()))
+    o2, l2, n2 = orc.attention(_replace(w, q=None, q16=q16), lib=lib)
+    assert np.array_equal(out, o2) and np.array_equal(lse, l2) and \
+        np.array_equal(nk, n2)
+    for wd in small_dense_workloads():
+        wb = workloads.with_bf16_query(wd, seed=4)
+        ob, _, _ = orc.attention(wb, lib=lib)
+        _close(ob, _sdpa_reference(wb), 1e-12)
+    for seed in (3, 4):
+        wb = workloads.with_bf16_query(tiny_sparse_workload(seed), seed=seed)
+        ob, lb, _ = orc.attention(wb, lib=lib)
+        bo, bl = orc.brute_force_attention(wb)
+        _close(ob, bo, 1e-12)
+        _close(lb, bl, 1e-12)
+
+
 def schedule_cases():
     """(workload, total_rows) pairs for the work-list pins: GQA groups from
     1 to 128 (chunks of 128 down to 1 token), ragged batches with two KV
@@ -483,4 +527,4 @@ def check_schedule(schedule=None):
 ALL_CHECKS = [check_e4m3, check_dense_equivalence, check_brute_force,
               check_block_table_permutation, check_padding_and_order,
               check_closed_forms, check_combine_identity, check_csr,
-              check_e4m3_encode, check_nvfp4]
+              check_e4m3_encode, check_nvfp4, check_bf16, check_bf16_query]

@@ -67,6 +67,16 @@ MUTATIONS = [
     ("NVFP4 block of 8 elements", "scales[t * (ORACLE_D / 16) + e / 16]",
      "scales[t * (ORACLE_D / 16) + e / 8 % 8]"),
     ("NVFP4 V slot written over K", "s * ORACLE_D + e] =", "0 * s + e] ="),
+    ("BF16 exponent bias 126", "ldexp(1.0 + (double)m / 128.0, e - 127)",
+     "ldexp(1.0 + (double)m / 128.0, e - 126)"),
+    ("BF16 mantissa read as 6 bits", "ldexp(1.0 + (double)m / 128.0, e - 127)",
+     "ldexp(1.0 + (double)(m & 0x3F) / 64.0, e - 127)"),
+    ("BF16 query without q_scale",
+     "qv[d] = (q16 ? oracle_bf16_decode(q16[at]) : g_dec[q[at]]) * q_scale;",
+     "qv[d] = q16 ? oracle_bf16_decode(q16[at]) : g_dec[q[at]] * q_scale;"),
+    ("BF16 query of the neighbouring head",
+     "const int64_t at = (t * Hq + hq) * ORACLE_D + d;",
+     "const int64_t at = (t * Hq + (q16 ? hq ^ 1 : hq)) * ORACLE_D + d;"),
 ]
 
 

@@ -47,7 +47,8 @@ SOFTMAX_SCALE = 1.0 / math.sqrt(HEAD_DIM)
 class Workload:
     """One batch of prefill (or decode) inputs, all in the library's layouts.
 
-    q           uint8  [T, Hq, 128]            E4M3 codes
+    q           uint8  [T, Hq, 128]            E4M3 codes (None with q16)
+    q16         bfloat16 [T, Hq, 128]          a BF16 query, or None
     kv          uint8  [num_pages, Hkv, 128, 256] E4M3 codes, K | V per token
     topk        int32  [T, Hkv, 16]            logical page ids, -1 = padding
     block_table int32  [B, bt_stride]          logical -> physical page, -1 pad
@@ -74,6 +75,9 @@ class Workload:
     # NVFP4 workload has no E4M3 pool (kv is None) and its k_scale / v_scale
     # are the global scales
     kv4: torch.Tensor = None
+    # BF16 query (torch.bfloat16 [T, Hq, 128]) of the BF16-query mode, or
+    # None; such a workload has no E4M3 query (q is None) and q_scale 1
+    q16: torch.Tensor = None
 
     @property
     def B(self) -> int:
@@ -111,7 +115,8 @@ class Workload:
     def to(self, device) -> "Workload":
         """Same workload with every tensor moved to ``device``."""
         mv = {k: (None if getattr(self, k) is None else getattr(self, k).to(device))
-              for k in ("q", "kv", "topk", "block_table", "cu_q", "cu_k", "kv4")}
+              for k in ("q", "kv", "topk", "block_table", "cu_q", "cu_k", "kv4",
+                        "q16")}
         return Workload(self.name, list(self.q_lens), list(self.seq_lens),
                         self.Hq, self.Hkv, q_scale=self.q_scale,
                         k_scale=self.k_scale, v_scale=self.v_scale,
@@ -352,9 +357,32 @@ CONFIGS = {
 }
 
 
+def with_bf16_query(w: Workload, seed: int = 0) -> Workload:
+    """The same batch with a BF16 query in place of the E4M3 one: N(0,1)
+    values rounded to bfloat16 (nearest even), drawn from a stream of their
+    own, so the real query has the scale of the E4M3 workload's
+    dec(q) * q_scale; q_scale becomes 1 and q is dropped."""
+    import dataclasses
+    qseed = int(np.random.SeedSequence([seed, 13]).generate_state(1)[0])
+    dev = w.cu_q.device
+    q16 = torch.empty((w.T, w.Hq, HEAD_DIM), dtype=torch.bfloat16, device=dev)
+    for a, b, x in _normal_chunks(qseed, (w.T, w.Hq, HEAD_DIM), str(dev)):
+        q16[a:b] = x.to(torch.bfloat16)
+    meta = dict(w.meta)
+    meta["query"] = "bf16"
+    return dataclasses.replace(w, q=None, q16=q16, q_scale=1.0, meta=meta)
+
+
 def make_config(name: str, seed: int = 0, device="cpu", kv_device=None):
     """A named workload; a name ending in "_nvfp4" is the same workload with
-    an NVFP4 page pool (the same normal draws) instead of the E4M3 one."""
+    an NVFP4 page pool (the same normal draws) instead of the E4M3 one, and
+    one ending in "_bf16q" the same workload with a BF16 query."""
+    if name.endswith("_bf16q"):
+        w = with_bf16_query(make_config(name[:-len("_bf16q")], seed, device,
+                                        kv_device), seed)
+        w.name = name
+        w.meta["description"] += "; BF16 query"
+        return w
     if name.endswith("_nvfp4"):
         w = _make_config(name[:-len("_nvfp4")], seed, device, kv_device, "nvfp4")
         w.name = name
