@@ -59,7 +59,7 @@ DECODE_KERNELS_PER_STEP = 7  # msa_decode: seq-lens prefix sums, then the same 6
 # bytes and 128 x 8 E4M3 block scales
 NVFP4_PAGE_HEAD_BYTES = 2 * (128 * 64 + 128 * 8)
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attention_kernel_traffic.json")
-ATTN_SOURCES = ["attention.cu", "ptx.cuh", "common.cuh", "nvfp4.cuh"]
+ATTN_SOURCES = ["attention.cu", "ptx.cuh", "common.cuh", "nvfp4.cuh", "partial.cuh"]
 
 
 def parse():
@@ -154,7 +154,7 @@ def algorithmic_bytes(w, unique_pages):
     """Bytes the step must move: Q once, each selected (KV head, page) once
     (E4M3: 128 x 256 bytes; NVFP4: two slots of codes and block scales),
     out bf16, the top-k ids."""
-    q = w.T * w.Hq * 128
+    q = w.T * w.Hq * 128 * (2 if is_bf16q(w) else 1)
     kv = unique_pages * (NVFP4_PAGE_HEAD_BYTES if is_nvfp4(w) else 128 * 256)
     out = w.T * w.Hq * 128 * 2
     topk = w.T * w.Hkv * 16 * 4
@@ -179,6 +179,10 @@ def source_hash(names):
 
 def is_nvfp4(w):
     return getattr(w, "kv4", None) is not None
+
+
+def is_bf16q(w):
+    return getattr(w, "q16", None) is not None
 
 
 def measured_traffic(workload):
@@ -272,10 +276,17 @@ def run_ours(args, rank, world):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     decode = is_decode(w)
     fp4 = is_nvfp4(w)
+    bf16q = is_bf16q(w)
+    if bf16q and (fp4 or decode):
+        raise SystemExit("the BF16-query mode is a prefill over the E4M3 pool")
     kv_dev = wd.kv4 if fp4 else wd.kv
     attention_fn = msa.msa_prefill_attention_nvfp4 if fp4 else msa.msa_prefill_attention
     prefill_fn = msa.msa_prefill_nvfp4 if fp4 else msa.msa_prefill
     decode_fn = msa.msa_decode_nvfp4 if fp4 else msa.msa_decode
+    if bf16q:
+        attention_fn, prefill_fn = msa.msa_prefill_attention_bf16q, msa.msa_prefill_bf16q
+    q_key = "q16" if bf16q else "q"
+    q_dev = getattr(wd, q_key)
     kv_key = "kv4" if fp4 else "kv"
     if decode:
         # decode-shaped batches go through msa_decode: n tokens at the tail
@@ -308,7 +319,7 @@ def run_ours(args, rank, world):
             plan = msa.msa_plan(wd.topk, wd.cu_q, wd.cu_k, wd.block_table,
                                 w.num_pages, w.Hq, w.total_rows, w.max_seqlen_q,
                                 w.max_seqlen_k, workspace=ws_plan, stream=st)
-            prefill_fn(wd.q, kv_dev, w.q_scale, w.k_scale, w.v_scale,
+            prefill_fn(q_dev, kv_dev, w.q_scale, w.k_scale, w.v_scale,
                        w.softmax_scale, wd.block_table, plan, workspace=ws_pre,
                        out=out, lse=lse, stream=st)
         ev[1].record(st)
@@ -323,7 +334,7 @@ def run_ours(args, rank, world):
                             w.max_seqlen_k, workspace=ws_plan, stream=st)
         if ev:
             ev[1].record(st)
-        attention_fn(wd.q, kv_dev, w.q_scale, w.k_scale, w.v_scale,
+        attention_fn(q_dev, kv_dev, w.q_scale, w.k_scale, w.v_scale,
                      w.softmax_scale, wd.block_table, plan, ws_pre, stream=st)
         if ev:
             ev[2].record(st)
@@ -398,7 +409,7 @@ def run_ours(args, rank, world):
     if not args.no_e2e:
         host = {k: getattr(w, k).cpu().pin_memory() if getattr(w, k).device.type == "cpu"
                 else getattr(w, k).cpu().pin_memory()
-                for k in ("q", kv_key, "topk", "block_table", "cu_q", "cu_k")}
+                for k in (q_key, kv_key, "topk", "block_table", "cu_q", "cu_k")}
         dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
         out_h = torch.empty((w.T, w.Hq, 128), dtype=torch.bfloat16).pin_memory()
         lse_h = torch.empty((w.T, w.Hq), dtype=torch.float32).pin_memory()
@@ -430,7 +441,7 @@ def run_ours(args, rank, world):
                              dev_in["block_table"], w.num_pages, w.Hq,
                              w.total_rows, w.max_seqlen_q, w.max_seqlen_k,
                              workspace=ws_plan, stream=stream)
-            prefill_fn(dev_in["q"], dev_in[kv_key], w.q_scale, w.k_scale,
+            prefill_fn(dev_in[q_key], dev_in[kv_key], w.q_scale, w.k_scale,
                        w.v_scale, w.softmax_scale, dev_in["block_table"],
                        p, workspace=ws_pre, out=out, lse=lse,
                        stream=stream)
@@ -571,6 +582,7 @@ def config_of(w, args):
             "T": w.T, "seq_lens": w.seq_lens if w.B <= 8 else "%d requests" % w.B,
             "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": 128, "page": 128, "topk": 16,
             "kv_cache": "nvfp4" if is_nvfp4(w) else "e4m3",
+            "query": "bf16" if is_bf16q(w) else "e4m3",
             "l2": "flushed before every timed step (256 MiB write)",
             "parallelism": "independent batch per GPU" if args.gpus > 1
             else "single GPU"}
@@ -610,9 +622,11 @@ def main():
                          "combine": r["comb_ms"] * 1e3}
             launches = KERNELS_PER_STEP * args.steps
         achieved = roof_bytes / roof_s / 1e9
-        fp8_peak = 2.0 * peaks["bf16_tflops"]
+        # the MMAs' own dtype: bf16 for the BF16 query, E4M3 (2 x the bf16
+        # rate) otherwise
+        tc_peak = peaks["bf16_tflops"] * (1.0 if is_bf16q(w) else 2.0)
         t_hbm = alg["step"] / (peaks["hbm_gbs"] * 1e9)
-        t_fp8 = flops / (fp8_peak * 1e12)
+        t_fp8 = flops / (tc_peak * 1e12)
         line = {
             "metric": METRIC,
             "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -621,7 +635,9 @@ def main():
             "us_per_layer_median": r["step_med_ms"] * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": ("nvfp4 K/V dequantised to e4m3, e4m3 Q (fp32 accumulate)"
-                      if is_nvfp4(w) else "e4m3 (fp32 accumulate)"),
+                      if is_nvfp4(w) else
+                      "bf16 Q, e4m3 K/V widened to bf16, bf16 MMAs (fp32 accumulate)"
+                      if is_bf16q(w) else "e4m3 (fp32 accumulate)"),
             "data": "synthetic",
             "config": config_of(w, args),
             "breakdown_us": breakdown,
@@ -634,8 +650,8 @@ def main():
                          "peak_source": peaks["source"] + " (burst hbm_gbs)"},
             "roofline_step": {
                 "note": "the whole per-layer step (plan + attention + "
-                        "combine) against the slower of FP8 tensor peak and "
-                        "its algorithmic bytes over HBM bandwidth",
+                        "combine) against the slower of the MMA dtype's tensor "
+                        "peak and its algorithmic bytes over HBM bandwidth",
                 "bound": "hbm" if t_hbm >= t_fp8 else "tensor",
                 "roofline_us": max(t_hbm, t_fp8) * 1e6,
                 "frac": max(t_hbm, t_fp8) / step_s,
@@ -643,8 +659,9 @@ def main():
                 "frac_vs_nominal_8tbs": max(alg["step"] / (NOMINAL_HBM_GBS * 1e9),
                                             t_fp8) / step_s,
                 "algorithmic_bytes": alg["step"], "flops": flops,
-                "fp8_peak_tflops": fp8_peak,
-                "fp8_peak_source": "2 x measured bf16 burst"},
+                "tensor_peak_tflops": tc_peak,
+                "tensor_peak_source": ("measured bf16 burst" if is_bf16q(w)
+                                       else "2 x measured bf16 burst (E4M3)")},
             "work": {"pairs": r["pairs"], "unique_kv_pages": r["upages"]},
             "gpu_launches": launches,
             "roofline_prefill": None if r["decode"] else {

@@ -101,6 +101,10 @@ def load():
         "msa_nvfp4_to_e4m3": ([P, i64, P, P], i32),
         "msa_prefill_attention_nvfp4": ([P, P, i64, f32, f32, f32, f32, P, i64,
                                          PL, P, ctypes.c_size_t, P], i32),
+        "msa_prefill_bf16q": ([P, P, i64, f32, f32, f32, f32, P, i64, PL, P,
+                               ctypes.c_size_t, P, P, P], i32),
+        "msa_prefill_attention_bf16q": ([P, P, i64, f32, f32, f32, f32, P, i64,
+                                         PL, P, ctypes.c_size_t, P], i32),
         "msa_test_set_wait_limit_ns": ([ctypes.c_uint64], i32),
         "msa_read_status": ([PL, ctypes.POINTER(ctypes.c_uint32)], i32),
         "msa_read_counters": ([PL, ctypes.POINTER(ctypes.c_int64),
@@ -345,6 +349,17 @@ def msa_prefill_nvfp4(q, kv4, q_scale, k_scale, v_scale, softmax_scale,
                     want_lse, stream)
 
 
+def msa_prefill_bf16q(q16, kv, q_scale, k_scale, v_scale, softmax_scale,
+                      block_table, plan: Plan, workspace=None, out=None,
+                      lse=None, want_lse=True, stream=None):
+    """msa_prefill with a BF16 query: q16 bf16 [T, Hq, 128] over the E4M3
+    pool (K/V widened to bf16, bf16 MMAs); q_scale multiplies the scores
+    (1.0 for a query that already carries its scale)."""
+    return _prefill("msa_prefill_bf16q", q16, kv, q_scale, k_scale, v_scale,
+                    softmax_scale, block_table, plan, workspace, out, lse,
+                    want_lse, stream)
+
+
 def msa_nvfp4_to_e4m3(kv4, out=None, stream=None):
     """NVFP4 pool -> the E4M3 pool [num_pages, Hkv, 128, 256] that the
     NVFP4 attention reads (each code times its block scale, rounded to
@@ -365,7 +380,7 @@ def msa_nvfp4_to_e4m3(kv4, out=None, stream=None):
 
 def _prefill(name, q, kv, q_scale, k_scale, v_scale, softmax_scale,
              block_table, plan, workspace, out, lse, want_lse, stream):
-    _need(q, "q", _E4M3)
+    _need(q, "q", (torch.bfloat16,) if name.endswith("bf16q") else _E4M3)
     _need(block_table, "block_table", (torch.int32,))
     s = plan.struct
     T, Hq = int(s.T), int(s.Hq)
@@ -409,10 +424,19 @@ def msa_prefill_attention_nvfp4(q, kv4, q_scale, k_scale, v_scale,
                       stream)
 
 
+def msa_prefill_attention_bf16q(q16, kv, q_scale, k_scale, v_scale,
+                                softmax_scale, block_table, plan: Plan,
+                                workspace, stream=None):
+    """The attention half of msa_prefill_bf16q."""
+    return _attention("msa_prefill_attention_bf16q", q16, kv, q_scale, k_scale,
+                      v_scale, softmax_scale, block_table, plan, workspace,
+                      stream)
+
+
 def _attention(name, q, kv, q_scale, k_scale, v_scale, softmax_scale,
                block_table, plan, workspace, stream):
     s = plan.struct
-    _need(q, "q", _E4M3)
+    _need(q, "q", (torch.bfloat16,) if name.endswith("bf16q") else _E4M3)
     _need_kv(kv, int(s.Hkv), name.endswith("nvfp4"))
     need = prefill_workspace_bytes(int(s.T), int(s.Hq))
     ws = _workspace(need, q.device, workspace)
@@ -546,7 +570,11 @@ def run_workload(w, stream=None):
     plan = msa_plan(w.topk, w.cu_q, w.cu_k, w.block_table, w.num_pages, w.Hq,
                     w.total_rows, w.max_seqlen_q, w.max_seqlen_k,
                     stream=stream)
-    if getattr(w, "kv4", None) is not None:
+    if getattr(w, "q16", None) is not None:
+        out, lse = msa_prefill_bf16q(w.q16, w.kv, w.q_scale, w.k_scale,
+                                     w.v_scale, w.softmax_scale,
+                                     w.block_table, plan, stream=stream)
+    elif getattr(w, "kv4", None) is not None:
         out, lse = msa_prefill_nvfp4(w.q, w.kv4, w.q_scale, w.k_scale,
                                      w.v_scale, w.softmax_scale,
                                      w.block_table, plan, stream=stream)

@@ -62,6 +62,7 @@
 
 #include "common.cuh"
 #include "nvfp4.cuh"
+#include "partial.cuh"
 #include "ptx.cuh"
 
 namespace msa {
@@ -220,21 +221,6 @@ __device__ __forceinline__ int div_G(int lrow, float inv_G) {
 // (unrounded) probabilities to four independent partial sums (column
 // e % 4 to l[e % 4]), so the additions form four short chains instead of
 // one long one.  Masked columns hold -inf and give 0.
-// Two floats rounded to bf16 (nearest even) in one word, the first in the
-// low half.
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// Four floats rounded to E4M3 (nearest even, saturating) in one word, the
-// first in the low byte.
-__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
-  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
-  return lo | (hi << 16);
-}
-
 __device__ __forceinline__ void exp_pack32(const uint32_t (&r)[32], int col0, float c,
                                            float off, uint8_t* prow, int row, float (&l)[4]) {
   uint32_t packed[8];
@@ -856,69 +842,10 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
           tmem_ld32(o_tmem + half * 64, ra);
           tmem_ld32(o_tmem + half * 64 + 32, rb);
           tmem_wait_ld();
-          if (valid) {
-            // The normalised row in V's code units is a convex combination
-            // of E4M3 V codes, so it stays within E4M3's range; word k holds
-            // columns 4k .. 4k+3 of this half.  A half with a code above
-            // p.e4m3_max_code (magnitude kE4M3PartialLimit, 2.0 in real
-            // units) goes to the bf16 overflow rows instead (error at most
-            // 2^-9 of the value), and its E4M3 half is filled with the NaN
-            // code, which no partial produces (the conversion saturates), as
-            // the marker the combine looks for.  So the E4M3 rounding error of
-            // a partial stays at most 2^-4 * 2.0 = 0.125 absolute however
-            // large the output, and the common case moves 64 bytes a half.
-            uint32_t o[16];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              o[k] = pack_e4m3x4(__uint_as_float(ra[4 * k]) * mt.inv,
-                                 __uint_as_float(ra[4 * k + 1]) * mt.inv,
-                                 __uint_as_float(ra[4 * k + 2]) * mt.inv,
-                                 __uint_as_float(ra[4 * k + 3]) * mt.inv);
-              o[8 + k] = pack_e4m3x4(__uint_as_float(rb[4 * k]) * mt.inv,
-                                     __uint_as_float(rb[4 * k + 1]) * mt.inv,
-                                     __uint_as_float(rb[4 * k + 2]) * mt.inv,
-                                     __uint_as_float(rb[4 * k + 3]) * mt.inv);
-            }
-            // any magnitude byte above the limit: (b & 0x7F) + (0x7F - limit)
-            // carries into bit 7 exactly when b & 0x7F exceeds the limit, and
-            // no byte carries into the next (both terms are at most 0x7F)
-            uint32_t over = 0;
-#pragma unroll
-            for (int k = 0; k < 16; ++k) over |= (o[k] & 0x7F7F7F7Fu) + p.e4m3_over4;
-            uint8_t* d = dst + half * 64;
-            if (!(over & 0x80808080u)) {
-              // 64 bytes as two whole 32-byte sectors
-              st_global_v8_hint(d, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7],
-                                pol_keep);
-              st_global_v8_hint(d + 32, o[8], o[9], o[10], o[11], o[12], o[13], o[14],
-                                o[15], pol_keep);
-            } else {
-              constexpr uint32_t kNaN4 = 0x7F7F7F7Fu;
-              st_global_v8_hint(d, kNaN4, kNaN4, kNaN4, kNaN4, kNaN4, kNaN4, kNaN4, kNaN4,
-                                pol_keep);
-              st_global_v8_hint(d + 32, kNaN4, kNaN4, kNaN4, kNaN4, kNaN4, kNaN4, kNaN4,
-                                kNaN4, pol_keep);
-              // word k holds columns 2k, 2k+1; 128 bytes as four sectors
-              uint8_t* g = p.part_big + mt.prow * (int64_t)(2 * kD) + half * 128;
-              uint32_t o[16];
-#pragma unroll
-              for (int k = 0; k < 16; ++k)
-                o[k] = pack_bf16x2(__uint_as_float(ra[2 * k]) * mt.inv,
-                                   __uint_as_float(ra[2 * k + 1]) * mt.inv);
-              st_global_v8_hint(g, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7],
-                                pol_keep);
-              st_global_v8_hint(g + 32, o[8], o[9], o[10], o[11], o[12], o[13], o[14],
-                                o[15], pol_keep);
-#pragma unroll
-              for (int k = 0; k < 16; ++k)
-                o[k] = pack_bf16x2(__uint_as_float(rb[2 * k]) * mt.inv,
-                                   __uint_as_float(rb[2 * k + 1]) * mt.inv);
-              st_global_v8_hint(g + 64, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7],
-                                pol_keep);
-              st_global_v8_hint(g + 96, o[8], o[9], o[10], o[11], o[12], o[13], o[14],
-                                o[15], pol_keep);
-            }
-          }
+          if (valid)
+            store_partial_half(ra, rb, mt.inv, dst + half * 64,
+                               p.part_big + mt.prow * (int64_t)(2 * kD) + half * 128,
+                               p.e4m3_over4, pol_keep);
         }
         if (valid) st_global_f32_hint(p.part_lse + mt.prow, mt.lse, pol_keep);
       }
@@ -936,12 +863,6 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
   }
 }
 
-// Value of a non-negative E4M3 code 0x00 .. 0x7E (OCP E4M3: bias 7,
-// subnormals m * 2^-9), for the host-side limit above.
-double e4m3_code_value(uint32_t c) {
-  const int e = (int)(c >> 3), m = (int)(c & 7);
-  return e == 0 ? std::ldexp((double)m, -9) : std::ldexp(1.0 + m / 8.0, e - 7);
-}
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                    void*, const cuuint64_t*, const cuuint64_t*,
@@ -1000,9 +921,24 @@ cudaError_t launch_kernel(const CUtensorMap& kv_map, const CUtensorMap& q_map,
 
 }  // namespace
 
+uint32_t partial_over4(float v_scale) {
+  // value of a non-negative E4M3 code 0x00 .. 0x7E (OCP E4M3: bias 7,
+  // subnormals m * 2^-9)
+  auto value = [](uint32_t c) {
+    const int e = (int)(c >> 3), m = (int)(c & 7);
+    return e == 0 ? std::ldexp((double)m, -9) : std::ldexp(1.0 + m / 8.0, e - 7);
+  };
+  const double lim = (double)kE4M3PartialLimit / (double)v_scale;
+  uint32_t c = 0;
+  while (c < 0x7E && value(c + 1) <= lim) ++c;
+  if (lim >= 448.0) c = 0x7F;
+  return (0x7Fu - c) * 0x01010101u;
+}
+
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   const msa_plan_t& pl = *a.plan;
   if (pl.max_work == 0) return cudaSuccess;
+  if (a.q_bf16) return launch_attention_bf16q(a, stream);
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const int G = (int)(pl.Hq / pl.Hkv);
@@ -1033,15 +969,7 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   p.part_vscale = a.part_vscale;
   p.part_lse = a.part_lse;
   p.part_big = a.part_big;
-  // the largest E4M3 magnitude code whose value (in V's code units) is at
-  // most kE4M3PartialLimit / v_scale; every code when that passes 448
-  {
-    const double lim = (double)kE4M3PartialLimit / (double)a.v_scale;
-    uint32_t c = 0;
-    while (c < 0x7E && e4m3_code_value(c + 1) <= lim) ++c;
-    if (lim >= 448.0) c = 0x7F;
-    p.e4m3_over4 = (0x7Fu - c) * 0x01010101u;
-  }
+  p.e4m3_over4 = partial_over4(a.v_scale);
   p.status = pl.status;
   p.Hq = (int)pl.Hq;
   p.G = G;

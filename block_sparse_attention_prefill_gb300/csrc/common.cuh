@@ -80,9 +80,13 @@ struct AttnArgs {
   int kv_format;      // MSA_KV_E4M3: kv is the E4M3 pool; MSA_KV_NVFP4: kv
                       // holds NVFP4 page-heads (nvfp4.cuh), dequantised to
                       // E4M3 in shared memory
+  int q_bf16 = 0;     // 1: q is bf16 [T][Hq][128] (E4M3 pool only)
 };
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
+// The BF16-query kernel (attention_bf16q.cu); launch_attention calls it
+// when a.q_bf16 is set.
+cudaError_t launch_attention_bf16q(const AttnArgs& a, cudaStream_t stream);
 
 // Combine over `splits` caller-given partials per row (bf16 or fp32 O,
 // [rows][splits][128], lse [rows][splits], -inf marking an empty split).

@@ -214,7 +214,7 @@ int attention_impl(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
                    float softmax_scale, const int32_t* block_table,
                    int64_t bt_stride, const msa_plan_t* plan, void* ws,
                    size_t ws_bytes, cudaStream_t stream,
-                   int kv_format = MSA_KV_E4M3) {
+                   int kv_format = MSA_KV_E4M3, bool q_bf16 = false) {
   if (!plan) return MSA_ERR_NULL;
   const int64_t T = plan->T, Hq = plan->Hq;
   if (T == 0) return MSA_OK;
@@ -240,6 +240,7 @@ int attention_impl(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
   a.bt_stride = bt_stride;
   a.plan = plan;
   a.kv_format = kv_format;
+  a.q_bf16 = q_bf16 ? 1 : 0;
   PartialBufs pb;
   prefill_layout(T, Hq, ws, &pb);
   a.part_o = pb.o;
@@ -271,14 +272,15 @@ int prefill_impl(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
                  float softmax_scale, const int32_t* block_table,
                  int64_t bt_stride, const msa_plan_t* plan, void* ws,
                  size_t ws_bytes, uint16_t* out, float* lse,
-                 cudaStream_t stream, int kv_format = MSA_KV_E4M3) {
+                 cudaStream_t stream, int kv_format = MSA_KV_E4M3,
+                 bool q_bf16 = false) {
   if (!plan) return MSA_ERR_NULL;
   if (plan->T == 0) return MSA_OK;
   if (!out) return MSA_ERR_NULL;
   if (!aligned(out, 8) || !aligned(lse, 4)) return MSA_ERR_ALIGN;
   int rc = attention_impl(q, kv, num_pages, q_scale, k_scale, v_scale,
                           softmax_scale, block_table, bt_stride, plan, ws,
-                          ws_bytes, stream, kv_format);
+                          ws_bytes, stream, kv_format, q_bf16);
   if (rc) return rc;
   return prefill_combine_impl(plan, ws, ws_bytes, out, lse, stream);
 }
@@ -475,6 +477,30 @@ int msa_prefill_attention_nvfp4(const uint8_t* q, const uint8_t* kv4,
                         softmax_scale, block_table, bt_stride, plan, workspace,
                         workspace_bytes, static_cast<cudaStream_t>(stream),
                         MSA_KV_NVFP4);
+}
+
+int msa_prefill_bf16q(const uint16_t* q16, const uint8_t* kv, int64_t num_pages,
+                      float q_scale, float k_scale, float v_scale,
+                      float softmax_scale, const int32_t* block_table,
+                      int64_t bt_stride, const msa_plan_t* plan,
+                      void* workspace, size_t workspace_bytes, uint16_t* out,
+                      float* lse, void* stream) {
+  return prefill_impl(reinterpret_cast<const uint8_t*>(q16), kv, num_pages, q_scale,
+                      k_scale, v_scale, softmax_scale, block_table, bt_stride, plan,
+                      workspace, workspace_bytes, out, lse,
+                      static_cast<cudaStream_t>(stream), MSA_KV_E4M3, true);
+}
+
+int msa_prefill_attention_bf16q(const uint16_t* q16, const uint8_t* kv,
+                                int64_t num_pages, float q_scale, float k_scale,
+                                float v_scale, float softmax_scale,
+                                const int32_t* block_table, int64_t bt_stride,
+                                const msa_plan_t* plan, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  return attention_impl(reinterpret_cast<const uint8_t*>(q16), kv, num_pages, q_scale,
+                        k_scale, v_scale, softmax_scale, block_table, bt_stride, plan,
+                        workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                        MSA_KV_E4M3, true);
 }
 
 int msa_prefill_combine(const msa_plan_t* plan, void* workspace,

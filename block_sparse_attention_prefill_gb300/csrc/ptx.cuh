@@ -214,6 +214,18 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc,
       : "memory");
 }
 
+// D[tmem] = (accumulate ? D : 0) + A[smem] * B[smem], kind::f16 (A and B
+// both bf16 here; see idesc_bf16_f32).
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when all previously issued tcgen05.mma of this thread
 // have completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -269,6 +281,14 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N,
   return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f16 with A = B = bf16 (bits 7-9 and 10-12
+// = 1), D = f32 (bits 4-5 = 1), A K-major (bit 15 = 0), B K-major or
+// MN-major (bit 16), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Per-warpgroup register budget changes (all four warps of the warpgroup

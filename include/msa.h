@@ -329,6 +329,38 @@ MSA_API int msa_prefill_attention_nvfp4(const uint8_t *q, const uint8_t *kv4,
                                         size_t workspace_bytes, void *stream);
 
 /*
+ * msa_prefill with a BF16 query ([P2] Details / "Kernel capability": the
+ * BF16-Q x FP8-K/V mode stages K/V up to BF16 and runs BF16 MMAs; Overview:
+ * the BF16 query is the E4M3 query dequantised, q_scale applied).
+ *   q16   bf16 [T][Hq][128] (uint16 codes), 16-byte aligned; q_scale still
+ *         multiplies the scores (1.0 for a query that carries its scale)
+ * Every other argument, the workspace and the outputs as in msa_prefill
+ * (E4M3 pool only).  Each selected page's K and V are widened to bf16 in
+ * shared memory (exact), QK and PV run as bf16 tensor-core MMAs with fp32
+ * accumulation, probabilities are rounded to bf16; the split partials and
+ * the combine are msa_prefill's.
+ */
+MSA_API int msa_prefill_bf16q(const uint16_t *q16, const uint8_t *kv,
+                              int64_t num_pages, float q_scale, float k_scale,
+                              float v_scale, float softmax_scale,
+                              const int32_t *block_table, int64_t bt_stride,
+                              const msa_plan_t *plan, void *workspace,
+                              size_t workspace_bytes, uint16_t *out,
+                              float *lse, void *stream);
+
+/* The attention half of msa_prefill_bf16q (see msa_prefill_attention);
+ * msa_prefill_combine() finishes it. */
+MSA_API int msa_prefill_attention_bf16q(const uint16_t *q16, const uint8_t *kv,
+                                        int64_t num_pages, float q_scale,
+                                        float k_scale, float v_scale,
+                                        float softmax_scale,
+                                        const int32_t *block_table,
+                                        int64_t bt_stride,
+                                        const msa_plan_t *plan,
+                                        void *workspace,
+                                        size_t workspace_bytes, void *stream);
+
+/*
  * Merge split partials by log-sum-exp ([P2] Performance: "combine" is the
  * third step of the per-layer call; Validation: probabilities are rounded
  * per split).  For each row r:

@@ -111,6 +111,11 @@ def test_host_validation_before_launch(lib):
     assert lib.msa_decode_nvfp4(fake, fake, 4, 1.0, 1.0, 1.0, 0.1, fake, fake,
                                 4, fake, 2, 9, 16, 2, 1000, fake, 1 << 30,
                                 fake, None, None, None) == 1
+    # BF16-query prefill and its attention half: NULL plan
+    assert lib.msa_prefill_bf16q(fake, fake, 4, 1.0, 1.0, 1.0, 0.1, fake, 4,
+                                 None, fake, 1 << 20, fake, None, None) == 6
+    assert lib.msa_prefill_attention_bf16q(fake, fake, 4, 1.0, 1.0, 1.0, 0.1, fake,
+                                           4, None, fake, 1 << 20, None) == 6
     # NVFP4 -> E4M3 staging: negative count, NULL, misaligned; zero is a no-op
     assert lib.msa_nvfp4_to_e4m3(fake, -1, fake, None) == 1
     assert lib.msa_nvfp4_to_e4m3(None, 4, fake, None) == 6
