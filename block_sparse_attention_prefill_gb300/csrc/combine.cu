@@ -101,7 +101,9 @@ combine_kernel(const TIn* __restrict__ part_o, const float* __restrict__ part_ls
 // half-warp per row, each lane owning 8 of the 128 columns: one 8-byte load
 // per slot, all of a row's loads issued before any is used, and a 16-byte
 // overflow load for a marked half.  The partials are read once here: they
-// are evicted from L2 first.
+// are evicted from L2 first.  With the weights normalised first, the sum is
+// a convex combination of values within E4M3's range, accumulated in packed
+// f16 (one conversion and one HFMA2 per pair of values).
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 combine16_kernel(const uint8_t* __restrict__ part_o,
                  const uint8_t* __restrict__ part_big,
@@ -134,17 +136,23 @@ combine16_kernel(const uint8_t* __restrict__ part_o,
   float M = l;
 #pragma unroll
   for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  const float wl = (l == -INFINITY) ? 0.f : __expf(l - M);
+  float wl = (l == -INFINITY) ? 0.f : __expf(l - M);
   float sum = wl;
 #pragma unroll
   for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  // normalised weights: the sums below stay convex combinations of the
+  // partials, within +-448 (V's code units), so they are kept in packed
+  // f16 (2^-11 relative per step, below the bf16 output's 2^-9)
+  wl *= 1.f / sum;
   // every lane runs the loops below (their shuffles span the warp); rows
   // past the end or with no partial are written after them
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  __half2 acc[4];  // columns (2u, 2u + 1) of this lane's 8
+#pragma unroll
+  for (int u = 0; u < 4; ++u) acc[u] = __float2half2_rn(0.f);
   uint32_t marked = 0;  // slots whose half (this lane's) is in the overflow rows
 #pragma unroll
   for (int j = 0; j < kTopK; ++j) {
-    const float wj = __shfl_sync(0xffffffffu, wl, (lane & 16) + j);
+    const __half2 wj = __float2half2_rn(__shfl_sync(0xffffffffu, wl, (lane & 16) + j));
     // a marked half counts here as zeros (its NaN bytes must not reach the
     // sums); its bf16 values are added below
     const bool mk = v[j].x == 0x7F7F7F7Fu;
@@ -156,12 +164,8 @@ combine16_kernel(const uint8_t* __restrict__ part_o,
           (__nv_fp8x2_storage_t)(w2[u] & 0xFFFFu), __NV_E4M3);
       const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
           (__nv_fp8x2_storage_t)(w2[u] >> 16), __NV_E4M3);
-      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
-      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
-      acc[4 * u + 0] = fmaf(wj, a.x, acc[4 * u + 0]);
-      acc[4 * u + 1] = fmaf(wj, a.y, acc[4 * u + 1]);
-      acc[4 * u + 2] = fmaf(wj, b.x, acc[4 * u + 2]);
-      acc[4 * u + 3] = fmaf(wj, b.y, acc[4 * u + 3]);
+      acc[2 * u] = __hfma2(wj, *reinterpret_cast<const __half2*>(&lo), acc[2 * u]);
+      acc[2 * u + 1] = __hfma2(wj, *reinterpret_cast<const __half2*>(&hi), acc[2 * u + 1]);
     }
   }
   // halves kept in bf16 (rare): this lane's 8 columns are 16 bytes of the
@@ -172,15 +176,16 @@ combine16_kernel(const uint8_t* __restrict__ part_o,
   marked &= mask;
   for (uint32_t bits = __reduce_or_sync(0xffffffffu, marked); bits; bits &= bits - 1) {
     const int j = __ffs(bits) - 1;
-    const float wj = __shfl_sync(0xffffffffu, wl, (lane & 16) + j);
+    const __half2 wj = __float2half2_rn(__shfl_sync(0xffffffffu, wl, (lane & 16) + j));
     if ((marked >> j) & 1u) {
       const uint4 b4 = ld_global_v4_hint(big + j * (2 * kD), pol);
       const uint32_t w4[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        acc[2 * u] = fmaf(wj, __uint_as_float(w4[u] << 16), acc[2 * u]);
-        acc[2 * u + 1] = fmaf(wj, __uint_as_float(w4[u] & 0xFFFF0000u), acc[2 * u + 1]);
-      }
+      for (int u = 0; u < 4; ++u)
+        acc[u] = __hfma2(wj,
+                         __floats2half2_rn(__uint_as_float(w4[u] << 16),
+                                           __uint_as_float(w4[u] & 0xFFFF0000u)),
+                         acc[u]);
     }
   }
   if (!live) return;
@@ -190,11 +195,12 @@ combine16_kernel(const uint8_t* __restrict__ part_o,
     if (lse_out && sub == 0) lse_out[r] = -INFINITY;
     return;
   }
-  const float inv = *v_scale_ptr / sum;
+  const float vs = *v_scale_ptr;
   uint32_t o[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * u] * inv, acc[2 * u + 1] * inv);
+    const float2 a = __half22float2(acc[u]);
+    __nv_bfloat162 h = __floats2bfloat162_rn(a.x * vs, a.y * vs);
     o[u] = *reinterpret_cast<uint32_t*>(&h);
   }
   *dst = make_uint4(o[0], o[1], o[2], o[3]);
