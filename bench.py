@@ -59,7 +59,10 @@ DECODE_KERNELS_PER_STEP = 7  # msa_decode: seq-lens prefix sums, then the same 6
 # bytes and 128 x 8 E4M3 block scales
 NVFP4_PAGE_HEAD_BYTES = 2 * (128 * 64 + 128 * 8)
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attention_kernel_traffic.json")
-ATTN_SOURCES = ["attention.cu", "ptx.cuh", "common.cuh", "nvfp4.cuh", "partial.cuh"]
+# the dominant kernel's sources, by query type: a recorded DRAM traffic
+# figure stays valid while their code is unchanged
+ATTN_SOURCES = {"e4m3": ["attention.cu", "ptx.cuh", "common.cuh", "nvfp4.cuh", "partial.cuh"],
+                "bf16": ["attention_bf16q.cu", "ptx.cuh", "common.cuh", "partial.cuh"]}
 
 
 def parse():
@@ -185,7 +188,7 @@ def is_bf16q(w):
     return getattr(w, "q16", None) is not None
 
 
-def measured_traffic(workload):
+def measured_traffic(workload, query="e4m3"):
     """dram bytes per attention launch on ``workload`` from the committed
     ncu summaries, or None when there is none for it or the kernel source
     changed since it was captured."""
@@ -194,7 +197,7 @@ def measured_traffic(workload):
             t = json.load(f)
     except (OSError, ValueError):
         return None
-    h = source_hash(ATTN_SOURCES)
+    h = source_hash(ATTN_SOURCES[query])
     for e in t if isinstance(t, list) else [t]:
         if e.get("workload") == workload and e.get("source_hash") == h:
             return e.get("bytes_per_launch")
@@ -616,8 +619,9 @@ def main():
             breakdown = {"decode": r["step_ms"] * 1e3}
             launches = DECODE_KERNELS_PER_STEP * args.steps
         else:
-            roof_bytes, roof_s, roof_kernel = alg["attention"], r["attn_ms"] / 1e3, "attention_kernel"
-            traffic = measured_traffic(w.name)
+            roof_kernel = "attention_bf16q_kernel" if is_bf16q(w) else "attention_kernel"
+            roof_bytes, roof_s = alg["attention"], r["attn_ms"] / 1e3
+            traffic = measured_traffic(w.name, "bf16" if is_bf16q(w) else "e4m3")
             breakdown = {"plan": r["plan_ms"] * 1e3, "attention": r["attn_ms"] * 1e3,
                          "combine": r["comb_ms"] * 1e3}
             launches = KERNELS_PER_STEP * args.steps

@@ -15,23 +15,23 @@
 // causal=True, page_table=block_table).  The kernel design is this
 // library's own.
 //
-// Two CTAs of four warps per SM, persistent; work items are dealt
+// Three CTAs of four warps per SM, persistent; work items are dealt
 // round-robin as in the E4M3-query kernel.  Per item, all 128 threads:
 //   1. the record into shared memory; the Q rows (256 bytes each) by
 //      cp.async into a 128 x 128 bf16 K-major tile (128-byte swizzle, two
 //      64-column blocks);
-//   2. once the page-head has landed (one 32 KB bulk copy, issued during
-//      the previous item), its K half widened into the K/V tile
-//      [128 keys][128 dims] (same layout);
+//   2. the page-head's K codes, which each thread loaded into registers
+//      during the previous item, widened into the K/V tile
+//      [128 keys][128 dims] (same layout); the V codes are loaded now;
 //   3. QK: 8 MMAs of K = 16 into S (TMEM columns 0-127);
-//   4. the V half widened into the same tile (K is dead once QK is done);
-//      the next item's page-head copy is issued; each thread takes its row
-//      of S (its TMEM lane), masks the keys after its query, and writes
-//      P = 2^(s c - m c) in bf16 over its Q row;
-//   5. PV: 8 MMAs into O (TMEM columns 128-255), V read MN-major;
+//   4. the V codes widened into the same tile (K is dead once QK is done);
+//      each thread takes its row of S (its TMEM lane), masks the keys after
+//      its query, and writes P = 2^(s c - m c) in bf16 over its Q row;
+//   5. PV: 8 MMAs into O, over the same TMEM columns as S (S is in
+//      registers by then), V read MN-major; the next item's K codes are
+//      loaded into registers while PV and the epilogue run;
 //   6. each thread normalises its O row and writes the partial.
-// The copy of the next page-head runs under steps 4-6 and the next item's
-// Q gather; the other CTA on the SM fills the MMA waits.
+// The other two CTAs on the SM fill one CTA's waits.
 #include <cuda.h>
 #include <atomic>
 #include <cuda_bf16.h>
@@ -46,25 +46,26 @@ namespace msa {
 namespace {
 
 constexpr int kThreadsB = 128;
+constexpr int kCtasPerSm = 3;
 constexpr int kBlockB = 128 * 128;          // 128 rows x 64 bf16 columns (16 KB)
 constexpr int kOffKV = 0;                   // K, then V: bf16 [128 keys][128 dims]
 constexpr int kOffQP = 2 * kBlockB;         // Q, then P: bf16 [128 rows][128]
-constexpr int kOffRaw = 4 * kBlockB;        // the page-head: 128 tokens x (K | V)
-constexpr int kRawBytes = kPage * 2 * kD;   // 32 KB
-constexpr int kOffRec = kOffRaw + kRawBytes;
+constexpr int kOffRec = 4 * kBlockB;
 constexpr int kOffBars = kOffRec + 16 * (1 + kTileM);
-constexpr int kTmemColsB = 256;             // S: 0-127, O: 128-255
+constexpr int kTmemColsB = 128;             // S, then O
+constexpr int kChunks = kPage * 16 / kThreadsB;  // 8-code chunks of a half per thread
 struct BarsB {
-  uint64_t raw_full;  // the page-head copy landed
   uint64_t mma;       // QK (even phases) and PV (odd phases) completed
   uint64_t mma_done;  // every MMA completed, before the CTA exits
   uint32_t tmem_base;
   int abort;
 };
 constexpr int kSmemB = kOffBars + (int)sizeof(BarsB) + 1024;
-static_assert(kOffBars % 8 == 0 && kOffRaw % 16 == 0, "alignment");
-// two CTAs per SM: 228 KB of shared memory, 1 KB of it reserved per CTA
-static_assert(2 * (kSmemB + 1024) <= 233472, "two CTAs per SM must fit");
+static_assert(kOffBars % 8 == 0, "alignment");
+// kCtasPerSm CTAs per SM: 228 KB of shared memory, 1 KB of it reserved per
+// CTA, and 512 TMEM columns
+static_assert(kCtasPerSm * (kSmemB + 1024) <= 233472, "the CTAs of an SM must fit");
+static_assert(kCtasPerSm * kTmemColsB <= 512, "tensor memory of an SM");
 
 struct ParamsB {
   const uint16_t* q16;   // bf16 [T][Hq][128]
@@ -107,31 +108,32 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
   return pack_bf16x2(f.x, f.y);
 }
 
-// One half of the page-head's 128 token rows (K at byte 0, V at byte 128 of
-// each 256-byte row), widened into the bf16 tile [128 tokens][128 dims]:
-// dims 0-63 in block 0, 64-127 in block 1, 128 bytes a row, 16-byte chunk c
-// of row t at chunk c ^ (t & 7) (the 128-byte swizzle).  Element e of the
-// 2048 8-code chunks goes to thread e % 128; a warp's loads cover two whole
-// 128-byte rows and its 16-byte stores whole rows of a block, so neither
-// has bank conflicts.  Loads of 8 chunks are issued before their stores.
-__device__ __forceinline__ void widen_half(const uint8_t* raw, int half, uint8_t* tile,
-                                           int tid) {
+// A page-head is 128 token rows of 256 bytes, K in bytes 0-127 and V in
+// 128-255.  Thread tid owns the 8-code chunks e = tid + 128 j (j < 16) of
+// each half: chunk e is codes 8 (e % 16) .. +7 of token row e / 16, so a
+// warp's loads cover two whole 128-byte half-rows.
+__device__ __forceinline__ void load_codes(const uint8_t* page, int half, int tid,
+                                           uint2 (&c)[kChunks]) {
 #pragma unroll
-  for (int j = 0; j < 16; j += 8) {
-    uint2 c8[8];
+  for (int j = 0; j < kChunks; ++j) {
+    const int e = tid + j * kThreadsB;
+    c[j] = ldg_nc_v2(page + (e >> 4) * (2 * kD) + half + (e & 15) * 8);
+  }
+}
+
+// The chunks above widened into the bf16 tile [128 tokens][128 dims]: dims
+// 0-63 in block 0, 64-127 in block 1, 128 bytes a row, 16-byte chunk c of
+// row t at chunk c ^ (t & 7) (the 128-byte swizzle).  A warp's 16-byte
+// stores cover whole rows of a block: no bank conflicts.
+__device__ __forceinline__ void store_widened(const uint2 (&c)[kChunks], uint8_t* tile,
+                                              int tid) {
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int e = tid + (j + u) * kThreadsB, t = e >> 4, c = e & 15;
-      c8[u] = *reinterpret_cast<const uint2*>(raw + t * (2 * kD) + half + c * 8);
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int e = tid + (j + u) * kThreadsB, t = e >> 4, c = e & 15;
-      const uint4 w = make_uint4(e4m3x2_to_bf16x2(c8[u].x), e4m3x2_to_bf16x2(c8[u].x >> 16),
-                                 e4m3x2_to_bf16x2(c8[u].y), e4m3x2_to_bf16x2(c8[u].y >> 16));
-      *reinterpret_cast<uint4*>(tile + (c >> 3) * kBlockB + t * 128 +
-                                (((c & 7) ^ (t & 7)) << 4)) = w;
-    }
+  for (int j = 0; j < kChunks; ++j) {
+    const int e = tid + j * kThreadsB, t = e >> 4, ch = e & 15;
+    const uint4 w = make_uint4(e4m3x2_to_bf16x2(c[j].x), e4m3x2_to_bf16x2(c[j].x >> 16),
+                               e4m3x2_to_bf16x2(c[j].y), e4m3x2_to_bf16x2(c[j].y >> 16));
+    *reinterpret_cast<uint4*>(tile + (ch >> 3) * kBlockB + t * 128 +
+                              (((ch & 7) ^ (t & 7)) << 4)) = w;
   }
 }
 
@@ -168,7 +170,7 @@ __device__ __forceinline__ void max_mask32(uint32_t (&r)[32], int col0, int kv_l
   }
 }
 
-__global__ void __launch_bounds__(kThreadsB, 2) attention_bf16q_kernel(const ParamsB p) {
+__global__ void __launch_bounds__(kThreadsB, kCtasPerSm) attention_bf16q_kernel(const ParamsB p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -176,7 +178,6 @@ __global__ void __launch_bounds__(kThreadsB, 2) attention_bf16q_kernel(const Par
   int4* srec = reinterpret_cast<int4*>(smem + kOffRec);
   uint8_t* kvt = smem + kOffKV;
   uint8_t* qp = smem + kOffQP;
-  const uint8_t* raw = smem + kOffRaw;
   const int tid = threadIdx.x, warp = tid >> 5;
 
   // the plan's counters and records are written by the kernels before this
@@ -192,7 +193,6 @@ __global__ void __launch_bounds__(kThreadsB, 2) attention_bf16q_kernel(const Par
   const int64_t rec_step = (int64_t)gridDim.x * p.rec_stride;
 
   if (tid == 0) {
-    mbar_init(&bars->raw_full, 1);
     mbar_init(&bars->mma, 1);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
@@ -211,16 +211,12 @@ __global__ void __launch_bounds__(kThreadsB, 2) attention_bf16q_kernel(const Par
   const int row = tid;  // tile row = TMEM lane
   const uint64_t pol_keep = l2_policy_evict_last();
 
-  // thread 0: the page-head of item li (rows of 256 bytes from the record's
-  // KV row), one bulk copy
-  int loads = 0;
-  auto load_page = [&](int li) {
-    const int4 h = grec[li * rec_step];
-    mbar_arrive_expect_tx(&bars->raw_full, kRawBytes);
-    bulk_load(smem + kOffRaw, p.kv + (int64_t)h.x * (2 * kD), kRawBytes, &bars->raw_full);
-    ++loads;
-  };
-  if (tid == 0 && cnt > 0) load_page(0);
+  // this thread's K code chunks, loaded one item ahead, and V code chunks,
+  // loaded when the item starts (a page-head is the rows of 256 bytes from
+  // the record's KV row)
+  uint2 kc[kChunks], vc[kChunks];
+  auto page_of = [&](int li) { return p.kv + (int64_t)grec[li * rec_step].x * (2 * kD); };
+  if (cnt > 0) load_codes(page_of(0), 0, tid, kc);
 
   constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
   constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, true);
@@ -229,6 +225,7 @@ __global__ void __launch_bounds__(kThreadsB, 2) attention_bf16q_kernel(const Par
     const int4* rec = grec + li * rec_step;
     const int4 hdr = rec[0];
     const int n = hdr.y;
+    load_codes(p.kv + (int64_t)hdr.x * (2 * kD), kD, tid, vc);
     for (int e = tid; e <= n; e += kThreadsB) srec[e] = rec[e];
     __syncthreads();
 
@@ -243,13 +240,8 @@ __global__ void __launch_bounds__(kThreadsB, 2) attention_bf16q_kernel(const Par
     }
     cp_async_commit();
 
-    // 2. K widened once the page-head has landed
-    bool ok = poll_wait(&bars->raw_full, li & 1, &bars->abort, p.wait_ns);
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      break;
-    }
-    widen_half(raw, 0, kvt, tid);
+    // 2. K widened (its codes were loaded during the previous item)
+    store_widened(kc, kvt, tid);
     cp_async_wait<0>();
     fence_proxy_async_smem();
     tc_fence_before();
@@ -268,7 +260,7 @@ __global__ void __launch_bounds__(kThreadsB, 2) attention_bf16q_kernel(const Par
       }
       mma_commit(&bars->mma);
     }
-    ok = poll_wait(&bars->mma, 0, &bars->abort, p.wait_ns);
+    bool ok = poll_wait(&bars->mma, 0, &bars->abort, p.wait_ns);
     if (__syncthreads_or(!ok)) {
       failed = true;
       break;
@@ -276,7 +268,7 @@ __global__ void __launch_bounds__(kThreadsB, 2) attention_bf16q_kernel(const Par
     tc_fence_after();
 
     // 4. V widened over K; the row's softmax, P over the row's Q
-    widen_half(raw, kD, kvt, tid);
+    store_widened(vc, kvt, tid);
     const int i = row / p.G, g = row - i * p.G;
     const bool valid = i < n;
     const bool warp_valid = __any_sync(0xffffffffu, valid);
@@ -289,46 +281,51 @@ __global__ void __launch_bounds__(kThreadsB, 2) attention_bf16q_kernel(const Par
     }
     float m2 = -INFINITY, l = 0.f;
     if (warp_valid) {
-      uint32_t r0[32], r1[32], r2[32], r3[32];
-      tmem_ld32(tmem + lane_off + 0, r0);
-      tmem_ld32(tmem + lane_off + 32, r1);
-      tmem_ld32(tmem + lane_off + 64, r2);
-      tmem_ld32(tmem + lane_off + 96, r3);
-      tmem_wait_ld();
+      // two passes over S in 32-column pieces (tensor memory is read twice
+      // rather than holding the row's 128 scores in registers): the
+      // maximum, then the probabilities
       float m = -INFINITY;
-      max_mask32(r0, 0, kv_lim, m);
-      max_mask32(r1, 32, kv_lim, m);
-      max_mask32(r2, 64, kv_lim, m);
-      max_mask32(r3, 96, kv_lim, m);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + c * 32, r);
+        tmem_wait_ld();
+        max_mask32(r, c * 32, kv_lim, m);
+      }
       m2 = m * p.score_log2;
       const float off = (m2 == -INFINITY) ? 0.f : -m2;
       uint8_t* prow_s = qp + row * 128;
-      exp_store32(r0, 0, p.score_log2, off, prow_s, row, l);
-      exp_store32(r1, 32, p.score_log2, off, prow_s, row, l);
-      exp_store32(r2, 64, p.score_log2, off, prow_s, row, l);
-      exp_store32(r3, 96, p.score_log2, off, prow_s, row, l);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + c * 32, r);
+        tmem_wait_ld();
+        float unused = -INFINITY;
+        max_mask32(r, c * 32, kv_lim, unused);
+        exp_store32(r, c * 32, p.score_log2, off, prow_s, row, l);
+      }
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
 
-    // 5. PV: A = P [128 rows][128 keys] K-major, B = V [128 keys][128 dims]
-    // MN-major: 16 keys per MMA are 16 rows (2 KB) further; the two
-    // 64-dim blocks are 16 KB apart (leading byte offset), groups of 8 key
-    // rows 1 KB apart (stride byte offset).  The raw page-head is free now:
-    // the next item's copy starts.
+    // 5. PV into the S columns: A = P [128 rows][128 keys] K-major, B = V
+    // [128 keys][128 dims] MN-major: 16 keys per MMA are 16 rows (2 KB)
+    // further; the two 64-dim blocks are 16 KB apart (leading byte offset),
+    // groups of 8 key rows 1 KB apart (stride byte offset)
     if (tid == 0) {
-      if (li + 1 < cnt) load_page(li + 1);
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t a_off = (uint32_t)((kk >> 2) * kBlockB + (kk & 3) * 32);
-        mma_f16(tmem + 128, smem_desc_sw128(smem_u32(qp + a_off), 16, 1024),
+        mma_f16(tmem, smem_desc_sw128(smem_u32(qp + a_off), 16, 1024),
                 smem_desc_sw128(smem_u32(kvt + kk * 16 * 128), kBlockB, 1024), idesc_pv,
                 kk > 0);
       }
       mma_commit(&bars->mma);
     }
+    // the next item's K codes: their loads run under PV and the epilogue
+    if (li + 1 < cnt) load_codes(page_of(li + 1), 0, tid, kc);
     ok = poll_wait(&bars->mma, 1, &bars->abort, p.wait_ns);
     if (__syncthreads_or(!ok)) {
       failed = true;
@@ -342,8 +339,8 @@ __global__ void __launch_bounds__(kThreadsB, 2) attention_bf16q_kernel(const Par
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         uint32_t ra[32], rb[32];
-        tmem_ld32(tmem + lane_off + 128 + half * 64, ra);
-        tmem_ld32(tmem + lane_off + 128 + half * 64 + 32, rb);
+        tmem_ld32(tmem + lane_off + half * 64, ra);
+        tmem_ld32(tmem + lane_off + half * 64 + 32, rb);
         tmem_wait_ld();
         if (valid)
           store_partial_half(ra, rb, inv, p.part_o + (int64_t)prow * kD + half * 64,
@@ -364,10 +361,8 @@ __global__ void __launch_bounds__(kThreadsB, 2) attention_bf16q_kernel(const Par
   }
   cp_async_wait<0>();
   if (tid == 0) {
-    // the last page-head copy and every MMA must complete before the CTA
-    // exits and frees its tensor memory
-    if (loads > 0)
-      bounded_wait(&bars->raw_full, (loads - 1) & 1, nullptr, kWaitLimitNs);
+    // every MMA must complete before the CTA exits and frees its tensor
+    // memory
     mma_commit(&bars->mma_done);
     bounded_wait(&bars->mma_done, 0, nullptr, kWaitLimitNs);
   }
@@ -415,7 +410,7 @@ cudaError_t launch_attention_bf16q(const AttnArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) attr_set[dev].store(true, std::memory_order_release);
   }
-  const int64_t grid = std::min<int64_t>(2 * (int64_t)num_sms(), pl.max_work);
+  const int64_t grid = std::min<int64_t>(kCtasPerSm * (int64_t)num_sms(), pl.max_work);
   return launch_pdl(attention_bf16q_kernel, dim3((unsigned)grid), dim3(kThreadsB),
                     (size_t)kSmemB, stream, p);
 }

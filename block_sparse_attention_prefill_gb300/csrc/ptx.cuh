@@ -347,6 +347,14 @@ __device__ __forceinline__ uint2 ld_global_v2_hint(const void* p, uint64_t polic
                : "l"(p), "l"(policy));
   return v;
 }
+// 8-byte load through the read-only path (data not written during the
+// kernel).
+__device__ __forceinline__ uint2 ldg_nc_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ float ld_global_f32_hint(const float* p, uint64_t policy) {
   float v;
   asm volatile("ld.global.L2::cache_hint.f32 %0, [%1], %2;"

@@ -105,8 +105,9 @@ def test_short_wait_limit_expires_and_the_next_call_is_clean():
     torch.cuda.synchronize()
     assert plan.status() == 0
     try:
-        # 300 ns: below a page-head copy, so a polling wait runs out
-        assert lib.msa_test_set_wait_limit_ns(300) == 0
+        # 1 ns: every wait for an MMA that has not completed when the clock
+        # next moves runs out
+        assert lib.msa_test_set_wait_limit_ns(1) == 0
         _, _, plan = msa.run_workload(w)
         torch.cuda.synchronize()
         assert plan.status() & msa.STATUS_TIMEOUT
