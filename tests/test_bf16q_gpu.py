@@ -21,7 +21,7 @@ def test_tiny_full_prefill_equals_dense(seed):
     assert st == 0
 
 
-@pytest.mark.parametrize("seed", range(2))
+@pytest.mark.parametrize("seed", range(16))
 def test_chunked_prefill_32k(seed):
     w = workloads.make_config("chunked_prefill_32k_bf16q", seed=seed)
     check_against_oracle(w, what="bf16q chunked seed %d" % seed)
@@ -56,6 +56,45 @@ def test_widened_e4m3_query_with_its_scale():
     wb = pins._replace(w, q=None, q16=q16)
     check_against_oracle(wb, tokens=sample_tokens(w.T, 128, seed=2),
                          what="bf16q widened")
+
+
+@pytest.mark.parametrize("seed", range(2))
+def test_mixed_decode_and_prefill_batch(seed):
+    # decode / speculative-verify requests and chunked prefills in one plan
+    # and one call, decodes first
+    w = workloads.with_bf16_query(
+        workloads.make_batch("mixed", [1, 8, 4, 8, 333, 1024],
+                             [40000, 65536, 9000, 131072, 5000, 1024], 16, 2,
+                             seed=40 + seed), seed=seed)
+    s, e, st = check_against_oracle(w, what="bf16q mixed seed %d" % seed)
+    assert st == 0
+
+
+def test_large_outputs_keep_the_acceptance_rule():
+    # outputs near +-19 (flat softmax, V codes near +-300): the partial
+    # halves above the E4M3 limit go to the bf16 overflow rows here too
+    w = workloads.with_bf16_query(pins.flat_large_v_workload(0))
+    s, e, st = check_against_oracle(w, what="bf16q large |out|")
+    assert st == 0
+
+
+def test_head_shards_equal_the_whole():
+    # the plan of each KV-head shard (msa_plan_heads) with the shard's own
+    # BF16 query and pool reproduces the unsharded result bit for bit
+    w = workloads.make_config("chunked_prefill_32k_bf16q", seed=3).to("cuda")
+    out, lse, _ = msa.run_workload(w)
+    G = w.G
+    for h0 in range(w.Hkv):
+        plan = msa.msa_plan(w.topk, w.cu_q, w.cu_k, w.block_table, w.num_pages, G,
+                            w.total_rows, w.max_seqlen_q, w.max_seqlen_k,
+                            h_begin=h0, h_count=1)
+        q = w.q16[:, h0 * G:(h0 + 1) * G].contiguous()
+        kv = w.kv[:, h0:h0 + 1].contiguous()
+        o, l = msa.msa_prefill_bf16q(q, kv, w.q_scale, w.k_scale, w.v_scale,
+                                     w.softmax_scale, w.block_table, plan)
+        torch.cuda.synchronize()
+        assert torch.equal(o, out[:, h0 * G:(h0 + 1) * G])
+        assert torch.equal(l, lse[:, h0 * G:(h0 + 1) * G])
 
 
 def test_all_padding_gives_zeros():
