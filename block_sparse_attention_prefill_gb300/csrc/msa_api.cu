@@ -182,6 +182,9 @@ int plan_impl(const int32_t* topk, const int32_t* cu_q, const int32_t* cu_k,
   if (!cu_q || !cu_k) return MSA_ERR_NULL;
   if (T > 0 && (!topk || !block_table)) return MSA_ERR_NULL;
   if (B > 0 && R > 0 && bt_stride < 1) return MSA_ERR_SHAPE;
+  // a request of max_k keys has ceil(max_k / 128) logical pages: its
+  // block_table row must hold them
+  if (B > 0 && bt_stride < ceil_div(max_k, kPage)) return MSA_ERR_SHAPE;
   if (!aligned(topk, 4) || !aligned(cu_q, 4) || !aligned(cu_k, 4) ||
       !aligned(block_table, 4))
     return MSA_ERR_ALIGN;
@@ -331,7 +334,7 @@ int decode_impl(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
   rc = plan_shape(B, B * n, Hq, Hkv, d.R, n, &s);
   if (rc) return rc;
   if (!q || !kv || !out || !topk || !block_table) return MSA_ERR_NULL;
-  if (bt_stride < 1 || num_pages < 0 ||
+  if (bt_stride < 1 || bt_stride < ceil_div(max_seqlen_k, kPage) || num_pages < 0 ||
       num_pages * Hkv * kPage >= kI32Max)
     return MSA_ERR_SHAPE;
   if (!(q_scale > 0.f) || !(k_scale > 0.f) || !(v_scale > 0.f) ||

@@ -7,7 +7,9 @@
 //
 // Four kernels, all on `stream`, no host synchronisation; each is a
 // programmatic dependent launch (its launch overlaps the tail of the kernel
-// before it on the stream, its work does not):
+// before it on the stream; on plans whose bitmap is large next to their
+// top-k entries, mark and scatter also read, before their wait, what the
+// kernels two and more before them produced):
 //   prep     CTA 0: per-request row offsets (sum of page counts), checks,
 //            status word, counters; every CTA: clears its share of the
 //            (row, token) membership bitmap
@@ -90,6 +92,7 @@ struct PlanDev {
   const int32_t* block_table;
   int64_t bt_stride, num_pages;
   int B, T, Hkv, G, W, C;
+  int early;  // 1: mark and scatter read their inputs before their wait
   int topk_hkv, h_begin;  // topk's KV heads, and the first of this plan's
   int64_t total_rows, rows, max_q, max_k;
   int32_t* req_off;
@@ -176,27 +179,15 @@ struct TokenInfo {
 
 // Per-request metadata (cu_seqlens_q, cu_seqlens_k, row offsets), copied
 // into shared memory by every CTA of the mark and scatter kernels when the
-// batch has at most kMetaCache requests, so that a thread's reads of it do
-// not add global round trips after its top-k entry; read from global memory
-// otherwise.
+// batch has fewer than kMetaCache requests, so that a thread's reads of it
+// do not add global round trips after its top-k entry; read from global
+// memory otherwise.
 constexpr int kMetaCache = 512;
 struct ReqMeta {
   const int32_t* cu_q;
   const int32_t* cu_k;
   const int32_t* req_off;
 };
-
-__device__ __forceinline__ ReqMeta stage_req_meta(const PlanDev& d, int32_t* s_cuq,
-                                                  int32_t* s_cuk, int32_t* s_off) {
-  if (d.B >= kMetaCache) return ReqMeta{d.cu_q, d.cu_k, d.req_off};
-  for (int i = threadIdx.x; i <= d.B; i += blockDim.x) {
-    s_cuq[i] = d.cu_q[i];
-    s_cuk[i] = d.cu_k[i];
-    s_off[i] = d.req_off[i];
-  }
-  __syncthreads();
-  return ReqMeta{s_cuq, s_cuk, s_off};
-}
 
 __device__ __forceinline__ TokenInfo token_info(const PlanDev& d, const ReqMeta& m,
                                                 int t, int h) {
@@ -212,21 +203,69 @@ __device__ __forceinline__ TokenInfo token_info(const PlanDev& d, const ReqMeta&
   return k;
 }
 
+// A load before the kernel's dependent-launch wait goes to L2
+// (ld.global.cg): only the wait makes earlier kernels' writes visible to
+// plain loads.  After the wait, plain loads keep the L1 hits of values that
+// many entries share (block_table entries, bitmap words).
+template <typename T>
+__device__ __forceinline__ T ld_early(const T* p, bool early) {
+  return early ? __ldcg(p) : *p;
+}
+
+// token_info without row0 (m.req_off unused): request, local index,
+// position, own page, page count.
+__device__ __forceinline__ TokenInfo token_info_noff(const PlanDev& d, const ReqMeta& m, int t) {
+  TokenInfo k;
+  k.b = upper_index(m.cu_q, d.B, t);
+  k.i = t - m.cu_q[k.b];
+  const int64_t ql = m.cu_q[k.b + 1] - m.cu_q[k.b];
+  const int64_t sl = m.cu_k[k.b + 1] - m.cu_k[k.b];
+  k.pos = (int)(sl - ql + k.i);
+  k.own = k.pos / kPage;
+  k.P = (int)ceil_div(sl, kPage);
+  k.row0 = 0;
+  return k;
+}
+
 // One thread per top-k entry (t, h, j); the 16 entries of a (t, h) list sit
 // in one half-warp and see each other through shuffles.
+//
+// This kernel starts once every prep CTA has passed its own wait, so every
+// kernel before prep on the stream (the producers of the top-k ids and of
+// cu_seqlens) is complete.  With d.early, the inputs -- the entry,
+// cu_seqlens and the block_table entry -- are read before this kernel's
+// wait, which then covers only prep's outputs (row offsets, status, the
+// cleared bitmap).
+// Reads before the wait go to L2 (ld.global.cg): the wait is what makes
+// earlier kernels' writes visible to plain loads.
 __global__ void __launch_bounds__(256) plan_mark_kernel(PlanDev d) {
-  pdl_wait();
-  pdl_trigger();
+  if (!d.early) {
+    pdl_wait();
+    pdl_trigger();
+  }
   const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t total = (int64_t)d.T * d.Hkv * kTopK;
   const int lane = threadIdx.x & 31;
   const int j = lane & (kTopK - 1);
   const bool live = e < total;
   const int64_t w = e / kTopK;
-  const int32_t p = live ? d.topk[topk_index(d, w, j)] : -1;
-  const int valid_plan = d.counters[2];
+  const int32_t p = live ? ld_early(d.topk + topk_index(d, w, j), d.early) : -1;
+  // prep's plan-valid flag: with the entry when the wait is behind us
+  int valid_plan = d.early ? 0 : d.counters[2];
   __shared__ int32_t s_cuq[kMetaCache + 1], s_cuk[kMetaCache + 1], s_off[kMetaCache + 1];
-  const ReqMeta m = stage_req_meta(d, s_cuq, s_cuk, s_off);
+  // (beyond kMetaCache requests, the metadata is read from global memory
+  // after the wait); the row offsets are prep's: staged with cu_seqlens
+  // when the wait is behind us, after it otherwise
+  const bool cache = d.B < kMetaCache;
+  if (cache) {
+    for (int i = threadIdx.x; i <= d.B; i += blockDim.x) {
+      s_cuq[i] = ld_early(d.cu_q + i, d.early);
+      s_cuk[i] = ld_early(d.cu_k + i, d.early);
+      if (!d.early) s_off[i] = d.req_off[i];
+    }
+  }
+  __syncthreads();
+  const ReqMeta m{cache ? s_cuq : d.cu_q, cache ? s_cuk : d.cu_k, cache ? s_off : d.req_off};
   // ids of the same list at positions before j
   bool dup = false;
 #pragma unroll
@@ -234,23 +273,43 @@ __global__ void __launch_bounds__(256) plan_mark_kernel(PlanDev d) {
     const int32_t o = __shfl_sync(0xffffffffu, p, (lane & ~(kTopK - 1)) + q);
     dup |= (q < j) && (o == p);
   }
+  const int t = (int)(w / d.Hkv);
+  const int h = (int)(w % d.Hkv);
+  TokenInfo k = {};
+  int32_t phys = -1;
+  if (cache && live && d.B > 0) {
+    k = token_info_noff(d, m, t);
+    // within the row and the table whatever the (not yet checked) seqlens
+    if (p >= 0 && p < k.P && p < d.bt_stride && !dup)
+      phys = ld_early(d.block_table + (int64_t)k.b * d.bt_stride + p, d.early);
+  }
+  if (d.early) {
+    pdl_wait();
+    pdl_trigger();
+    valid_plan = d.counters[2];
+    if (cache) {
+      for (int i = threadIdx.x; i <= d.B; i += blockDim.x) s_off[i] = d.req_off[i];
+      __syncthreads();
+    }
+  }
+  if (!cache && live && d.B > 0) {
+    k = token_info_noff(d, m, t);
+    if (p >= 0 && p < k.P && p < d.bt_stride && !dup)
+      phys = d.block_table[(int64_t)k.b * d.bt_stride + p];
+  }
   bool keep = false;
   if (live && valid_plan == 1) {
-    const int t = (int)(w / d.Hkv);
-    const int h = (int)(w % d.Hkv);
-    const TokenInfo k = token_info(d, m, t, h);
     unsigned st = 0;
     if (p != -1) {
       if (p < -1 || p >= k.P) {
         st |= MSA_STATUS_BAD_PAGE_ID;
       } else if (!dup) {
-        const int32_t phys = d.block_table[(int64_t)k.b * d.bt_stride + p];
         if (phys < 0 || (int64_t)phys >= d.num_pages) {
           st |= MSA_STATUS_BAD_BLOCK;
         } else if (p <= k.own) {
           keep = true;
-          atomicOr(d.bitmap + (k.row0 + p) * d.W + (k.i >> 5),
-                   1u << (k.i & 31));
+          const int64_t row0 = (int64_t)h * d.total_rows + m.req_off[k.b];
+          atomicOr(d.bitmap + (row0 + p) * d.W + (k.i >> 5), 1u << (k.i & 31));
         }
       }
     }
@@ -420,8 +479,15 @@ __global__ void __launch_bounds__(kRowThreads) plan_rows_kernel(PlanDev d) {
 // entry of each chunk of a row also writes the chunk's work item and record
 // header.
 __global__ void __launch_bounds__(kRowThreads) plan_scatter_kernel(PlanDev d) {
-  pdl_wait();
-  pdl_trigger();
+  // This kernel starts once every rows CTA has passed its own wait, so prep
+  // and mark are complete.  With d.early, the entry, its slot mask, the
+  // plan-valid flag, the request metadata, the block_table entry and the
+  // bitmap word are read before this kernel's wait (through L2:
+  // ld.global.cg), which then covers only the rows kernel's outputs.
+  if (!d.early) {
+    pdl_wait();
+    pdl_trigger();
+  }
   __shared__ uint64_t s_base[kMaxRowTiles];  // entries << 32 | work items before each tile
   __shared__ uint64_t s_warp[kRowThreads / 32];
   __shared__ int32_t s_cuq[kMetaCache + 1], s_cuk[kMetaCache + 1], s_off[kMetaCache + 1];
@@ -429,35 +495,60 @@ __global__ void __launch_bounds__(kRowThreads) plan_scatter_kernel(PlanDev d) {
   const bool live = e < (int64_t)d.T * d.Hkv * kTopK;
   const int64_t w = e / kTopK;
   const int j = (int)(e % kTopK);
-  // the entry's loads go out together with the metadata's and the tiles'
-  const int32_t p = live ? d.topk[topk_index(d, w, j)] : -1;
-  const uint32_t mask = live ? d.slot_mask[w] : 0u;
-  const int valid_plan = d.counters[2];
-  const uint64_t tv = (int)threadIdx.x < d.ntiles ? d.tile_state[threadIdx.x] : 0ull;
+  const int32_t p = live ? ld_early(d.topk + topk_index(d, w, j), d.early) : -1;
+  const uint32_t mask = live ? ld_early(d.slot_mask + w, d.early) : 0u;
+  const int valid_plan = ld_early(d.counters + 2, d.early);
   // this thread's rows of row_ptr: r0, r0 + grid threads, ... (rows < 2^31:
-  // 32-bit indices); the first one's offset is loaded here too
+  // 32-bit indices); the first one's offset is loaded with the tile totals:
+  // together with the entry when the wait is behind us, after it otherwise
   const int r0 = blockIdx.x * blockDim.x + threadIdx.x;
-  const int loc0 = r0 < (int)d.rows ? d.row_loc[2 * (int64_t)r0] : 0;
-  const ReqMeta m = stage_req_meta(d, s_cuq, s_cuk, s_off);
-  // a kept entry's second loads go out before the tiles' scan
+  uint64_t tv = 0;
+  int loc0 = 0;
+  auto tiles = [&]() {
+    tv = (int)threadIdx.x < d.ntiles ? d.tile_state[threadIdx.x] : 0ull;
+    loc0 = r0 < (int)d.rows ? d.row_loc[2 * (int64_t)r0] : 0;
+  };
+  if (!d.early) tiles();
+  const bool cache = d.B < kMetaCache;
+  if (cache) {
+    for (int i = threadIdx.x; i <= d.B; i += blockDim.x) {
+      s_cuq[i] = ld_early(d.cu_q + i, d.early);
+      s_cuk[i] = ld_early(d.cu_k + i, d.early);
+      s_off[i] = ld_early(d.req_off + i, d.early);
+    }
+  }
+  __syncthreads();
+  const ReqMeta m = cache ? ReqMeta{s_cuq, s_cuk, s_off} : ReqMeta{d.cu_q, d.cu_k, d.req_off};
   const bool kept = live && valid_plan == 1 && ((mask >> j) & 1u);
   const int t = (int)(w / d.Hkv);
   const int h = (int)(w % d.Hkv);
   TokenInfo k = {};
   int32_t phys = 0;
   int64_t r = 0, wi = 0;
-  int2 loc = make_int2(0, 0);
-  int cnt = 0, pre = 0;
   uint32_t word = 0;
-  if (kept) {
+  auto entry = [&](bool cg) {
     k = token_info(d, m, t, h);
-    phys = d.block_table[(int64_t)k.b * d.bt_stride + p];  // checked by mark
+    const int32_t* bt = d.block_table + (int64_t)k.b * d.bt_stride + p;  // checked by mark
     r = k.row0 + p;
     wi = r * d.W + (k.i >> 5);
+    phys = cg ? __ldcg(bt) : *bt;
+    word = cg ? __ldcg(d.bitmap + wi) : d.bitmap[wi];
+  };
+  if (kept && cache) entry(d.early);
+  if (d.early) {
+    pdl_wait();
+    pdl_trigger();
+    tiles();
+  }
+  if (kept && !cache) entry(false);
+  // a kept entry's loads of the rows kernel's outputs go out before the
+  // tiles' scan
+  int2 loc = make_int2(0, 0);
+  int cnt = 0, pre = 0;
+  if (kept) {
     loc = reinterpret_cast<const int2*>(d.row_loc)[r];
     cnt = d.row_cnt[r];
     pre = d.word_pre[wi];
-    word = d.bitmap[wi];
   }
   uint64_t all;
   const uint64_t tin = block_incl_scan64(tv, s_warp, &all);
@@ -520,6 +611,13 @@ cudaError_t launch_plan(const msa_plan_t& pl, const int32_t* topk,
   d.row_cnt = pl.row_cnt;
   d.row_loc = pl.row_loc;
   d.tile_state = pl.tile_state;
+  // Reading inputs before the wait pays when the kernel in front -- prep
+  // clearing the bitmap, rows scanning it -- runs long next to that early
+  // work, which grows with the top-k entries: measured on GB300, it gains
+  // 3 us on plans with 64 and more bitmap bytes per entry (1M-token
+  // prefill, decode batches) and loses 1-3 us at 10 and fewer (chunked and
+  // ragged prefills); the switch sits at 32.
+  d.early = pl.rows * pl.bitmap_words * 4 >= 32 * pl.T * pl.Hkv * (int64_t)kTopK ? 1 : 0;
   d.lane_shift = plan_row_lane_shift(pl.bitmap_words);
   d.tile_rows = (int)plan_tile_rows(pl.rows, pl.bitmap_words);
   d.ntiles = (int)ceil_div(pl.rows, d.tile_rows);

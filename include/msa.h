@@ -184,7 +184,8 @@ MSA_API int msa_plan_workspace_bytes(int64_t B, int64_t T, int64_t Hq, int64_t H
  *   cu_seqlens_k  int32 [B+1]  prefix sums of sequence lengths (cached keys
  *                 plus this chunk); request b's queries are the LAST
  *                 q_len_b positions of its seq_len_b tokens.
- *   block_table   int32 [B][bt_stride]  logical -> physical page; an entry
+ *   block_table   int32 [B][bt_stride]  logical -> physical page, bt_stride
+ *                 >= ceil(max_seqlen_k / 128) (else MSA_ERR_SHAPE); an entry
  *                 used by a valid selection must lie in [0, num_pages), else
  *                 MSA_STATUS_BAD_BLOCK is set and that selection is skipped.
  *   Hq, Hkv       query / KV heads; Hq % Hkv == 0, 1 <= Hq / Hkv <= 128.

@@ -83,6 +83,10 @@ def test_host_validation_before_launch(lib):
     # max_seqlen_q above max_seqlen_k
     assert lib.msa_plan(fake, fake, fake, fake, 4, 8, 1, 10, 16, 2, 8, 200,
                         100, fake, 1 << 30, ctypes.byref(plan), None) == 1
+    # block_table rows narrower than the pages of max_seqlen_k (300 keys: 3
+    # pages, stride 2)
+    assert lib.msa_plan(fake, fake, fake, fake, 2, 8, 1, 10, 16, 2, 8, 10, 300,
+                        fake, 1 << 30, ctypes.byref(plan), None) == 1
     # misaligned workspace
     assert lib.msa_plan(fake, fake, fake, fake, 4, 8, 1, 10, 16, 2, 8, 10, 100,
                         P(4096 + 8), 1 << 30, ctypes.byref(plan), None) == 3
