@@ -112,14 +112,17 @@ combine16_kernel(const uint8_t* __restrict__ part_o,
                  const uint16_t* __restrict__ slot_mask, int64_t group,
                  int64_t rows, uint16_t* __restrict__ out,
                  float* __restrict__ lse_out) {
-  pdl_wait();
-  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int sub = lane & 15;                 // lane within the half-warp
   const int64_t r = ((int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5)) * 2 +
                     (lane >> 4);
   const bool live = r < rows;
-  const uint32_t mask = live ? slot_mask[r / group] : 0u;
+  // The slot masks are the plan's, complete once the attention kernel has
+  // passed its own wait, which is before it let this kernel launch: read
+  // before this kernel's wait (through L2), which covers the partials.
+  const uint32_t mask = live ? __ldcg(slot_mask + r / group) : 0u;
+  pdl_wait();
+  pdl_trigger();
   const uint64_t pol = l2_policy_evict_first();
   const uint8_t* base = part_o + r * (int64_t)kTopK * kD + sub * 8;
   uint2 v[kTopK];
