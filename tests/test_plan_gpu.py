@@ -109,6 +109,37 @@ def test_plan_all_padding_and_empty_requests():
     compare_plan(w2)
 
 
+def _early_read_plan(w):
+    """True when the plan's bitmap has at least 32 bytes per top-k entry:
+    then mark and scatter read their inputs before their dependent-launch
+    wait (the library's switch, restated)."""
+    W = 4 * -(-w.max_seqlen_q // 128)
+    return w.Hkv * w.total_rows * W * 4 >= 32 * w.T * w.Hkv * 16
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_early_read_plan_with_invalid_entries(seed):
+    # few tokens over long contexts (43 bitmap bytes per entry: the early
+    # reads), with ids past the request's pages, ids below -1, repeats, a
+    # future page and a block_table entry outside the pool, as in the
+    # oracle's own pins
+    w = workloads.make_batch("early_bad", [150, 12], [300000, 150000], 8, 2, seed=30 + seed)
+    assert _early_read_plan(w)
+    tk = w.topk.clone()
+    tk[0, 0, 5] = 10**6                # past the request's 2344 pages
+    tk[1, 1, 3] = -7                   # below -1
+    tk[2, 0, 7] = tk[2, 0, 1]          # a repeat
+    tk[20, 1, 2] = tk[20, 1, 9]        # a repeat
+    tk[155, 0, 4] = 2000               # past request 1's 1172 pages
+    tk[0, 1, 8] = 2343                 # token 0 sits on page 2342: a future page
+    bt = w.block_table.clone()
+    bt[0, int(w.topk[4, 0, 6])] = -1   # a page token 4 selects: not in the pool
+    w = pins._replace(w, topk=tk, block_table=bt)
+    plan = compare_plan(w)
+    st = plan.status()
+    assert st & msa.STATUS_BAD_PAGE_ID and st & msa.STATUS_BAD_BLOCK
+
+
 def test_plan_bad_seqlens_gives_empty_plan():
     w = workloads.make_batch("bad", [64], [5000], 8, 2, seed=6)
     cu_k = w.cu_k.clone()
