@@ -189,31 +189,8 @@ struct ReqMeta {
   const int32_t* req_off;
 };
 
-__device__ __forceinline__ TokenInfo token_info(const PlanDev& d, const ReqMeta& m,
-                                                int t, int h) {
-  TokenInfo k;
-  k.b = upper_index(m.cu_q, d.B, t);
-  k.i = t - m.cu_q[k.b];
-  const int64_t ql = m.cu_q[k.b + 1] - m.cu_q[k.b];
-  const int64_t sl = m.cu_k[k.b + 1] - m.cu_k[k.b];
-  k.pos = (int)(sl - ql + k.i);
-  k.own = k.pos / kPage;
-  k.P = (int)ceil_div(sl, kPage);
-  k.row0 = (int64_t)h * d.total_rows + m.req_off[k.b];
-  return k;
-}
-
-// A load before the kernel's dependent-launch wait goes to L2
-// (ld.global.cg): only the wait makes earlier kernels' writes visible to
-// plain loads.  After the wait, plain loads keep the L1 hits of values that
-// many entries share (block_table entries, bitmap words).
-template <typename T>
-__device__ __forceinline__ T ld_early(const T* p, bool early) {
-  return early ? __ldcg(p) : *p;
-}
-
-// token_info without row0 (m.req_off unused): request, local index,
-// position, own page, page count.
+// Token t's request, index in it, position, own page and the request's
+// page count (m.req_off unused; row0 left 0).
 __device__ __forceinline__ TokenInfo token_info_noff(const PlanDev& d, const ReqMeta& m, int t) {
   TokenInfo k;
   k.b = upper_index(m.cu_q, d.B, t);
@@ -225,6 +202,24 @@ __device__ __forceinline__ TokenInfo token_info_noff(const PlanDev& d, const Req
   k.P = (int)ceil_div(sl, kPage);
   k.row0 = 0;
   return k;
+}
+
+// The same with row0, the CSR row of the token's request's page 0 for KV
+// head h.
+__device__ __forceinline__ TokenInfo token_info(const PlanDev& d, const ReqMeta& m,
+                                                int t, int h) {
+  TokenInfo k = token_info_noff(d, m, t);
+  k.row0 = (int64_t)h * d.total_rows + m.req_off[k.b];
+  return k;
+}
+
+// A load before the kernel's dependent-launch wait goes to L2
+// (ld.global.cg): only the wait makes earlier kernels' writes visible to
+// plain loads.  After the wait, plain loads keep the L1 hits of values that
+// many entries share (block_table entries, bitmap words).
+template <typename T>
+__device__ __forceinline__ T ld_early(const T* p, bool early) {
+  return early ? __ldcg(p) : *p;
 }
 
 // One thread per top-k entry (t, h, j); the 16 entries of a (t, h) list sit
