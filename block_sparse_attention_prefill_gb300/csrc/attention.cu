@@ -132,13 +132,19 @@ struct Barriers {
 //   lookup table.  A record is read until its softmax starts, which
 //   precedes the conversion of the K and V slots two items later, so a ring
 //   of min(K slots, V slots) + 2 records never overwrites one in use.
-template <bool kFp4>
+// kDepth: the E4M3 pool's V and Q/P ring depth, 5 for sparse plans and 4
+// for dense ones.  Measured on GB300 in whole steps (plan, attention and
+// combine chained): 5 is 3-4 us faster on long_prefill_1m and the 64-request
+// decode, 4 is 14-15 us faster on long_prefill_150k and the ragged batch
+// (with the attention kernel timed alone, the two are equal there); the
+// NVFP4 pool has rings of its own.
+template <bool kFp4, int kDepth>
 struct Ring {
   static constexpr int k = kFp4 ? 2 : 3;  // K tiles (free once QK is done)
-  static constexpr int v = kFp4 ? 2 : 5;  // V tiles (free once PV is done)
+  static constexpr int v = kFp4 ? 2 : kDepth;  // V tiles (free once PV is done)
   static constexpr int kraw = kFp4 ? 3 : 0;
   static constexpr int vraw = kFp4 ? 3 : 0;
-  static constexpr int q = kFp4 ? 4 : 5;  // Q/P slots: P(n) overwrites Q(n)
+  static constexpr int q = kFp4 ? 4 : kDepth;  // Q/P slots: P(n) overwrites Q(n)
   static constexpr int rec = kFp4 ? (kraw < vraw ? kraw : vraw) + 2 : v;
   static constexpr int off_k = 0;
   static constexpr int off_v = off_k + k * kTile;
@@ -299,11 +305,11 @@ __device__ __forceinline__ void convert_slot(const uint8_t* raw, uint8_t* tile,
   }
 }
 
-template <bool kFp4>
+template <bool kFp4, int kDepth>
 __global__ void __launch_bounds__(kThreads, 1)
 attention_kernel(const __grid_constant__ CUtensorMap kv_map,
                  const __grid_constant__ CUtensorMap q_map, const Params p) {
-  using L = Ring<kFp4>;
+  using L = Ring<kFp4, kDepth>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -900,7 +906,7 @@ bool encode_rows(EncodeTiledFn enc, CUtensorMap* map, const void* base,
 
 // The dynamic shared-memory limit is a per-device function attribute: set
 // it once for every device the kernel is launched on.
-template <bool kFp4>
+template <bool kFp4, int kDepth>
 cudaError_t launch_kernel(const CUtensorMap& kv_map, const CUtensorMap& q_map,
                           const Params& p, int64_t grid, cudaStream_t stream) {
   constexpr int kMaxDevices = 64;
@@ -909,14 +915,14 @@ cudaError_t launch_kernel(const CUtensorMap& kv_map, const CUtensorMap& q_map,
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices || !attr_set[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(attention_kernel<kFp4>,
+    e = cudaFuncSetAttribute(attention_kernel<kFp4, kDepth>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Ring<kFp4>::bytes);
+                             Ring<kFp4, kDepth>::bytes);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) attr_set[dev].store(true, std::memory_order_release);
   }
-  return launch_pdl(attention_kernel<kFp4>, dim3((unsigned)grid), dim3(kThreads),
-                    Ring<kFp4>::bytes, stream, kv_map, q_map, p);
+  return launch_pdl(attention_kernel<kFp4, kDepth>, dim3((unsigned)grid), dim3(kThreads),
+                    Ring<kFp4, kDepth>::bytes, stream, kv_map, q_map, p);
 }
 
 }  // namespace
@@ -981,8 +987,10 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   p.wait_ns = (uint32_t)std::min<uint64_t>(pipeline_wait_limit_ns(), kWaitLimitNs);
 
   const int64_t grid = std::min<int64_t>(num_sms(), pl.max_work);
-  return fp4 ? launch_kernel<true>(kv_map, q_map, p, grid, stream)
-             : launch_kernel<false>(kv_map, q_map, p, grid, stream);
+  if (fp4) return launch_kernel<true, 5>(kv_map, q_map, p, grid, stream);
+  return plan_is_sparse(pl.rows, pl.bitmap_words, pl.T, pl.Hkv)
+             ? launch_kernel<false, 5>(kv_map, q_map, p, grid, stream)
+             : launch_kernel<false, 4>(kv_map, q_map, p, grid, stream);
 }
 
 }  // namespace msa

@@ -38,6 +38,15 @@ __host__ __device__ inline int64_t plan_tile_rows(int64_t rows, int64_t W) {
   return tr < rp ? rp : tr;
 }
 
+// A sparse plan: its membership bitmap holds at least 32 bytes per top-k
+// entry, i.e. few tokens per selected page (long contexts, decode
+// batches).  The plan's mark and scatter kernels and the attention kernel
+// are tuned differently for sparse and dense plans (measured on GB300).
+__host__ __device__ inline bool plan_is_sparse(int64_t rows, int64_t bitmap_words, int64_t T,
+                                               int64_t Hkv) {
+  return rows * bitmap_words * 4 >= 32 * T * Hkv * kTopK;
+}
+
 // Wall-time bound of every device-side wait (about a second).
 constexpr uint32_t kWaitLimitNs = 1000000000u;
 

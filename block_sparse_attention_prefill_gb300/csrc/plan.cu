@@ -612,7 +612,7 @@ cudaError_t launch_plan(const msa_plan_t& pl, const int32_t* topk,
   // 3 us on plans with 64 and more bitmap bytes per entry (1M-token
   // prefill, decode batches) and loses 1-3 us at 10 and fewer (chunked and
   // ragged prefills); the switch sits at 32.
-  d.early = pl.rows * pl.bitmap_words * 4 >= 32 * pl.T * pl.Hkv * (int64_t)kTopK ? 1 : 0;
+  d.early = plan_is_sparse(pl.rows, pl.bitmap_words, pl.T, pl.Hkv) ? 1 : 0;
   d.lane_shift = plan_row_lane_shift(pl.bitmap_words);
   d.tile_rows = (int)plan_tile_rows(pl.rows, pl.bitmap_words);
   d.ntiles = (int)ceil_div(pl.rows, d.tile_rows);
