@@ -132,12 +132,12 @@ struct Barriers {
 //   lookup table.  A record is read until its softmax starts, which
 //   precedes the conversion of the K and V slots two items later, so a ring
 //   of min(K slots, V slots) + 2 records never overwrites one in use.
-// kDepth: the E4M3 pool's V and Q/P ring depth, 5 for sparse plans and 4
+// kDepth: the E4M3 pool's V and Q/P ring depth, 5 for sparse plans and 3
 // for dense ones.  Measured on GB300 in whole steps (plan, attention and
-// combine chained): 5 is 3-4 us faster on long_prefill_1m and the 64-request
-// decode, 4 is 14-15 us faster on long_prefill_150k and the ragged batch
-// (with the attention kernel timed alone, the two are equal there); the
-// NVFP4 pool has rings of its own.
+// combine chained): 5 is 3-4 us faster than 4 on long_prefill_1m and the
+// 64-request decode; on long_prefill_150k and the ragged batch 4 is
+// 14-15 us faster than 5 and 3 another 4-5 us faster than 4, while 2 is
+// 40 us slower; the NVFP4 pool has rings of its own.
 template <bool kFp4, int kDepth>
 struct Ring {
   static constexpr int k = kFp4 ? 2 : 3;  // K tiles (free once QK is done)
@@ -990,7 +990,7 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   if (fp4) return launch_kernel<true, 5>(kv_map, q_map, p, grid, stream);
   return plan_is_sparse(pl.rows, pl.bitmap_words, pl.T, pl.Hkv)
              ? launch_kernel<false, 5>(kv_map, q_map, p, grid, stream)
-             : launch_kernel<false, 4>(kv_map, q_map, p, grid, stream);
+             : launch_kernel<false, 3>(kv_map, q_map, p, grid, stream);
 }
 
 }  // namespace msa
