@@ -38,8 +38,9 @@
 //               code units (the combine applies v_scale), written as whole
 //               32-byte sectors
 // Shared memory (E4M3 pool): a 3-slot ring of K tiles (16 KB, released when
-// QK completes), a 5-slot ring of V tiles with the item's record (released
-// when PV completes), a 5-slot ring of Q/P tiles -- the item's Q rows,
+// QK completes), a ring of V tiles with the item's record (released when PV
+// completes) and a ring of Q/P tiles, 5 deep on sparse plans and 3 on dense
+// ones (Ring below) -- the item's Q rows,
 // which its softmax overwrites with P once QK has completed (released when
 // PV completes) -- and a ring of per-row results handed from softmax to
 // epilogue.  K leaves shared memory as soon as the scores are computed, so
