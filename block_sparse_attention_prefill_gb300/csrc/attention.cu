@@ -399,11 +399,14 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
   // caches of an SM sub-partition, so it decides how long warps stall on
   // instruction fetch (ncu: 1.60 such stalls per issue in one layout, 0.92
   // in another, for the same 47.9 M instructions).  The orders below are the
-  // fastest of those measured on GB300: E4M3 pool, softmax, epilogue, warps
-  // 2-3, producer, MMA issuer (attention on long_prefill_1m 116.8 us; 125.1
-  // us with the control warps first, 134 us with the MMA issuer leading
-  // them); NVFP4 pool, softmax, epilogue, producer, warps 2-3 (the V
-  // converter), MMA issuer (226.3 us; 231.1 us control warps first).
+  // fastest of those measured on GB300 among the admissible ones: the four
+  // control warps form one warpgroup, and setmaxnreg must be one instruction
+  // executed by all warps of a warpgroup, so they share one resize and stay
+  // together in the order.  E4M3 pool: softmax, epilogue, then warps 2-3,
+  // producer, MMA issuer (attention on long_prefill_1m 116.8 us; 125.1 us
+  // with the control warps first, 134 us with the MMA issuer leading them).
+  // NVFP4 pool: softmax, epilogue, then producer, warps 2-3 (the V
+  // converter), MMA issuer (228.5 us; 231.1 us control warps first).
   auto role_producer = [&]() {
     // ------------------------------------------------------------ producer
     // whole warp: lane 0 waits for free slots and issues the record / K / V
@@ -878,15 +881,11 @@ attention_kernel(const __grid_constant__ CUtensorMap kv_map,
       role_softmax();
     } else if (warp >= 12) {
       role_epilogue();
-    } else if (warp == 0) {
-      setmaxnreg_dec<kRegsControl>();
-      role_producer();
-    } else if (warp == 2 || warp == 3) {
-      setmaxnreg_dec<kRegsControl>();
-      role_warps23();
     } else {
       setmaxnreg_dec<kRegsControl>();
-      role_mma();
+      if (warp == 0) role_producer();
+      else if (warp >= 2) role_warps23();
+      else role_mma();
     }
   } else {
     if (warp >= 4 && warp < 12) {
