@@ -135,7 +135,8 @@ struct Barriers {
 //   of min(K slots, V slots) + 2 records never overwrites one in use.
 // kDepth: the E4M3 pool's V and Q/P ring depth, 5 for sparse plans and 3
 // for dense ones.  Measured on GB300 in whole steps (plan, attention and
-// combine chained): 5 is 3-4 us faster than 4 on long_prefill_1m and the
+// combine chained), with the warp roles in their earlier order in the code
+// (control warps first): 5 is 3-4 us faster than 4 on long_prefill_1m and the
 // 64-request decode; on long_prefill_150k and the ragged batch 4 is
 // 14-15 us faster than 5 and 3 another 4-5 us faster than 4, while 2 is
 // 40 us slower; the NVFP4 pool has rings of its own.
